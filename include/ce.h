@@ -1,0 +1,132 @@
+/*
+ * ce.h -- fused softmax cross-entropy forward + gradient on one GB300 GPU.
+ *
+ * The operation is the GPU-fused cross-entropy loss of the rumus project page
+ * (milestone M7a: log-sum-exp stabilised, with the gradient computed in the
+ * same pass as the loss), whose per-row steps are Pass 1 (Steps 1-4) of the
+ * cross_entropy.wgsl source page of rumus 0.1.1 and whose batch reduction is
+ * that page's Pass 2.  For logits z[B][C] and integer targets t[B]:
+ *
+ *   l_b       = logsumexp(z_b) - z_b[t_b]                      (per row)
+ *   *loss_out = (1/B) * sum_b l_b                               (one fp32)
+ *   grad[b][c] = (softmax(z_b)[c] - [c == t_b]) / B             ([B][C])
+ *
+ * Every entry point is plain C: device or host pointers and sizes, no
+ * framework types.  All device pointers are owned by the caller.
+ */
+#ifndef CE_H
+#define CE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of the logits and of the gradient (always the same type). */
+typedef enum {
+    CE_F32 = 0,  /* IEEE fp32                                           */
+    CE_BF16 = 1  /* bfloat16; computed in fp32, gradient rounded to nearest even */
+} ce_dtype;
+
+/* Return codes.  Host-detectable errors return before anything is launched. */
+typedef enum {
+    CE_OK = 0,
+    CE_ERR_NULL = 1,     /* a required pointer is NULL                          */
+    CE_ERR_SHAPE = 2,    /* B < 1, C < 1, B or C above 2^31-1, or bytes overflow */
+    CE_ERR_DTYPE = 3,    /* dtype is not a ce_dtype                             */
+    CE_ERR_ALIGN = 4,    /* a pointer is not aligned to its element size        */
+    CE_ERR_CUDA = 5,     /* a CUDA runtime call failed (see ce_last_cuda_error) */
+    CE_ERR_OVERLAP = 6,  /* grad_out overlaps logits, targets or loss_out       */
+    CE_ERR_POINTER = 7,  /* a pointer is not accessible from the current device */
+    CE_ERR_CAPTURE = 8,  /* the call needs to grow its workspace while the
+                            stream is being captured; call once uncaptured first */
+    CE_ERR_PATH = 9      /* a forced path/split cannot run this shape           */
+} ce_status;
+
+/* Kernel paths (for ce_fwd_bwd_path and ce_query_plan). */
+typedef enum {
+    CE_PATH_AUTO = 0,      /* let the library choose                                */
+    CE_PATH_ROWS_WARP = 1, /* small rows: one warp per row, rows staged by TMA       */
+    CE_PATH_ROW_SPLIT = 2, /* rows (or row slices across a cluster of `split` CTAs)
+                              staged once in shared memory by TMA                    */
+    CE_PATH_STREAM = 3     /* rows too large for a cluster's shared memory: chunk
+                              partials, then a recompute-and-write pass               */
+} ce_path;
+
+/*
+ * ce_fwd_bwd -- loss and gradient of softmax cross-entropy over rows.
+ *
+ *   logits    device, [B][C] row-major contiguous, element type `dtype`
+ *             (row b starts at element b*C); read only.
+ *   targets   device, [B] int32 class indices.  A target outside [0, C) is a
+ *             data error, not a launch error: that row's loss is NaN (so
+ *             *loss_out is NaN), its gradient is softmax/B with no one-hot
+ *             term, and the per-stream device error count is incremented
+ *             (read it with ce_get_device_errors).  Nothing traps.
+ *   B, C      rows and classes, 1 <= B, C <= 2^31-1.
+ *   dtype     a ce_dtype.
+ *   loss_out  device, one fp32: (1/B) * sum_b l_b.  The row losses are summed
+ *             in a fixed order, so the value is bitwise reproducible for the
+ *             same inputs on the same GPU model, whichever path runs.
+ *   grad_out  device, [B][C] row-major contiguous, element type `dtype`; must
+ *             not overlap logits, targets or loss_out.
+ *   stream    a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Pointers must be aligned to their element size (4 bytes for fp32 and
+ * int32, 2 for bf16) and accessible from the current device.  The call is
+ * asynchronous on `stream` and never synchronises, except that the first call
+ * on a stream (or the first with a larger B than before) allocates the
+ * stream's small workspace (B floats plus counters) and waits for that
+ * stream's earlier work when it has to grow it.  Calls on one stream are
+ * ordered; calls on different streams use different workspaces and may run
+ * concurrently.  Returns a ce_status.
+ */
+int ce_fwd_bwd(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
+               float *loss_out, void *grad_out, void *stream);
+
+/*
+ * ce_fwd_bwd_path -- ce_fwd_bwd with the kernel path forced (tests, tuning).
+ *   path   a ce_path; CE_PATH_AUTO behaves exactly as ce_fwd_bwd.
+ *   split  CE_PATH_ROW_SPLIT: CTAs per row (1, 2, 4 or 8; 0 = choose);
+ *          CE_PATH_STREAM: classes per chunk (multiple of 8; 0 = choose);
+ *          ignored otherwise.
+ * Returns CE_ERR_PATH when the forced path cannot hold the row in shared
+ * memory; otherwise as ce_fwd_bwd.  All paths give results within the same
+ * tolerances, and the same loss bits for the same row losses.
+ */
+int ce_fwd_bwd_path(const void *logits, const int32_t *targets, int64_t B, int64_t C,
+                    int dtype, float *loss_out, void *grad_out, void *stream, int path,
+                    int split);
+
+/*
+ * ce_query_plan -- the launch that ce_fwd_bwd would make for this shape on
+ * the current device (path, split, total CTAs, threads per CTA, dynamic shared
+ * memory per CTA, kernel launches per call).  Any output pointer may be NULL.
+ */
+int ce_query_plan(int64_t B, int64_t C, int dtype, int *path, int *split, int *ctas,
+                  int *threads, int *smem_bytes, int *launches);
+
+/*
+ * ce_get_device_errors -- read and clear the device error counters of the
+ * workspace used by `stream` on the current device: the number of rows seen
+ * with an out-of-range target, and the number of bounded waits that gave up
+ * (a copy that never completed; the kernel then skips its work and returns
+ * instead of hanging).  Synchronises `stream`.  Either output may be NULL.
+ */
+int ce_get_device_errors(void *stream, int32_t *bad_targets, int32_t *timeouts);
+
+/* Free every cached workspace of every device (after their streams are idle). */
+int ce_release_workspaces(void);
+
+/* Static text for a ce_status value. */
+const char *ce_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread in the library ("" if none). */
+const char *ce_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CE_H */

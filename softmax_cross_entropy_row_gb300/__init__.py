@@ -1,0 +1,181 @@
+"""Fused softmax cross-entropy forward + gradient on one GB300 GPU.
+
+A thin binding over the C-ABI library ``libce.so`` (declared in
+``include/ce.h``): each function marshals torch tensors into the pointers,
+sizes and stream of the C call of the same name and turns a non-zero status
+into an exception.  Every step of the computation runs in the library's
+CUDA kernels; there is no CPU fallback: every call raises ImportError when
+the library has not been built (``build()``).
+
+The operation (the rumus project page, milestone M7a; the per-row steps of
+Pass 1 and the reduction of Pass 2 of rumus 0.1.1's cross_entropy.wgsl):
+
+    loss = (1/B) * sum_b (logsumexp(z_b) - z_b[t_b])
+    grad = (softmax(z_b) - onehot(t_b)) / B
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB, build  # noqa: F401
+
+CE_F32 = 0
+CE_BF16 = 1
+
+CE_PATH_AUTO = 0
+CE_PATH_ROWS_WARP = 1
+CE_PATH_ROW_SPLIT = 2
+CE_PATH_STREAM = 3
+
+PATH_NAMES = {CE_PATH_ROWS_WARP: "rows_warp", CE_PATH_ROW_SPLIT: "row_split",
+              CE_PATH_STREAM: "stream"}
+
+STATUS = {0: "CE_OK", 1: "CE_ERR_NULL", 2: "CE_ERR_SHAPE", 3: "CE_ERR_DTYPE",
+          4: "CE_ERR_ALIGN", 5: "CE_ERR_CUDA", 6: "CE_ERR_OVERLAP", 7: "CE_ERR_POINTER",
+          8: "CE_ERR_CAPTURE", 9: "CE_ERR_PATH"}
+
+# Symbols declared in include/ce.h.
+EXPORTS = ("ce_fwd_bwd", "ce_fwd_bwd_path", "ce_query_plan", "ce_get_device_errors",
+           "ce_release_workspaces", "ce_status_string", "ce_last_cuda_error")
+
+
+class CEError(RuntimeError):
+    """A non-zero ce_status from the library."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libce.so (no CUDA call is made by loading it)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB
+    if not os.path.exists(p):
+        raise ImportError(f"{p} is missing: build it with softmax_cross_entropy_row_gb300.build()")
+    lib = ctypes.CDLL(p)
+    i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    pi = ctypes.POINTER(ctypes.c_int)
+    lib.ce_fwd_bwd.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp]
+    lib.ce_fwd_bwd.restype = ci
+    lib.ce_fwd_bwd_path.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp, ci, ci]
+    lib.ce_fwd_bwd_path.restype = ci
+    lib.ce_query_plan.argtypes = [i64, i64, ci, pi, pi, pi, pi, pi, pi]
+    lib.ce_query_plan.restype = ci
+    lib.ce_get_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_int32),
+                                         ctypes.POINTER(ctypes.c_int32)]
+    lib.ce_get_device_errors.restype = ci
+    lib.ce_release_workspaces.argtypes = []
+    lib.ce_release_workspaces.restype = ci
+    lib.ce_status_string.argtypes = [ci]
+    lib.ce_status_string.restype = ctypes.c_char_p
+    lib.ce_last_cuda_error.argtypes = []
+    lib.ce_last_cuda_error.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        lib = load_library()
+        msg = lib.ce_status_string(rc).decode()
+        if rc == 5:
+            msg += ": " + lib.ce_last_cuda_error().decode()
+        raise CEError(rc, msg)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float32:
+        return CE_F32
+    if t.dtype == torch.bfloat16:
+        return CE_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream_handle(stream) -> int:
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def ce_fwd_bwd(logits, targets, loss_out, grad_out, stream=None) -> None:
+    """Loss (one fp32 on the device) and gradient of softmax cross-entropy.
+
+    logits   [B, C] float32 or bfloat16 CUDA tensor, contiguous
+    targets  [B] int32 CUDA tensor
+    loss_out one-element float32 CUDA tensor
+    grad_out [B, C] CUDA tensor of the logits' dtype, contiguous
+    stream   torch.cuda.Stream, raw cudaStream_t int, or None (current stream)
+    """
+    ce_fwd_bwd_path(logits, targets, loss_out, grad_out, stream, CE_PATH_AUTO, 0)
+
+
+def ce_fwd_bwd_path(logits, targets, loss_out, grad_out, stream=None, path=CE_PATH_AUTO,
+                    split=0) -> None:
+    """ce_fwd_bwd with the kernel path (and split) forced."""
+    lib = load_library()
+    if logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous [B, C] tensor")
+    if grad_out.shape != logits.shape or grad_out.dtype != logits.dtype or not grad_out.is_contiguous():
+        raise ValueError("grad_out must be a contiguous tensor of the logits' shape and dtype")
+    B, C = logits.shape
+    _check(lib.ce_fwd_bwd_path(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
+                               _ptr(loss_out), _ptr(grad_out), _stream_handle(stream),
+                               int(path), int(split)))
+
+
+def ce_fwd_bwd_raw(logits_ptr: int, targets_ptr: int, B: int, C: int, dtype: int,
+                   loss_ptr: int, grad_ptr: int, stream: int = 0, path: int = CE_PATH_AUTO,
+                   split: int = 0) -> int:
+    """The C call with raw integer pointers; returns the ce_status (no raise)."""
+    return load_library().ce_fwd_bwd_path(logits_ptr, targets_ptr, B, C, dtype, loss_ptr,
+                                          grad_ptr, stream, path, split)
+
+
+def ce_query_plan(B: int, C: int, dtype: int) -> dict:
+    lib = load_library()
+    vals = [ctypes.c_int(0) for _ in range(6)]
+    _check(lib.ce_query_plan(B, C, dtype, *[ctypes.byref(v) for v in vals]))
+    path, split, ctas, threads, smem, launches = (v.value for v in vals)
+    return {"path": path, "path_name": PATH_NAMES.get(path, "?"), "split": split, "ctas": ctas,
+            "threads": threads, "smem_bytes": smem, "launches": launches}
+
+
+def ce_get_device_errors(stream=None) -> tuple[int, int]:
+    """(rows with an out-of-range target, waits that gave up) since the last read."""
+    lib = load_library()
+    bad, tmo = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib.ce_get_device_errors(_stream_handle(stream), ctypes.byref(bad), ctypes.byref(tmo)))
+    return bad.value, tmo.value
+
+
+def ce_release_workspaces() -> None:
+    _check(load_library().ce_release_workspaces())
+
+
+def cross_entropy_fwd_bwd(logits, targets, stream=None):
+    """Allocate the outputs and run ce_fwd_bwd; returns (loss [1] fp32, grad)."""
+    import torch
+
+    loss = torch.empty(1, dtype=torch.float32, device=logits.device)
+    grad = torch.empty_like(logits)
+    ce_fwd_bwd(logits, targets, loss, grad, stream)
+    return loss, grad

@@ -1,0 +1,490 @@
+// C-ABI of the fused softmax cross-entropy forward + gradient (include/ce.h):
+// argument checks, the per-stream workspace, the choice of kernel path and the
+// launch.  Nothing here computes on the host; every step runs in the kernels.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <utility>
+
+#include "../../include/ce.h"
+#include "ce_launch.h"
+
+namespace {
+
+using ce::Params;
+
+thread_local char g_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e) {
+    const char *s = cudaGetErrorString(e);
+    strncpy(g_cuda_error, s ? s : "unknown CUDA error", sizeof g_cuda_error - 1);
+    g_cuda_error[sizeof g_cuda_error - 1] = '\0';
+    return CE_ERR_CUDA;
+}
+
+// ----------------------------------------------------------- device facts
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;  // max dynamic shared memory per CTA
+    int pageable = 0;    // device can access pageable host memory
+};
+
+std::mutex g_dev_mu;
+std::map<int, DeviceInfo> g_dev;
+
+int device_info(int dev, DeviceInfo *out) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    auto it = g_dev.find(dev);
+    if (it != g_dev.end()) {
+        *out = it->second;
+        return CE_OK;
+    }
+    DeviceInfo d;
+    cudaError_t e;
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                    dev)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&d.pageable, cudaDevAttrPageableMemoryAccess, dev)) !=
+        cudaSuccess)
+        return cuda_fail(e);
+    g_dev[dev] = d;
+    *out = d;
+    return CE_OK;
+}
+
+// ---------------------------------------------------------------- plans
+
+// Occupancy answers per (device, dtype, path, split, smem), so that a call made
+// during stream capture repeats no occupancy query of an earlier call.
+std::mutex g_occ_mu;
+std::map<std::tuple<int, int, int, int, int>, int> g_occ;
+
+template <typename F>
+int cached_occupancy(int dtype, int path, int split, int smem, F query, int *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const auto key = std::make_tuple(dev, dtype, path, split, smem);
+    {
+        std::lock_guard<std::mutex> lk(g_occ_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) {
+            *out = it->second;
+            return CE_OK;
+        }
+    }
+    int v = 0;
+    if ((e = query(&v)) != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    g_occ[key] = v;
+    *out = v;
+    return CE_OK;
+}
+
+struct Plan {
+    int path = 0;
+    int split = 0;        // CTAs per row (split path) / classes per chunk (stream)
+    int ctas = 0;         // CTAs of the (main) launch
+    int threads = 0;
+    int smem = 0;         // dynamic shared memory per CTA
+    int launches = 1;
+    int nslots = 0;       // staged slices (split) or tiles per warp (warp path)
+    int slot_bytes = 0;
+    long long slice = 0;  // classes per slice (split path)
+    int rows_per_tile = 0;
+    long long chunks = 0; // stream path
+};
+
+constexpr int kStaticSmemReserve = 2048;       // static __shared__ of the kernels
+constexpr long long kWarpRowMax = 8192;        // bytes: warp-per-row path up to here
+constexpr long long kWarpTileTarget = 2048;    // bytes of rows per warp tile
+constexpr long long kSplitSliceTarget = 65536; // bytes per CTA slice when K allows
+
+int round_up(long long v, long long a) { return (int)((v + a - 1) / a * a); }
+
+int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, Plan *pl) {
+    const long long row_bytes = C * es;
+    if (row_bytes > kWarpRowMax) return CE_ERR_PATH;
+    long long R = kWarpTileTarget / row_bytes;
+    if (R < 1) R = 1;
+    if (R > B) R = B;
+    const int slot_bytes = round_up(R * row_bytes + 32, 128);
+    const int budget = d.smem_optin - kStaticSmemReserve;
+    int slots = ce::kMaxWarpSlots;
+    while (slots > 1 && (long long)slots * slot_bytes * ce::kWarpKernelWarps > budget) --slots;
+    if ((long long)slots * slot_bytes * ce::kWarpKernelWarps > budget) return CE_ERR_PATH;
+    // Smaller rings than the budget allows when all tiles fit anyway.
+    const long long ntiles = (B + R - 1) / R;
+    const int smem = slots * slot_bytes * ce::kWarpKernelWarps;
+    int per_sm = 1;
+    int rc = cached_occupancy(dtype, CE_PATH_ROWS_WARP, 0, smem,
+                              [&](int *v) { return ce::rows_warp_max_ctas_per_sm(dtype, smem, v); },
+                              &per_sm);
+    if (rc != CE_OK) return rc;
+    if (per_sm < 1) return CE_ERR_PATH;
+    long long ctas = (ntiles + ce::kWarpKernelWarps - 1) / ce::kWarpKernelWarps;
+    const long long cap = (long long)d.sms * per_sm;
+    if (ctas > cap) ctas = cap;
+    pl->path = CE_PATH_ROWS_WARP;
+    pl->split = 1;
+    pl->ctas = (int)ctas;
+    pl->threads = ce::kWarpKernelWarps * 32;
+    pl->smem = smem;
+    pl->launches = 1;
+    pl->nslots = slots;
+    pl->slot_bytes = slot_bytes;
+    pl->rows_per_tile = (int)R;
+    return CE_OK;
+}
+
+int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype, int K_forced,
+               Plan *pl) {
+    const int budget = d.smem_optin - kStaticSmemReserve;
+    auto slice_of = [&](int K) {
+        long long se = (C + K - 1) / K;
+        return (se + 7) / 8 * 8;  // slices start 16-byte aligned relative to the row
+    };
+    auto slot_of = [&](long long se) { return (long long)round_up(se * es + 32, 128); };
+    int K = K_forced;
+    if (K == 0) {
+        // Smallest cluster whose slices are at most the target size; else the
+        // smallest whose slice fits shared memory at all.
+        for (int k : {1, 2, 4, 8}) {
+            if (slot_of(slice_of(k)) <= kSplitSliceTarget + 128 && slice_of(k) > 0) {
+                K = k;
+                break;
+            }
+        }
+        if (K == 0) {
+            for (int k : {1, 2, 4, 8}) {
+                if (slot_of(slice_of(k)) <= budget) {
+                    K = k;
+                    break;
+                }
+            }
+        }
+        if (K == 0) return CE_ERR_PATH;
+    }
+    if (K != 1 && K != 2 && K != 4 && K != 8) return CE_ERR_PATH;
+    const long long se = slice_of(K);
+    const long long slot_bytes = slot_of(se);
+    if (slot_bytes > budget) return CE_ERR_PATH;
+    int nslots = (int)(budget / slot_bytes);
+    if (nslots > ce::kMaxSplitSlots) nslots = ce::kMaxSplitSlots;
+    const int smem = nslots * (int)slot_bytes;
+    int clusters = 0;
+    int rc = cached_occupancy(dtype, CE_PATH_ROW_SPLIT, K, smem,
+                              [&](int *v) { return ce::split_max_clusters(dtype, K, smem, v); },
+                              &clusters);
+    if (rc != CE_OK) return rc;
+    if (clusters < 1) return CE_ERR_PATH;
+    if ((long long)clusters > B) clusters = (int)B;
+    pl->path = CE_PATH_ROW_SPLIT;
+    pl->split = K;
+    pl->ctas = clusters * K;
+    pl->threads = ce::kSplitThreads;
+    pl->smem = smem;
+    pl->launches = 1;
+    pl->nslots = nslots;
+    pl->slot_bytes = (int)slot_bytes;
+    pl->slice = se;
+    return CE_OK;
+}
+
+int plan_stream(long long B, long long C, Plan *pl) {
+    const long long chunks = (C + ce::kStreamChunk - 1) / ce::kStreamChunk;
+    if (B * chunks > 0x7fffffffLL) return CE_ERR_SHAPE;
+    pl->path = CE_PATH_STREAM;
+    pl->split = ce::kStreamChunk;
+    pl->ctas = (int)(B * chunks);
+    pl->threads = ce::kStreamThreads;
+    pl->smem = 0;
+    pl->launches = 2;
+    pl->chunks = chunks;
+    return CE_OK;
+}
+
+int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DeviceInfo d;
+    int rc = device_info(dev, &d);
+    if (rc != CE_OK) return rc;
+    const int es = dtype == CE_F32 ? 4 : 2;
+    const long long row_bytes = C * es;
+    switch (path) {
+        case CE_PATH_AUTO:
+            if (row_bytes <= kWarpRowMax) return plan_warp(B, C, es, d, dtype, pl);
+            rc = plan_split(B, C, es, d, dtype, 0, pl);
+            if (rc == CE_ERR_PATH) return plan_stream(B, C, pl);
+            return rc;
+        case CE_PATH_ROWS_WARP: return plan_warp(B, C, es, d, dtype, pl);
+        case CE_PATH_ROW_SPLIT: return plan_split(B, C, es, d, dtype, split, pl);
+        case CE_PATH_STREAM:
+            if (split != 0 && split != ce::kStreamChunk) return CE_ERR_PATH;
+            return plan_stream(B, C, pl);
+        default: return CE_ERR_PATH;
+    }
+}
+
+// -------------------------------------------------------------- workspace
+
+// Per (device, stream): [ticket u32 | bad-target i32 | timeout i32 | pad] in
+// the first 256 bytes, then B (rounded up) fp32 row losses, then the
+// streaming path's partials.  Kernels leave the ticket at zero when they end.
+struct Workspace {
+    unsigned char *base = nullptr;
+    size_t bytes = 0;
+};
+
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+
+constexpr size_t kHeaderBytes = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int get_workspace(int dev, cudaStream_t s, size_t need, Workspace *out) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace &w = g_ws[{dev, reinterpret_cast<uintptr_t>(s)}];
+    if (w.bytes < need) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(s, &cs);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (cs != cudaStreamCaptureStatusNone) return CE_ERR_CAPTURE;
+        if (w.base) {
+            if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+            cudaFree(w.base);
+            w.base = nullptr;
+            w.bytes = 0;
+        }
+        size_t bytes = align_up(need, 1 << 16);
+        void *p = nullptr;
+        if ((e = cudaMalloc(&p, bytes)) != cudaSuccess) return cuda_fail(e);
+        // Ordered before this call's kernel on the same stream.
+        if ((e = cudaMemsetAsync(p, 0, kHeaderBytes, s)) != cudaSuccess) {
+            cudaFree(p);
+            return cuda_fail(e);
+        }
+        w.base = static_cast<unsigned char *>(p);
+        w.bytes = bytes;
+    }
+    *out = w;
+    return CE_OK;
+}
+
+// ------------------------------------------------------------- validation
+
+bool ranges_overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) {
+    return a < b + nb && b < a + na;
+}
+
+int check_pointer(const void *p, const DeviceInfo &d) {
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CE_ERR_POINTER;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return CE_OK;
+    if (at.type == cudaMemoryTypeHost && at.devicePointer != nullptr) return CE_OK;
+    if (at.type == cudaMemoryTypeUnregistered && d.pageable) return CE_OK;
+    return CE_ERR_POINTER;
+}
+
+int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
+        float *loss_out, void *grad_out, void *stream, int path, int split) {
+    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_DTYPE;
+    if (!logits || !targets || !loss_out || !grad_out) return CE_ERR_NULL;
+    if (B < 1 || C < 1 || B > 0x7fffffffLL || C > 0x7fffffffLL) return CE_ERR_SHAPE;
+    const int es = dtype == CE_F32 ? 4 : 2;
+    if ((unsigned long long)B * (unsigned long long)C > (1ull << 61) / (unsigned)es)
+        return CE_ERR_SHAPE;
+    const uintptr_t lz = reinterpret_cast<uintptr_t>(logits);
+    const uintptr_t gz = reinterpret_cast<uintptr_t>(grad_out);
+    const uintptr_t tz = reinterpret_cast<uintptr_t>(targets);
+    const uintptr_t oz = reinterpret_cast<uintptr_t>(loss_out);
+    if (lz % es || gz % es || tz % 4 || oz % 4) return CE_ERR_ALIGN;
+    const size_t nbytes = (size_t)B * (size_t)C * es;
+    if (ranges_overlap(gz, nbytes, lz, nbytes) || ranges_overlap(gz, nbytes, tz, (size_t)B * 4) ||
+        ranges_overlap(gz, nbytes, oz, 4))
+        return CE_ERR_OVERLAP;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DeviceInfo d;
+    int rc = device_info(dev, &d);
+    if (rc != CE_OK) return rc;
+    for (const void *ptr : {logits, (const void *)targets, (const void *)loss_out,
+                            (const void *)grad_out}) {
+        if ((rc = check_pointer(ptr, d)) != CE_OK) return rc;
+    }
+
+    Plan pl;
+    if ((rc = make_plan(B, C, dtype, path, split, &pl)) != CE_OK) return rc;
+
+    const size_t rows_bytes = align_up((size_t)B, 1024) * sizeof(float);
+    size_t need = kHeaderBytes + rows_bytes;
+    size_t parts_off = 0, zt_off = 0;
+    if (pl.path == CE_PATH_STREAM) {
+        parts_off = need;
+        need += align_up((size_t)B * (size_t)pl.chunks * sizeof(float2), 256);
+        zt_off = need;
+        need += align_up((size_t)B * sizeof(float), 256);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Workspace ws;
+    if ((rc = get_workspace(dev, s, need, &ws)) != CE_OK) return rc;
+
+    Params p;
+    p.logits = static_cast<const unsigned char *>(logits);
+    p.targets = targets;
+    p.grad = static_cast<unsigned char *>(grad_out);
+    p.loss_out = loss_out;
+    p.ticket = reinterpret_cast<unsigned int *>(ws.base);
+    p.err = reinterpret_cast<int *>(ws.base + 4);
+    p.loss_rows = reinterpret_cast<float *>(ws.base + kHeaderBytes);
+    p.parts = pl.path == CE_PATH_STREAM ? reinterpret_cast<float2 *>(ws.base + parts_off) : nullptr;
+    p.zt = pl.path == CE_PATH_STREAM ? reinterpret_cast<float *>(ws.base + zt_off) : nullptr;
+    p.B = B;
+    p.C = C;
+    p.inv_b = (float)(1.0 / (double)B);
+    p.lo_clip = (uint64_t)((lz + 15) & ~(uintptr_t)15);
+    p.hi_clip = (uint64_t)((lz + nbytes) & ~(uintptr_t)15);
+    if (p.hi_clip < p.lo_clip) p.hi_clip = p.lo_clip;
+    p.grad_vec_ok = ((gz - lz) % 16) == 0;
+
+    switch (pl.path) {
+        case CE_PATH_ROWS_WARP:
+            e = ce::launch_rows_warp(p, dtype, pl.ctas, pl.nslots, pl.rows_per_tile,
+                                     pl.slot_bytes, pl.smem, s);
+            break;
+        case CE_PATH_ROW_SPLIT:
+            e = ce::launch_split(p, dtype, pl.split, pl.ctas, pl.nslots, pl.slot_bytes, pl.slice,
+                                 pl.smem, s);
+            break;
+        default:
+            e = ce::launch_stream(p, dtype, pl.chunks, s);
+            break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CE_OK;
+}
+
+}  // namespace
+
+namespace ce {
+
+cudaError_t ensure_smem_attr(const void *func, int smem) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, int> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    int &have = done[{dev, func}];
+    if (have >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) have = smem;
+    return e;
+}
+
+}  // namespace ce
+
+extern "C" {
+
+int ce_fwd_bwd(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
+               float *loss_out, void *grad_out, void *stream) {
+    return run(logits, targets, B, C, dtype, loss_out, grad_out, stream, CE_PATH_AUTO, 0);
+}
+
+int ce_fwd_bwd_path(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
+                    float *loss_out, void *grad_out, void *stream, int path, int split) {
+    return run(logits, targets, B, C, dtype, loss_out, grad_out, stream, path, split);
+}
+
+int ce_query_plan(int64_t B, int64_t C, int dtype, int *path, int *split, int *ctas,
+                  int *threads, int *smem_bytes, int *launches) {
+    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_DTYPE;
+    if (B < 1 || C < 1 || B > 0x7fffffffLL || C > 0x7fffffffLL) return CE_ERR_SHAPE;
+    Plan pl;
+    int rc = make_plan(B, C, dtype, CE_PATH_AUTO, 0, &pl);
+    if (rc != CE_OK) return rc;
+    if (path) *path = pl.path;
+    if (split) *split = pl.split;
+    if (ctas) *ctas = pl.ctas;
+    if (threads) *threads = pl.threads;
+    if (smem_bytes) *smem_bytes = pl.smem;
+    if (launches) *launches = pl.launches;
+    return CE_OK;
+}
+
+int ce_get_device_errors(void *stream, int32_t *bad_targets, int32_t *timeouts) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        auto it = g_ws.find({dev, reinterpret_cast<uintptr_t>(s)});
+        if (it != g_ws.end()) base = it->second.base;
+    }
+    int32_t h[2] = {0, 0};
+    if (base) {
+        if ((e = cudaMemcpyAsync(h, base + 4, sizeof h, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaMemsetAsync(base + 4, 0, sizeof h, s)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+    }
+    if (bad_targets) *bad_targets = h[0];
+    if (timeouts) *timeouts = h[1];
+    return CE_OK;
+}
+
+int ce_release_workspaces(void) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    int rc = CE_OK;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto &kv : g_ws) {
+        if (!kv.second.base) continue;
+        cudaSetDevice(kv.first.first);
+        cudaError_t e = cudaFree(kv.second.base);
+        if (e != cudaSuccess) rc = cuda_fail(e);
+    }
+    g_ws.clear();
+    cudaSetDevice(cur);
+    return rc;
+}
+
+const char *ce_status_string(int status) {
+    switch (status) {
+        case CE_OK: return "ok";
+        case CE_ERR_NULL: return "a required pointer is NULL";
+        case CE_ERR_SHAPE: return "invalid shape (B and C must be in [1, 2^31-1])";
+        case CE_ERR_DTYPE: return "unknown dtype";
+        case CE_ERR_ALIGN: return "pointer not aligned to its element size";
+        case CE_ERR_CUDA: return "CUDA runtime error";
+        case CE_ERR_OVERLAP: return "grad_out overlaps an input or loss_out";
+        case CE_ERR_POINTER: return "pointer not accessible from the current device";
+        case CE_ERR_CAPTURE: return "workspace must grow while the stream is being captured";
+        case CE_ERR_PATH: return "the forced path cannot run this shape";
+        default: return "unknown status";
+    }
+}
+
+const char *ce_last_cuda_error(void) { return g_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,342 @@
+// Device-side building blocks of the softmax cross-entropy kernels (sm_103a):
+// PTX wrappers for TMA bulk copies, mbarriers and thread-block clusters, the
+// element-type traits, block reductions and the fixed-order batch-loss tail.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace ce {
+
+// log2(e) and ln(2) as fp32.  The kernels evaluate e^(z - m) as
+// 2^(z*log2e - M) with M = fp32(m*log2e): one FFMA per element and one
+// ex2.approx.  M is the same for every element of a row, so its rounding is a
+// common factor that cancels in softmax = e/S; the row loss uses the same M.
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Bounded waits: a wait gives up after this many SM clock cycles (about a
+// second at 2 GHz), records a timeout in the device error word and the kernel
+// skips the rest of its work instead of hanging the GPU.
+constexpr long long kWaitLimitCycles = 2000000000LL;
+
+// Device error word layout (two int32 counters in the workspace).
+constexpr int kErrBadTarget = 0;
+constexpr int kErrTimeout = 1;
+
+// Kernel parameters shared by every path.
+struct Params {
+    const unsigned char *logits;  // [B][C] elements, byte pointer
+    const int32_t *targets;       // [B]
+    unsigned char *grad;          // [B][C] elements, byte pointer
+    float *loss_out;              // one fp32
+    float *loss_rows;             // workspace: [B] per-row losses
+    unsigned int *ticket;         // workspace: CTA completion counter (self-resetting)
+    int *err;                     // workspace: error counters
+    float2 *parts;                // workspace of the streaming path: [B][chunks] (M, S)
+    float *zt;                    // workspace of the streaming path: [B] target logits
+    long long B;
+    long long C;
+    float inv_b;                  // fp32(1/B)
+    uint64_t lo_clip;             // TMA-safe byte range of the logits:
+    uint64_t hi_clip;             //   [round_up16(begin), round_down16(end))
+    int grad_vec_ok;              // grad and logits share their address mod 16
+};
+
+// ------------------------------------------------------------ element types
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    static constexpr int kBytes = 4;
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+    __device__ __forceinline__ static float load(const unsigned char *p) {
+        return *reinterpret_cast<const float *>(p);
+    }
+    __device__ __forceinline__ static float load_global(const unsigned char *p) {
+        return __ldg(reinterpret_cast<const float *>(p));
+    }
+    __device__ __forceinline__ static void unpack(const uint4 &w, float (&v)[4]) {
+        v[0] = __uint_as_float(w.x);
+        v[1] = __uint_as_float(w.y);
+        v[2] = __uint_as_float(w.z);
+        v[3] = __uint_as_float(w.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&v)[4]) {
+        return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                          __float_as_uint(v[2]), __float_as_uint(v[3]));
+    }
+    __device__ __forceinline__ static void store(unsigned char *p, float v) {
+        *reinterpret_cast<float *>(p) = v;
+    }
+    // Max over one 16-byte vector (exact).
+    __device__ __forceinline__ static float vmax(const uint4 &w) {
+        return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                     fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+    }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int kBytes = 2;
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static float widen(uint16_t b) {
+        return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    }
+    __device__ __forceinline__ static float load(const unsigned char *p) {
+        return widen(*reinterpret_cast<const uint16_t *>(p));
+    }
+    __device__ __forceinline__ static float load_global(const unsigned char *p) {
+        return widen(__ldg(reinterpret_cast<const unsigned short *>(p)));
+    }
+    __device__ __forceinline__ static void unpack(const uint4 &w, float (&v)[8]) {
+        v[0] = __uint_as_float(w.x << 16);
+        v[1] = __uint_as_float(w.x & 0xffff0000u);
+        v[2] = __uint_as_float(w.y << 16);
+        v[3] = __uint_as_float(w.y & 0xffff0000u);
+        v[4] = __uint_as_float(w.z << 16);
+        v[5] = __uint_as_float(w.z & 0xffff0000u);
+        v[6] = __uint_as_float(w.w << 16);
+        v[7] = __uint_as_float(w.w & 0xffff0000u);
+    }
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&v)[8]) {
+        return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]),
+                          pack2(v[6], v[7]));
+    }
+    __device__ __forceinline__ static void store(unsigned char *p, float v) {
+        *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
+    }
+    // Max over one 16-byte vector, taken on the packed bf16 pairs (exact: the
+    // widening to fp32 is monotonic).
+    __device__ __forceinline__ static float vmax(const uint4 &w) {
+        __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&w.x);
+        __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w.y);
+        __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162 *>(&w.z);
+        __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162 *>(&w.w);
+        __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+        return fmaxf(__low2float(m), __high2float(m));
+    }
+};
+
+// ---------------------------------------------------------------- arithmetic
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Butterfly sum: every lane ends with the same bits.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------------ shared memory
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for phase `parity` of an mbarrier, for at most kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitLimitCycles) return false;
+    }
+    return true;
+}
+
+// One TMA bulk copy global -> this CTA's shared memory, completing on `bar`.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const unsigned char *p) {
+    return *reinterpret_cast<const uint4 *>(p);
+}
+
+__device__ __forceinline__ void stg128(unsigned char *p, const uint4 &v) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ------------------------------------------------------------------ clusters
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// Read a float4 from the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ float4 ld_dsmem_f4(const void *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)),
+                 "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------- batch-loss tail
+
+// Error-free sum of two floats (Knuth's TwoSum): a + b = s + e exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = a + b;
+    float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// Number of lanes of the fixed-order tail reduction.  Every kernel launches at
+// least this many threads per CTA, so the summation order depends only on B.
+constexpr int kTailThreads = 256;
+
+// L = (1/B) * sum_b loss_rows[b], summed in a fixed order with a compensated
+// (float, float) accumulator: lane i sums rows 4i..4i+3, 4i+1024.. in order,
+// then the lanes combine in a fixed tree.  Called by every thread of the last
+// CTA to finish; threads >= kTailThreads only take part in the barriers.
+__device__ __forceinline__ void batch_loss_tail(const Params &p, float2 *scratch /* [8] */) {
+    const int tid = threadIdx.x;
+    float hi = 0.f, lo = 0.f;
+    if (tid < kTailThreads) {
+        const long long B = p.B;
+        for (long long base = 4LL * tid; base < B; base += 4LL * kTailThreads) {
+            float x[4];
+            if (base + 3 < B) {
+                float4 q = __ldcg(reinterpret_cast<const float4 *>(p.loss_rows + base));
+                x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) x[k] = base + k < B ? __ldcg(p.loss_rows + base + k) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float s, e;
+                two_sum(hi, x[k], s, e);
+                hi = s;
+                lo += e;
+            }
+        }
+        // fixed tree inside the warp (lane 0 ends with the warp's total)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float h2 = __shfl_down_sync(0xffffffffu, hi, o);
+            float l2 = __shfl_down_sync(0xffffffffu, lo, o);
+            float s, e;
+            two_sum(hi, h2, s, e);
+            hi = s;
+            lo += l2 + e;
+        }
+        if ((tid & 31) == 0) scratch[tid >> 5] = make_float2(hi, lo);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float h = 0.f, l = 0.f;
+        for (int w = 0; w < kTailThreads / 32; ++w) {
+            float s, e;
+            two_sum(h, scratch[w].x, s, e);
+            h = s;
+            l += scratch[w].y + e;
+        }
+        const double total = static_cast<double>(h) + static_cast<double>(l);
+        *p.loss_out = static_cast<float>(total / static_cast<double>(p.B));
+        *p.ticket = 0u;  // ready for the next launch on this workspace
+    }
+}
+
+// Called once per CTA after its last row loss is stored.  The CTA that
+// finishes last reduces the batch loss.  `flag` and `scratch` are shared.
+__device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *scratch) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
+        const unsigned int prev = atomicAdd(p.ticket, 1u);
+        *flag = (prev == total - 1u);
+    }
+    __syncthreads();
+    if (*flag) {
+        __threadfence();
+        batch_loss_tail(p, scratch);
+    }
+}
+
+}  // namespace ce

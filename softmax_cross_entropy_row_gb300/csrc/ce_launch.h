@@ -1,0 +1,42 @@
+// Host-side interface between the C-ABI layer (ce_api.cu) and the kernel
+// translation units.  Internal to the library.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "ce_device.cuh"
+
+namespace ce {
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, kernel)
+// and size: later launches (including ones made during stream capture) skip it.
+cudaError_t ensure_smem_attr(const void *func, int smem);
+
+// Threads per CTA of each path.
+constexpr int kSplitThreads = 512;
+constexpr int kWarpKernelWarps = 16;
+constexpr int kStreamThreads = 256;
+constexpr int kStreamPerThread = 16;  // elements each thread keeps in registers
+constexpr int kStreamChunk = kStreamThreads * kStreamPerThread;
+
+// Upper bounds of the shared-memory ring sizes (slots of staged rows).
+constexpr int kMaxSplitSlots = 8;
+constexpr int kMaxWarpSlots = 4;  // per warp
+
+// Split-row path: one row (K = 1) or one slice of a row per CTA of a cluster
+// of K CTAs; `nslots` staged slices of `slot_bytes` each per CTA.
+cudaError_t launch_split(const Params &p, int dtype, int K, int ctas, int nslots,
+                         int slot_bytes, long long slice_elems, int smem, cudaStream_t s);
+// Largest number of co-resident clusters of K CTAs with `smem` dynamic bytes.
+cudaError_t split_max_clusters(int dtype, int K, int smem, int *clusters);
+
+// Warp-per-row path: tiles of `rows_per_tile` consecutive rows, `slots` tiles
+// staged per warp.
+cudaError_t launch_rows_warp(const Params &p, int dtype, int ctas, int slots,
+                             int rows_per_tile, int slot_bytes, int smem, cudaStream_t s);
+cudaError_t rows_warp_max_ctas_per_sm(int dtype, int smem, int *ctas);
+
+// Streaming path: pass A (chunk partials) and pass B (combine, gradient, loss).
+cudaError_t launch_stream(const Params &p, int dtype, long long chunks, cudaStream_t s);
+
+}  // namespace ce

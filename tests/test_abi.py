@@ -1,0 +1,77 @@
+"""The C-ABI library builds, loads without a GPU and exports what ce.h declares."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import softmax_cross_entropy_row_gb300 as ce
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ce.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ce_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ce.build()
+    return ce.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert "ce_fwd_bwd" in names and "ce_status_string" in names
+    assert set(names) == set(ce.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libce.so does not export {name}"
+
+
+def test_status_strings_need_no_gpu(lib):
+    for code in range(10):
+        s = lib.ce_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.ce_status_string(99).decode() == "unknown status"
+    assert lib.ce_last_cuda_error().decode() == ""
+
+
+def test_host_side_argument_errors_need_no_gpu(lib):
+    """Argument checks run before any CUDA call, so they answer on a CPU machine."""
+    f = ce.ce_fwd_bwd_raw
+    assert f(0, 0, 4, 4, 0, 0, 0) == 1                      # NULL
+    assert f(256, 512, 4, 4, 7, 1024, 4096) == 3            # dtype
+    assert f(256, 512, 0, 4, 0, 1024, 4096) == 2            # B = 0
+    assert f(256, 512, 4, 0, 0, 1024, 4096) == 2            # C = 0
+    assert f(256, 512, 2**31, 4, 0, 1024, 4096) == 2        # B too large
+    assert f(258, 512, 4, 4, 0, 1024, 4096) == 4            # fp32 logits at 2 mod 4
+    assert f(256, 514, 4, 4, 1, 1024, 4096) == 4            # int32 targets at 2 mod 4
+    assert f(1 << 20, 512, 4, 4, 0, 1024, (1 << 20) + 32) == 6  # grad overlaps logits
+    assert f(1 << 20, 1 << 24, 4, 4, 0, 1 << 25, (1 << 24) - 32) == 6  # grad covers targets
+
+
+def test_no_cpu_fallback_without_library(tmp_path):
+    """The binding refuses to run when the CUDA library is absent."""
+    import importlib
+
+    mod = importlib.import_module("softmax_cross_entropy_row_gb300")
+    with pytest.raises(ImportError):
+        mod.load_library(str(tmp_path / "missing_libce.so"))
+
+
+def test_product_does_not_touch_the_oracle(lib):
+    """Neither the library nor the binding loads anything of the oracle."""
+    import subprocess
+    import sys
+
+    assert not hasattr(lib, "ce_oracle_rows") and not hasattr(lib, "ce_oracle_fwd_bwd")
+    code = ("import sys, softmax_cross_entropy_row_gb300 as ce; ce.load_library(); "
+            "assert 'oracle' not in sys.modules and 'workloads' not in sys.modules")
+    subprocess.run([sys.executable, "-c", code], check=True, cwd=ROOT)

@@ -1,0 +1,328 @@
+"""GPU parity: the CUDA path through the C-ABI against the fp64 oracle.
+
+Small cases are compared element by element; the full-size workloads are
+compared on the batch loss (oracle over every row) and on sampled gradient
+rows (the structured rows, the first and last rows and a seeded random
+sample), plus the row-sum property on every row.
+"""
+
+import numpy as np
+import pytest
+
+import workloads as wl
+
+from parity import (GRAD_ATOL_TIMES_B, ROWSUM_ATOL_TIMES_B, check_full, check_grad, check_loss,
+                    check_sampled, device_inputs, grad_rows_host, run, ulp_bf16)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import softmax_cross_entropy_row_gb300 as ce  # noqa: E402
+import oracle  # noqa: E402
+
+AUTO, WARP, SPLIT, STREAM = (ce.CE_PATH_AUTO, ce.CE_PATH_ROWS_WARP, ce.CE_PATH_ROW_SPLIT,
+                             ce.CE_PATH_STREAM)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ce.build()
+    ce.load_library()
+    oracle.build()
+    yield
+    torch.cuda.synchronize()
+
+
+def _case(B, C, dtype, seed, sigma=2.0):
+    return wl.random_case(B, C, dtype, seed=seed, sigma=sigma)
+
+
+# --------------------------------------------------------- small workloads
+
+@pytest.mark.parametrize("name", ["tiny_8x10_f32", "classifier_4096x1000_f32"])
+def test_small_workloads_full(name):
+    inp = wl.make_inputs(wl.WORKLOADS_BY_NAME[name])
+    z, t = device_inputs(inp)
+    loss, grad = run(z, t)
+    torch.cuda.synchronize()
+    check_full(inp, loss, grad, name)
+
+
+# ------------------------------------------------- edge shapes, every path
+
+WARP_SHAPES = [(1, 1), (3, 2), (8, 3), (5, 5), (7, 7), (64, 10), (33, 31), (9, 33), (300, 1000),
+               (17, 1023), (16, 1025), (4, 2047), (5, 2048)]
+SPLIT_SHAPES = [(1, 1), (2, 3), (3, 17), (5, 1000), (4, 4099), (3, 8191), (6, 16385), (2, 40000),
+                (3, 50257)]
+STREAM_SHAPES = [(1, 1), (3, 5), (2, 4095), (2, 4096), (3, 4097), (2, 10000), (2, 50257)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,C", WARP_SHAPES)
+def test_warp_path_shapes(B, C, dtype):
+    inp = _case(B, C, dtype, seed=B * 7919 + C)
+    z, t = device_inputs(inp)
+    loss, grad = run(z, t, WARP)
+    torch.cuda.synchronize()
+    check_full(inp, loss, grad, f"warp {B}x{C} {dtype}")
+
+
+@pytest.mark.parametrize("K", [1, 2, 4, 8])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,C", SPLIT_SHAPES)
+def test_split_path_shapes(B, C, dtype, K):
+    inp = _case(B, C, dtype, seed=B * 104729 + C + K, sigma=3.0)
+    z, t = device_inputs(inp)
+    loss, grad = run(z, t, SPLIT, K)
+    torch.cuda.synchronize()
+    check_full(inp, loss, grad, f"split K={K} {B}x{C} {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("B,C", STREAM_SHAPES)
+def test_stream_path_shapes(B, C, dtype):
+    inp = _case(B, C, dtype, seed=B * 31 + C, sigma=3.0)
+    z, t = device_inputs(inp)
+    loss, grad = run(z, t, STREAM)
+    torch.cuda.synchronize()
+    check_full(inp, loss, grad, f"stream {B}x{C} {dtype}")
+
+
+def test_many_rows_per_cluster():
+    """More rows than clusters: the shared-memory rings wrap several times."""
+    for dtype, C, K in [("f32", 3000, 1), ("bf16", 9000, 2), ("f32", 20000, 4)]:
+        inp = _case(1500, C, dtype, seed=C + K, sigma=2.0)
+        z, t = device_inputs(inp)
+        loss, grad = run(z, t, SPLIT, K)
+        torch.cuda.synchronize()
+        check_full(inp, loss, grad, f"ring wrap {dtype} C={C} K={K}")
+    inp = _case(20000, 100, "bf16", seed=5)
+    z, t = device_inputs(inp)
+    loss, grad = run(z, t, WARP)
+    torch.cuda.synchronize()
+    check_full(inp, loss, grad, "warp ring wrap")
+
+
+# ------------------------------------------------------ pointer alignment
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("path,split,C", [(WARP, 0, 37), (WARP, 0, 1001), (SPLIT, 1, 5003),
+                                          (SPLIT, 4, 7001), (STREAM, 0, 5003)])
+@pytest.mark.parametrize("zoff,goff", [(1, 0), (0, 1), (3, 2), (1, 1)])
+def test_unaligned_tensors(dtype, path, split, C, zoff, goff):
+    """Logits and grad starting at any element offset (not 16-byte aligned),
+    with an unaligned end: the copy cannot cover the first and last bytes."""
+    B = 5
+    inp = _case(B, C, dtype, seed=C + zoff * 10 + goff, sigma=2.0)
+    z0, t = device_inputs(inp)
+    n = B * C
+    zbuf = torch.empty(n + 16, dtype=z0.dtype, device="cuda")
+    zbuf.fill_(float("nan"))
+    z = zbuf[zoff:zoff + n].view(B, C)
+    z.copy_(z0)
+    gbuf = torch.full((n + 16,), 7.0, dtype=z0.dtype, device="cuda")
+    g = gbuf[goff:goff + n].view(B, C)
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    ce.ce_fwd_bwd_path(z, t, loss, g, None, path, split)
+    torch.cuda.synchronize()
+    check_full(inp, loss, g, f"offsets z+{zoff} g+{goff}")
+    # nothing outside the grad tensor was written
+    assert torch.all(gbuf[:goff] == 7.0) and torch.all(gbuf[goff + n:] == 7.0)
+
+
+# ------------------------------------------------------------- data errors
+
+@pytest.mark.parametrize("path,split,C,dtype", [(WARP, 0, 100, "f32"), (SPLIT, 1, 9000, "bf16"),
+                                                (SPLIT, 4, 9000, "f32"), (STREAM, 0, 9000, "f32")])
+def test_out_of_range_targets(path, split, C, dtype):
+    """Reading: an out-of-range target gives a NaN loss, a softmax/B gradient
+    row (no one-hot term) and one count per bad row; other rows unaffected."""
+    B = 6
+    inp = _case(B, C, dtype, seed=C + path)
+    inp.targets[1] = -1
+    inp.targets[4] = C
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ce.ce_get_device_errors(s)  # clear
+        z, t = device_inputs(inp)
+        loss, grad = run(z, t, path, split, s)
+        bad, tmo = ce.ce_get_device_errors(s)
+    assert (bad, tmo) == (2, 0)
+    assert ce.ce_get_device_errors(s) == (0, 0)
+    check_full(inp, loss, grad, "bad targets")
+
+
+# ------------------------------------------------------ stated properties
+
+@pytest.mark.parametrize("path,split,C,dtype", [(WARP, 0, 1000, "f32"), (SPLIT, 1, 32000, "bf16"),
+                                                (SPLIT, 4, 50257, "f32"), (STREAM, 0, 9000, "bf16")])
+def test_bitwise_deterministic(path, split, C, dtype):
+    inp = _case(64, C, dtype, seed=77)
+    z, t = device_inputs(inp)
+    loss0, grad0 = run(z, t, path, split)
+    for _ in range(9):
+        loss, grad = run(z, t, path, split)
+        assert torch.equal(loss, loss0)
+        assert torch.equal(grad.view(torch.int16) if dtype == "bf16" else grad.view(torch.int32),
+                           grad0.view(torch.int16) if dtype == "bf16" else grad0.view(torch.int32))
+
+
+def test_structured_rows_small():
+    """The stress recipe (uniform rows, +80 spikes, 30*N(0,1)) and the peaked
+    bf16 recipe at sizes the oracle compares element by element."""
+    stress = wl.Workload("stress_small", 400, 5003, "f32", seed=4, sigma=30.0,
+                         uniform_frac=0.01, spike=80.0)
+    peaked = wl.Workload("peaked_small", 256, 12829, "bf16", seed=3, sigma=3.0, peak=8.0)
+    for w, paths in [(stress, [(AUTO, 0), (SPLIT, 2), (SPLIT, 4), (STREAM, 0)]),
+                     (peaked, [(AUTO, 0), (SPLIT, 1), (SPLIT, 8), (STREAM, 0)])]:
+        inp = wl.make_inputs(w)
+        z, t = device_inputs(inp)
+        for path, split in paths:
+            loss, grad = run(z, t, path, split)
+            torch.cuda.synchronize()
+            check_full(inp, loss, grad, f"{w.name} path {path}/{split}")
+
+
+# ------------------------------------------------------ full-size workloads
+
+EXPECTED_PLAN = {
+    "classifier_4096x1000_f32": ("rows_warp", 1),
+    "lm_head_8192x32000_bf16": ("row_split", 1),
+    "lm_head_4096x128256_bf16_peaked": ("row_split", 4),
+    "stress_16384x50257_f32": ("row_split", 4),
+}
+
+
+def _sample_rows(inp, n=40):
+    B = inp.workload.B
+    g = np.random.default_rng(inp.workload.seed + 1000)
+    rows = [0, 1, B // 2, B - 2, B - 1]
+    rows += list(g.choice(B, size=n, replace=False))
+    rows += list(inp.uniform_rows[:8]) + list(inp.spike_rows[:8])
+    return np.array(rows, dtype=np.int64)
+
+
+def _row_sums_ok(grad, B, dtype):
+    worst = 0.0
+    for r0 in range(0, grad.shape[0], 512):
+        blk = grad[r0:r0 + 512]
+        s = blk.double().sum(dim=1).abs()
+        if dtype == "f32":
+            worst = max(worst, float(s.max()) * B)
+        else:
+            g = blk.float()
+            e = torch.floor(torch.log2(torch.clamp(g.abs(), min=2.0 ** -126)))
+            bound = ROWSUM_ATOL_TIMES_B / B + 0.5 * torch.exp2(e - 7).double().sum(dim=1)
+            assert torch.all(s <= bound), "bf16 row sums beyond their rounding bound"
+    if dtype == "f32":
+        assert worst <= ROWSUM_ATOL_TIMES_B, f"row sum {worst:.3g}/B"
+
+
+@pytest.mark.parametrize("name", ["classifier_4096x1000_f32", "lm_head_8192x32000_bf16",
+                                  "lm_head_4096x128256_bf16_peaked", "stress_16384x50257_f32"])
+def test_full_size_workload(name):
+    w = wl.WORKLOADS_BY_NAME[name]
+    plan = ce.ce_query_plan(w.B, w.C, w.dtype_code)
+    assert (plan["path_name"], plan["split"]) == EXPECTED_PLAN[name]
+    inp = wl.make_inputs(w)
+    z, t = device_inputs(inp)
+    loss, grad = run(z, t)
+    torch.cuda.synchronize()
+    check_sampled(inp, loss, grad, _sample_rows(inp), name)
+    _row_sums_ok(grad, w.B, w.dtype)
+    # uniform rows: softmax is exactly 1/C
+    for r in inp.uniform_rows[:4]:
+        g = grad_rows_host(grad, [r])[0]
+        expect = np.full(w.C, 1.0 / w.C / w.B)
+        expect[inp.targets[r]] -= 1.0 / w.B
+        check_grad(g[None], expect[None], w.B, w.dtype, "uniform row")
+    bad, tmo = ce.ce_get_device_errors()
+    assert (bad, tmo) == (0, 0)
+
+
+def test_stress_workload_stream_path():
+    """The streaming path on the full ragged stress workload (sampled rows)."""
+    w = wl.WORKLOADS_BY_NAME["stress_16384x50257_f32"]
+    inp = wl.make_inputs(w)
+    z, t = device_inputs(inp)
+    loss, grad = run(z, t, STREAM)
+    torch.cuda.synchronize()
+    check_sampled(inp, loss, grad, _sample_rows(inp, 16), "stress via stream path")
+
+
+# --------------------------------------------------------------- runtime
+
+def test_graph_capture_and_replay():
+    inp = _case(512, 3000, "bf16", seed=9)
+    z, t = device_inputs(inp)
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    grad = torch.empty_like(z)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ce.ce_fwd_bwd(z, t, loss, grad, s)  # sizes the stream's workspace
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            ce.ce_fwd_bwd(z, t, loss, grad, s)
+    inp2 = _case(512, 3000, "bf16", seed=10)
+    z2, t2 = device_inputs(inp2)
+    z.copy_(z2)
+    t.copy_(t2)
+    loss.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    check_full(inp2, loss, grad, "graph replay")
+
+
+def test_capture_needs_a_sized_workspace():
+    z = torch.zeros(4, 8, device="cuda")
+    t = torch.zeros(4, dtype=torch.int32, device="cuda")
+    loss = torch.empty(1, device="cuda")
+    grad = torch.empty_like(z)
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with pytest.raises(ce.CEError) as ei:
+            with torch.cuda.graph(graph, stream=s):
+                ce.ce_fwd_bwd(z, t, loss, grad, s)
+    assert ei.value.status == 8
+
+
+def test_concurrent_streams():
+    cases = [_case(300, 7000, "f32", seed=1), _case(200, 5000, "bf16", seed=2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for inp, s in zip(cases, streams):
+        with torch.cuda.stream(s):
+            z, t = device_inputs(inp)
+            outs.append(run(z, t, AUTO, 0, s))
+    torch.cuda.synchronize()
+    for inp, (loss, grad) in zip(cases, outs):
+        check_full(inp, loss, grad, "concurrent streams")
+
+
+def test_forced_path_limits():
+    z = torch.zeros(2, 100000, device="cuda")
+    t = torch.zeros(2, dtype=torch.int32, device="cuda")
+    loss = torch.empty(1, device="cuda")
+    grad = torch.empty_like(z)
+    for path, split in [(WARP, 0), (SPLIT, 3), (SPLIT, 1)]:
+        with pytest.raises(ce.CEError) as ei:
+            ce.ce_fwd_bwd_path(z, t, loss, grad, None, path, split)
+        assert ei.value.status == 9
+
+
+def test_error_codes_on_device_pointers():
+    z = torch.zeros(4, 8, device="cuda")
+    t = torch.zeros(4, dtype=torch.int32, device="cuda")
+    loss = torch.empty(1, device="cuda")
+    grad = torch.empty_like(z)
+    raw = ce.ce_fwd_bwd_raw
+    assert raw(z.data_ptr(), t.data_ptr(), 4, 8, 0, loss.data_ptr(), grad.data_ptr()) == 0
+    assert raw(z.data_ptr(), t.data_ptr(), 4, 8, 0, loss.data_ptr(), z.data_ptr()) == 6
+    assert raw(z.data_ptr() + 2, t.data_ptr(), 4, 8, 0, loss.data_ptr(), grad.data_ptr()) == 4
+    assert raw(z.data_ptr(), t.data_ptr(), 4, 8, 2, loss.data_ptr(), grad.data_ptr()) == 3
+    torch.cuda.synchronize()
