@@ -167,17 +167,26 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         for (int w = 1; w < NW; ++w) m = fmaxf(m, red_a[w]);
         float M = m * kLog2e;
 
-        // ---- Step 2: slice sum of exponentials
+        // ---- Step 2: slice sum of exponentials, the target's term left out
+        // (it is added back after the combine, so that 1 - p_t keeps its
+        // relative precision when the target dominates the row)
         float sa = 0.f, sb = 0.f;
         if (!failed) {
 #pragma unroll 2
             for (int v = vb + tid; v < ve; v += NT) {
                 float z[W];
                 E::unpack(lds128(slot + 16 * v), z);
+                const long long d = t - (e0 + (long long)v * W);
+                if ((unsigned long long)d < (unsigned long long)W) {
 #pragma unroll
-                for (int k = 0; k < W; k += 2) {
-                    sa += ex2(fmaf(z[k], kLog2e, -M));
-                    sb += ex2(fmaf(z[k + 1], kLog2e, -M));
+                    for (int k = 0; k < W; ++k)
+                        if (k != d) sa += ex2(fmaf(z[k], kLog2e, -M));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < W; k += 2) {
+                        sa += ex2(fmaf(z[k], kLog2e, -M));
+                        sb += ex2(fmaf(z[k + 1], kLog2e, -M));
+                    }
                 }
             }
             if ((tid == 0 && rv0 >= 0) || (tid == NT - 1 && rv1 >= 0)) {
@@ -187,7 +196,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 #pragma unroll
                 for (int k = 0; k < W; ++k) {
                     const long long e = e0 + (long long)v * W + k;
-                    if (e >= c0 && e < c1) sa += ex2(fmaf(z[k], kLog2e, -M));
+                    if (e >= c0 && e < c1 && e != t) sa += ex2(fmaf(z[k], kLog2e, -M));
                 }
             }
         }
@@ -235,10 +244,15 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
             zt = cb.z;
             has_t = cb.w != 0.f;
         }
+        // S holds the sum without the target's term: S_rest = S * (1 - p_t).
+        const float s_rest = S;
+        const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
+        S = s_rest + e_t;
 
         // ---- Step 4: gradient of the slice
         const float scale = (1.0f / S) * p.inv_b;
-        const float inv_b = p.inv_b;
+        // (p_t - 1) / B = -S_rest / (S B): no cancellation when p_t is near 1
+        const float g_t = -s_rest * scale;
         if (!failed) {
             unsigned char *gbase = p.grad + (g0 - lbase);  // grad byte of vector 0
             const bool vec_store = p.grad_vec_ok != 0;
@@ -253,7 +267,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                 if ((unsigned long long)d < (unsigned long long)W) {
 #pragma unroll
                     for (int k = 0; k < W; ++k)
-                        if (k == d) g[k] = fmaf(ex2(fmaf(z[k], kLog2e, -M)), scale, -inv_b);
+                        if (k == d) g[k] = g_t;
                 }
                 if (vec_store) {
                     stg128(gbase + 16 * (size_t)v, E::pack(g));
@@ -270,8 +284,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                 for (int k = 0; k < W; ++k) {
                     const long long e = e0 + (long long)v * W + k;
                     if (e >= c0 && e < c1) {
-                        const float ev = ex2(fmaf(z[k], kLog2e, -M));
-                        const float gv = e == t ? fmaf(ev, scale, -inv_b) : ev * scale;
+                        const float gv = e == t ? g_t : ex2(fmaf(z[k], kLog2e, -M)) * scale;
                         E::store(gbase + 16 * (size_t)v + k * ES, gv);
                     }
                 }
@@ -282,7 +295,10 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         if (rank == 0 && tid == 0 && !failed) {
             float l;
             if (has_t) {
-                l = kLn2 * (log2f(S) - fmaf(zt, kLog2e, -M));
+                // l = log(S / e_t) = log1p(S_rest / e_t): the second form keeps
+                // its precision when the target dominates (then e_t > S / 2).
+                l = s_rest < e_t ? log1pf(s_rest / e_t)
+                                 : kLn2 * (log2f(S) - fmaf(zt, kLog2e, -M));
             } else {
                 l = NAN;
                 atomicAdd(&p.err[kErrBadTarget], 1);

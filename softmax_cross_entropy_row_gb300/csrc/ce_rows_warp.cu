@@ -126,27 +126,36 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32)
             for (long long c = lane; c < C; c += 32) m = fmaxf(m, E::load(row + c * ES));
             m = warp_max(m);
             const float M = m * kLog2e;
-            // Step 2: sum of exponentials
+            // Step 2: sum of exponentials without the target's term (added
+            // back below, so that 1 - p_t keeps its relative precision)
             float sa = 0.f, sb = 0.f;
             long long c = lane;
             for (; c + 32 < C; c += 64) {
-                sa += ex2(fmaf(E::load(row + c * ES), kLog2e, -M));
-                sb += ex2(fmaf(E::load(row + (c + 32) * ES), kLog2e, -M));
+                const float ea = ex2(fmaf(E::load(row + c * ES), kLog2e, -M));
+                const float eb = ex2(fmaf(E::load(row + (c + 32) * ES), kLog2e, -M));
+                sa += c == t ? 0.f : ea;
+                sb += c + 32 == t ? 0.f : eb;
             }
-            if (c < C) sa += ex2(fmaf(E::load(row + c * ES), kLog2e, -M));
-            const float S = warp_sum(sa + sb);
-            // Step 4: gradient
+            if (c < C && c != t) sa += ex2(fmaf(E::load(row + c * ES), kLog2e, -M));
+            const float s_rest = warp_sum(sa + sb);
+            const bool has_t = t >= 0 && t < C;
+            const float zt = has_t ? E::load(row + t * ES) : 0.f;
+            const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
+            const float S = s_rest + e_t;
+            // Step 4: gradient; (p_t - 1) / B = -S_rest / (S B)
             const float scale = (1.0f / S) * inv_b;
+            const float g_t = -s_rest * scale;
             unsigned char *grow = p.grad + (size_t)(r * C) * ES;
             for (long long k = lane; k < C; k += 32) {
                 const float ev = ex2(fmaf(E::load(row + k * ES), kLog2e, -M));
-                E::store(grow + k * ES, k == t ? fmaf(ev, scale, -inv_b) : ev * scale);
+                E::store(grow + k * ES, k == t ? g_t : ev * scale);
             }
-            // Step 3: loss of the row
+            // Step 3: loss of the row, log(S / e_t)
             if (lane == 0) {
                 float l;
-                if (t >= 0 && t < C) {
-                    l = kLn2 * (log2f(S) - fmaf(E::load(row + t * ES), kLog2e, -M));
+                if (has_t) {
+                    l = s_rest < e_t ? log1pf(s_rest / e_t)
+                                     : kLn2 * (log2f(S) - fmaf(zt, kLog2e, -M));
                 } else {
                     l = NAN;
                     atomicAdd(&p.err[kErrBadTarget], 1);

@@ -59,15 +59,15 @@ __global__ void __launch_bounds__(NT) stream_partials_kernel(Params p, long long
         mx = fmaxf(mx, z[i]);
     }
     const float M = block_max(mx, red) * kLog2e;
-    float s = 0.f;
+    const long long t = __ldg(p.targets + b);
+    float s = 0.f;  // without the target's term
 #pragma unroll
     for (int i = 0; i < PT; ++i) {
         const long long c = cbeg + i * NT + threadIdx.x;
-        if (c < C) s += ex2(fmaf(z[i], kLog2e, -M));
+        if (c < C && c != t) s += ex2(fmaf(z[i], kLog2e, -M));
     }
     const float S = block_sum(s, red);
     if (threadIdx.x == 0) p.parts[b * chunks + k] = make_float2(M, S);
-    const long long t = __ldg(p.targets + b);
     if (t >= cbeg && t < cbeg + kStreamChunk && t < C && threadIdx.x == 0)
         p.zt[b] = E::load_global(row + t * E::kBytes);
 }
@@ -94,11 +94,16 @@ __global__ void __launch_bounds__(NT) stream_grad_kernel(Params p, long long chu
         const float2 pq = __ldcg(&part[q]);
         sloc += pq.y * ex2(pq.x - M);
     }
-    const float S = block_sum(sloc, red);
+    const float s_rest = block_sum(sloc, red);  // the row's sum without the target's term
 
     const long long t = __ldg(p.targets + b);
+    const bool has_t = t >= 0 && t < C;
+    const float zt = has_t ? __ldcg(p.zt + b) : 0.f;
+    const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
+    const float S = s_rest + e_t;
     const float inv_b = p.inv_b;
     const float scale = (1.0f / S) * inv_b;
+    const float g_t = -s_rest * scale;  // (p_t - 1) / B without cancellation
     const unsigned char *row = p.logits + (size_t)(b * C) * E::kBytes;
     unsigned char *grow = p.grad + (size_t)(b * C) * E::kBytes;
 #pragma unroll
@@ -106,13 +111,13 @@ __global__ void __launch_bounds__(NT) stream_grad_kernel(Params p, long long chu
         const long long c = cbeg + i * NT + threadIdx.x;
         if (c < C) {
             const float ev = ex2(fmaf(E::load_global(row + c * E::kBytes), kLog2e, -M));
-            E::store(grow + c * E::kBytes, c == t ? fmaf(ev, scale, -inv_b) : ev * scale);
+            E::store(grow + c * E::kBytes, c == t ? g_t : ev * scale);
         }
     }
     if (k == 0 && threadIdx.x == 0) {
         float l;
-        if (t >= 0 && t < C) {
-            l = kLn2 * (log2f(S) - fmaf(__ldcg(p.zt + b), kLog2e, -M));
+        if (has_t) {
+            l = s_rest < e_t ? log1pf(s_rest / e_t) : kLn2 * (log2f(S) - fmaf(zt, kLog2e, -M));
         } else {
             l = NAN;
             atomicAdd(&p.err[kErrBadTarget], 1);
