@@ -1,0 +1,470 @@
+"""Benchmark of the fused softmax cross-entropy forward + gradient.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--headline-only]
+
+Prints ONE JSON line.  The headline ``value`` is rows/s of the classifier-head
+workload (B=4096, C=1000, fp32) processed by the library's kernels with the
+inputs resident in HBM; ``workloads`` carries the same measurement for every
+workload (all five, in the same run).  A step is one ``ce_fwd_bwd`` call: the
+loss and the full gradient of one batch.
+
+Timing: steps run from a CUDA graph (one library call per step, captured
+once), cycling through enough buffer sets that every step reads inputs that
+are not in L2; CUDA events on the launching stream bracket the timed steps.
+``e2e`` times the eager public call with the step's inputs copied from pinned
+host memory and the loss copied back, every step.  ``--impl reference`` times
+the fp64 CPU oracle (the only reference this path has) on the host cores.
+
+With torchrun (N > 1) every rank runs an independent replica of the workload
+(rows are independent; the path has no exchange step), barriers bracket the
+timed region and rank 0 reports the max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "fused CE fwd+grad rows/s and achieved HBM GB/s vs ~8 TB/s roofline (1×GB300)"
+HEADLINE = "classifier_4096x1000_f32"
+FALLBACK_HBM_GBS = 6800.0
+TARGET_REGION_S = 1.5      # timed work per workload when --steps is not given
+CPU_SAMPLE_S = 10.0
+MAX_SETS = 64              # a workload this small stays L2-resident (said in the output)
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "softmax_cross_entropy_row_gb300", "csrc", "*")))
+    for p in files:
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None if the kernels changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("source_sha") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="ce_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"samples": 0, "note": "nvidia-smi unavailable"}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# -------------------------------------------------------------- oracle arm
+
+def time_oracle(inp, budget_s: float = CPU_SAMPLE_S):
+    """Rows/s of the fp64 oracle's forward + gradient on a bounded sample of
+    the workload's rows (whole batch repeated, or a leading block of rows)."""
+    import oracle
+
+    oracle.build()
+    B, C = inp.logits.shape
+    # calibrate on a small block, then size the sample to the budget
+    probe = max(1, min(B, 64))
+    z = np.ascontiguousarray(inp.logits[:probe])
+    t = np.ascontiguousarray(inp.targets[:probe])
+    g = np.empty_like(z)
+    sc = np.empty(probe, dtype=np.float64)
+    t0 = time.perf_counter()
+    oracle.fwd_bwd(z, t, g, sc)
+    per_row = max((time.perf_counter() - t0) / probe, 1e-9)
+    rows = int(min(B, max(1, 0.5 * budget_s / per_row)))
+    z = np.ascontiguousarray(inp.logits[:rows])
+    t = np.ascontiguousarray(inp.targets[:rows])
+    g = np.empty_like(z)
+    sc = np.empty(rows, dtype=np.float64)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.fwd_bwd(z, t, g, sc)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            break
+    value = rows * reps / dt
+    sample = (f"leading {rows} of {B} rows x {C} classes ({inp.workload.dtype}), "
+              f"{reps} pass(es), {dt:.1f} s wall-clock on {oracle.threads()} threads")
+    return {"value": value, "unit": "rows/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": sample}
+
+
+# ------------------------------------------------------------------ our arm
+
+def device_set(inp, device):
+    import torch
+
+    if inp.workload.dtype == "bf16":
+        z = torch.from_numpy(inp.logits.view(np.int16)).view(torch.bfloat16).to(device)
+    else:
+        z = torch.from_numpy(inp.logits).to(device)
+    t = torch.from_numpy(inp.targets).to(device)
+    return z, t
+
+
+def bench_workload(w, inp, steps, warmup, device, l2_bytes, hbm_peak, peak_note, sampler_gpu,
+                   world, with_e2e=True):
+    import torch
+
+    import softmax_cross_entropy_row_gb300 as ce
+
+    plan = ce.ce_query_plan(w.B, w.C, w.dtype_code)
+    set_bytes = 2 * w.B * w.C * w.elem_bytes + 4 * w.B
+    nsets = 1
+    if set_bytes <= 2 * l2_bytes:
+        nsets = min(MAX_SETS, int(np.ceil(2 * l2_bytes / set_bytes)) + 1)
+    z0, t0 = device_set(inp, device)
+    sets = []
+    for i in range(nsets):
+        z = z0 if i == 0 else z0.clone()
+        t = t0 if i == 0 else t0.clone()
+        sets.append((z, t, torch.empty(1, dtype=torch.float32, device=device),
+                     torch.empty_like(z)))
+    s = torch.cuda.Stream(device)
+    with torch.cuda.stream(s):
+        for i in range(max(warmup, 3)):
+            z, t, loss, grad = sets[i % nsets]
+            ce.ce_fwd_bwd(z, t, loss, grad, s)
+        s.synchronize()
+        # one graph runs a whole number of passes over the buffer sets
+        per_graph = nsets * max(1, int(np.ceil(64 / nsets)))
+
+        def capture(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for i in range(n):
+                    z, t, loss, grad = sets[i % nsets]
+                    ce.ce_fwd_bwd(z, t, loss, grad, s)
+            return g
+
+        graph = capture(per_graph)
+        graph.replay()  # warm the graph
+        s.synchronize()
+        # estimate the step time to size the timed region
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        graph.replay()
+        e1.record(s)
+        e1.synchronize()
+        est = e0.elapsed_time(e1) / 1e3 / per_graph
+        if steps is None:
+            steps = per_graph * max(1, int(np.ceil(TARGET_REGION_S / (est * per_graph))))
+        replays, rest = divmod(steps, per_graph)
+        tail = capture(rest) if rest else None
+        if tail is not None:
+            tail.replay()
+        n_steps = steps
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+        sampler = ClockSampler(sampler_gpu)
+        with sampler:
+            e0.record(s)
+            for _ in range(replays):
+                graph.replay()
+            if tail is not None:
+                tail.replay()
+            e1.record(s)
+            e1.synchronize()
+        torch.cuda.synchronize(device)
+        elapsed = e0.elapsed_time(e1) / 1e3
+        if world > 1:
+            tt = torch.tensor([elapsed], dtype=torch.float64, device=device)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            elapsed = float(tt.item())
+            torch.distributed.barrier()
+        bad, tmo = ce.ce_get_device_errors(s)
+    del graph, tail
+    per_step = elapsed / n_steps
+    per_launch = per_step / plan["launches"] if plan["launches"] == 1 else None
+    achieved = w.min_bytes / per_step / 1e9
+    res = {
+        "workload": w.name, "B": w.B, "C": w.C, "logits_dtype": w.dtype,
+        "path": plan["path_name"], "split": plan["split"], "ctas": plan["ctas"],
+        "threads": plan["threads"], "smem_bytes": plan["smem_bytes"],
+        "launches_per_step": plan["launches"], "steps": n_steps, "buffer_sets": nsets,
+        "ms_per_step": per_step * 1e3, "rows_per_s": world * w.B / per_step,
+        "achieved_gbs": achieved, "frac_of_peak": achieved / hbm_peak,
+        "min_bytes_per_step": w.min_bytes, "device_errors": [bad, tmo],
+        "clocks": sampler.summary(),
+    }
+    if per_launch is not None:
+        res["kernel_ms_per_launch"] = per_launch * 1e3
+    if with_e2e:
+        res["e2e"] = bench_e2e(w, inp, device, steps=min(50, max(5, int(0.5 / max(est, 1e-6)))))
+    for z, t, loss, grad in sets:
+        del z, t, loss, grad
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_e2e(w, inp, device, steps):
+    """The public call with host inputs: pinned H2D copies of logits and
+    targets, ce_fwd_bwd, and the 4-byte loss copied back, every step."""
+    import torch
+
+    import softmax_cross_entropy_row_gb300 as ce
+
+    if w.dtype == "bf16":
+        hz = torch.from_numpy(inp.logits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    else:
+        hz = torch.from_numpy(inp.logits).pin_memory()
+    ht = torch.from_numpy(inp.targets).pin_memory()
+    hl = torch.empty(1, dtype=torch.float32).pin_memory()
+    dz = torch.empty(hz.shape, dtype=hz.dtype, device=device)
+    dt = torch.empty(ht.shape, dtype=ht.dtype, device=device)
+    dl = torch.empty(1, dtype=torch.float32, device=device)
+    dg = torch.empty_like(dz)
+    s = torch.cuda.Stream(device)
+
+    def step():
+        dz.copy_(hz, non_blocking=True)
+        dt.copy_(ht, non_blocking=True)
+        ce.ce_fwd_bwd(dz, dt, dl, dg, s)
+        hl.copy_(dl, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            step()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            step()
+        e1.record(s)
+        e1.synchronize()
+    per_step = e0.elapsed_time(e1) / 1e3 / steps
+    h2d = hz.numel() * hz.element_size() + ht.numel() * ht.element_size()
+    return {"value": w.B / per_step, "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": 4, "steps": steps, "ms_per_step": per_step * 1e3}
+
+
+def l2_note(res, w, l2_bytes):
+    n = res["buffer_sets"]
+    total = n * (2 * w.B * w.C * w.elem_bytes + 4 * w.B)
+    if n == 1:
+        return f"inputs larger than L2 ({total / 1e6:.0f} MB vs L2 {l2_bytes / 1e6:.0f} MB)"
+    if total > 2 * l2_bytes:
+        return (f"{n} rotating buffer sets ({total / 1e6:.0f} MB > 2x L2 "
+                f"{l2_bytes / 1e6:.0f} MB): every step reads inputs not in L2")
+    return f"{n} rotating buffer sets, {total / 1e3:.1f} KB in all: L2-resident (tiny workload)"
+
+
+# --------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps of the headline workload (default: ~1.5 s of work)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(wl.WORKLOADS_BY_NAME))
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--cpu-sample-s", type=float, default=CPU_SAMPLE_S,
+                    help="seconds of oracle timing for cpu_baseline (0: skip)")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="profiling only: run the workload's recipe with this many rows")
+    ap.add_argument("--no-e2e", action="store_true", help="profiling only: skip the e2e leg")
+    args = ap.parse_args()
+
+    world, rank, local = dist_env()
+    w = wl.WORKLOADS_BY_NAME[args.workload]
+    if args.rows:
+        import dataclasses
+
+        w = dataclasses.replace(w, B=int(args.rows), name=f"{w.name}_rows{args.rows}")
+        wl.WORKLOADS_BY_NAME[w.name] = w
+        args.headline_only = True
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = wl.make_inputs(w)
+        cb = time_oracle(inp, args.cpu_sample_s)
+        out = {"metric": METRIC, "value": cb["value"], "unit": "rows/s", "impl": "reference",
+               "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "f64", "data": "synthetic",
+               "config": {"workload": w.name, "B": w.B, "C": w.C, "logits_dtype": w.dtype},
+               "cpu_baseline": cb,
+               "e2e": {"value": cb["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+                       "d2h_bytes_per_step": 0}}
+        print(json.dumps(out))
+        return
+
+    import torch
+
+    import softmax_cross_entropy_row_gb300 as ce
+
+    ce.build()
+    ce.load_library()
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    props = torch.cuda.get_device_properties(device)
+    l2_bytes = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
+    hbm_peak, peak_note = measured_peaks()
+    sampler_gpu = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(device.index)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else device.index
+
+    names = [w.name] if args.headline_only else [w.name] + [x.name for x in wl.WORKLOADS
+                                                            if x.name != w.name]
+    results = {}
+    for name in names:
+        ww = wl.WORKLOADS_BY_NAME[name]
+        inp = wl.make_inputs(ww)
+        steps = args.steps if name == w.name else None
+        results[name] = bench_workload(ww, inp, steps, args.warmup, device, l2_bytes, hbm_peak,
+                                       peak_note, sampler_gpu, world,
+                                       with_e2e=not args.no_e2e)
+        if name == w.name and rank == 0:
+            head_inp = inp
+        del inp
+
+    head = results[w.name]
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_sample_s > 0:
+        cpu = time_oracle(head_inp, args.cpu_sample_s)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    roof = {"bound": "hbm", "achieved": head["achieved_gbs"], "peak": hbm_peak, "unit": "GB/s",
+            "frac": head["frac_of_peak"], "traffic": recorded_traffic(w.name),
+            "peak_source": peak_note,
+            "algorithmic_bytes_per_launch": w.min_bytes,
+            "kernel": head["path"]}
+    out = {
+        "metric": METRIC, "value": head["rows_per_s"], "unit": "rows/s", "n_gpus": world,
+        "steps": head["steps"], "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "C": w.C, "logits_dtype": w.dtype,
+                   "l2": l2_note(head, w, l2_bytes),
+                   "launch": "CUDA graph replay, one ce_fwd_bwd per step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": ({k: head["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step",
+                                             "d2h_bytes_per_step")} if "e2e" in head else None),
+        "gpu_launches": head["steps"] * head["launches_per_step"],
+        "clocks": head["clocks"],
+        "workloads": [dict(results[n], l2=l2_note(results[n], wl.WORKLOADS_BY_NAME[n], l2_bytes))
+                      for n in names],
+    }
+    print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -69,13 +69,18 @@ def check_loss(L: float, L_ref: float) -> None:
     assert err <= LOSS_RTOL * abs(L_ref) + LOSS_ATOL, f"loss {L!r} vs oracle {L_ref!r} (err {err:.3g})"
 
 
-def check_grad(g: np.ndarray, g_ref: np.ndarray, B: int, dtype: str, what: str = "") -> None:
+def check_grad(g: np.ndarray, g_ref: np.ndarray, B: int, dtype: str, what: str = "",
+               valid=None) -> None:
+    """``valid`` marks rows whose target is in range (default: all); a row with
+    an out-of-range target has no one-hot term, so it sums to 1/B instead of 0."""
     assert g.shape == g_ref.shape
+    valid = np.ones(g.shape[0], dtype=bool) if valid is None else np.asarray(valid, dtype=bool)
+    target_sum = np.where(valid, 0.0, 1.0 / B)
     if dtype == "f32":
         err = np.abs(g - g_ref)
         worst = float(err.max()) * B if err.size else 0.0
         assert worst <= GRAD_ATOL_TIMES_B, f"{what}: max |g - g_ref| = {worst:.3g}/B"
-        rs = np.abs(g.sum(axis=1)) * B
+        rs = np.abs(g.sum(axis=1) - target_sum) * B
         assert float(rs.max()) <= ROWSUM_ATOL_TIMES_B, f"{what}: row sum {float(rs.max()):.3g}/B"
     else:
         tol = ulp_bf16(g_ref)
@@ -85,7 +90,7 @@ def check_grad(g: np.ndarray, g_ref: np.ndarray, B: int, dtype: str, what: str =
             i = np.argwhere(bad)[0]
             raise AssertionError(f"{what}: {int(bad.sum())} bf16 grads beyond 1 ulp, first at "
                                  f"{tuple(i)}: {g[tuple(i)]!r} vs {g_ref[tuple(i)]!r}")
-        rs = np.abs(g.sum(axis=1))
+        rs = np.abs(g.sum(axis=1) - target_sum)
         bound = ROWSUM_ATOL_TIMES_B / B + 0.5 * ulp_bf16(g).sum(axis=1)
         assert np.all(rs <= bound), f"{what}: bf16 row sum beyond its rounding bound"
 
@@ -94,7 +99,8 @@ def check_full(inp, loss, grad, what: str = "") -> None:
     """Element-by-element comparison of a whole (small) batch."""
     L_ref, _, g_ref = oracle.loss_and_grad(inp.logits, inp.targets)
     check_loss(float(loss.item()), L_ref)
-    check_grad(grad_rows_host(grad), g_ref, inp.workload.B, inp.workload.dtype, what)
+    valid = (inp.targets >= 0) & (inp.targets < inp.workload.C)
+    check_grad(grad_rows_host(grad), g_ref, inp.workload.B, inp.workload.dtype, what, valid)
 
 
 def check_sampled(inp, loss, grad, rows, what: str = "") -> None:
@@ -103,4 +109,6 @@ def check_sampled(inp, loss, grad, rows, what: str = "") -> None:
     check_loss(float(loss.item()), oracle.batch_loss(l_all))
     rows = np.unique(np.asarray(rows, dtype=np.int64))
     _, g_ref = oracle.rows(inp.logits, inp.targets, row_ids=rows)
-    check_grad(grad_rows_host(grad, rows), g_ref, inp.workload.B, inp.workload.dtype, what)
+    t = inp.targets[rows]
+    check_grad(grad_rows_host(grad, rows), g_ref, inp.workload.B, inp.workload.dtype, what,
+               (t >= 0) & (t < inp.workload.C))
