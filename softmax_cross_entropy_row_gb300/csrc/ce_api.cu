@@ -3,6 +3,7 @@
 // launch.  Nothing here computes on the host; every step runs in the kernels.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <map>
@@ -124,8 +125,8 @@ int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, 
     const long long ntiles = (B + R - 1) / R;
     const int smem = slots * slot_bytes * ce::kWarpKernelWarps;
     int per_sm = 1;
-    int rc = cached_occupancy(dtype, CE_PATH_ROWS_WARP, 0, smem,
-                              [&](int *v) { return ce::rows_warp_max_ctas_per_sm(dtype, smem, v); },
+    int rc = cached_occupancy(dtype, CE_PATH_ROWS_WARP, (int)C, smem,
+                              [&](int *v) { return ce::rows_warp_max_ctas_per_sm(dtype, C, smem, v); },
                               &per_sm);
     if (rc != CE_OK) return rc;
     if (per_sm < 1) return CE_ERR_PATH;
@@ -142,6 +143,17 @@ int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, 
     pl->slot_bytes = slot_bytes;
     pl->rows_per_tile = (int)R;
     return CE_OK;
+}
+
+// Threads per CTA of the split-row kernel: 1024, or 512 when the environment
+// variable CE_SPLIT_THREADS says so (a tuning knob, read once).
+int split_threads() {
+    static const int n = [] {
+        const char *e = getenv("CE_SPLIT_THREADS");
+        if (e && atoi(e) == 512) return 512;
+        return ce::kSplitThreads;
+    }();
+    return n;
 }
 
 int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype, int K_forced,
@@ -180,8 +192,11 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     if (nslots > ce::kMaxSplitSlots) nslots = ce::kMaxSplitSlots;
     const int smem = nslots * (int)slot_bytes;
     int clusters = 0;
-    int rc = cached_occupancy(dtype, CE_PATH_ROW_SPLIT, K, smem,
-                              [&](int *v) { return ce::split_max_clusters(dtype, K, smem, v); },
+    const int threads = split_threads();
+    int rc = cached_occupancy(dtype, CE_PATH_ROW_SPLIT, K * 4096 + threads, smem,
+                              [&](int *v) {
+                                  return ce::split_max_clusters(dtype, K, threads, smem, v);
+                              },
                               &clusters);
     if (rc != CE_OK) return rc;
     if (clusters < 1) return CE_ERR_PATH;
@@ -189,7 +204,7 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     pl->path = CE_PATH_ROW_SPLIT;
     pl->split = K;
     pl->ctas = clusters * K;
-    pl->threads = ce::kSplitThreads;
+    pl->threads = threads;
     pl->smem = smem;
     pl->launches = 1;
     pl->nslots = nslots;
@@ -369,7 +384,8 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
                                      pl.slot_bytes, pl.smem, s);
             break;
         case CE_PATH_ROW_SPLIT:
-            e = ce::launch_split(p, dtype, pl.split, pl.ctas, pl.nslots, pl.slot_bytes, pl.slice,
+            e = ce::launch_split(p, dtype, pl.split, pl.threads, pl.ctas, pl.nslots, pl.slot_bytes,
+                                 pl.slice,
                                  pl.smem, s);
             break;
         default:

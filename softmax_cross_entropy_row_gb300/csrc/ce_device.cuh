@@ -211,12 +211,6 @@ __device__ __forceinline__ uint4 lds128(const unsigned char *p) {
     return *reinterpret_cast<const uint4 *>(p);
 }
 
-__device__ __forceinline__ void stg128(unsigned char *p, const uint4 &v) {
-    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
 // ------------------------------------------------------------------ clusters
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -235,6 +229,18 @@ __device__ __forceinline__ uint32_t cluster_count_x() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
     return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {

@@ -25,14 +25,14 @@
 namespace ce {
 namespace {
 
-template <typename T, int K>
-__global__ void __launch_bounds__(kSplitThreads, 1)
+template <typename T, int K, int NT>
+__global__ void __launch_bounds__(NT, 1)
     row_split_kernel(Params p, int nslots, int slot_bytes, long long SE) {
     using E = Elem<T>;
-    constexpr int NT = kSplitThreads;
     constexpr int NW = NT / 32;
     constexpr int W = E::kVec;
     constexpr int ES = E::kBytes;
+    constexpr int kNoTarget = -0x40000000;
 
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[kMaxSplitSlots];
@@ -52,15 +52,17 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     const long long C = p.C;
     const long long c0 = min((long long)rank * SE, C);
     const long long c1 = min(c0 + SE, C);
+    const int slice_n = (int)(c1 - c0);
     const long long nrows = cid < p.B ? (p.B - cid + ncl - 1) / ncl : 0;
     const uint64_t lbase = reinterpret_cast<uint64_t>(p.logits);
+    const bool vec_store = p.grad_vec_ok != 0;
 
     // Byte range [gs, ge) of this CTA's slice of row `row`, and the aligned
     // span that the TMA copy can cover inside the tensor.
     auto span = [&](long long row, uint64_t &gs, uint64_t &ge, uint64_t &g0, uint64_t &lo,
                     uint64_t &hi) {
         gs = lbase + (uint64_t)(row * C + c0) * ES;
-        ge = gs + (uint64_t)(c1 - c0) * ES;
+        ge = gs + (uint64_t)slice_n * ES;
         g0 = gs & ~15ull;
         lo = g0 > p.lo_clip ? g0 : p.lo_clip;
         const uint64_t ghi = (ge + 15) & ~15ull;
@@ -114,22 +116,26 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 
         uint64_t gs, ge, g0, lo, hi;
         span(row, gs, ge, g0, lo, hi);
-        const long long e0 = c0 - (long long)((gs - g0) / ES);  // class of vector 0's first element
+        // Vector v of the slot holds the slice's local elements v*W - head ..
+        // v*W - head + W - 1; local element l is valid for 0 <= l < slice_n.
+        const int head = (int)((gs - g0) / ES);
         const int nv = (int)((((ge + 15) & ~15ull) - g0) >> 4);
-        const bool head_part = gs != g0;
+        const bool head_part = head != 0;
         const bool tail_part = (ge & 15ull) != 0;
         const int vb = head_part ? 1 : 0;
         const int ve = nv - (tail_part ? 1 : 0);
         const int rv0 = head_part ? 0 : -1;
         const int rv1 = (tail_part && nv - 1 != rv0) ? nv - 1 : -1;
+        bool has_t = t >= c0 && t < c1;
+        const int tl = has_t ? (int)(t - c0) + head : kNoTarget;  // target, vector-0 based
 
         // Elements whose bytes the copy could not cover (only at the very
         // beginning or end of an unaligned tensor): plain loads.
         if (!failed && (g0 < p.lo_clip || ((ge + 15) & ~15ull) > p.hi_clip)) {
             if (tid < 16) {
-                const long long e = tid < 8 ? c0 + tid : c1 - 16 + tid;
-                if (e >= c0 && e < c1) {
-                    const uint64_t a = gs + (uint64_t)(e - c0) * ES;
+                const int l = tid < 8 ? tid : slice_n - 16 + tid;
+                if (l >= 0 && l < slice_n) {
+                    const uint64_t a = gs + (uint64_t)l * ES;
                     if (a < lo || a + ES > hi) {
                         if (ES == 4)
                             *reinterpret_cast<uint32_t *>(slot + (a - g0)) =
@@ -142,21 +148,20 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
             }
             __syncthreads();
         }
+        const bool ragged = (tid == 0 && rv0 >= 0) || (tid == NT - 1 && rv1 >= 0);
+        const int rv = tid == 0 ? rv0 : rv1;
 
         // ---- Step 1: slice max
         float mx = -INFINITY;
         if (!failed) {
 #pragma unroll 4
             for (int v = vb + tid; v < ve; v += NT) mx = fmaxf(mx, E::vmax(lds128(slot + 16 * v)));
-            if ((tid == 0 && rv0 >= 0) || (tid == NT - 1 && rv1 >= 0)) {
-                const int v = tid == 0 ? rv0 : rv1;
+            if (ragged) {
                 float z[W];
-                E::unpack(lds128(slot + 16 * v), z);
+                E::unpack(lds128(slot + 16 * rv), z);
 #pragma unroll
-                for (int k = 0; k < W; ++k) {
-                    const long long e = e0 + (long long)v * W + k;
-                    if (e >= c0 && e < c1) mx = fmaxf(mx, z[k]);
-                }
+                for (int k = 0; k < W; ++k)
+                    if ((unsigned)(rv * W + k - head) < (unsigned)slice_n) mx = fmaxf(mx, z[k]);
             }
         }
         mx = warp_max(mx);
@@ -176,8 +181,8 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
             for (int v = vb + tid; v < ve; v += NT) {
                 float z[W];
                 E::unpack(lds128(slot + 16 * v), z);
-                const long long d = t - (e0 + (long long)v * W);
-                if ((unsigned long long)d < (unsigned long long)W) {
+                const int d = tl - v * W;
+                if ((unsigned)d < (unsigned)W) {
 #pragma unroll
                     for (int k = 0; k < W; ++k)
                         if (k != d) sa += ex2(fmaf(z[k], kLog2e, -M));
@@ -189,14 +194,14 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                     }
                 }
             }
-            if ((tid == 0 && rv0 >= 0) || (tid == NT - 1 && rv1 >= 0)) {
-                const int v = tid == 0 ? rv0 : rv1;
+            if (ragged) {
                 float z[W];
-                E::unpack(lds128(slot + 16 * v), z);
+                E::unpack(lds128(slot + 16 * rv), z);
 #pragma unroll
                 for (int k = 0; k < W; ++k) {
-                    const long long e = e0 + (long long)v * W + k;
-                    if (e >= c0 && e < c1 && e != t) sa += ex2(fmaf(z[k], kLog2e, -M));
+                    const int e = rv * W + k;
+                    if ((unsigned)(e - head) < (unsigned)slice_n && e != tl)
+                        sa += ex2(fmaf(z[k], kLog2e, -M));
                 }
             }
         }
@@ -207,15 +212,19 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
 #pragma unroll
         for (int w = 1; w < NW; ++w) S += red_b[w];
 
-        bool has_t = t >= c0 && t < c1;
         float zt = 0.f;
-        if (has_t && !failed) zt = E::load(slot + (gs - g0) + (size_t)(t - c0) * ES);
+        if (has_t && !failed) zt = E::load(slot + (size_t)tl * ES);
 
         if (K > 1) {
             // Combine the K slices' (M_r, S_r) in rank order; every CTA of the
-            // cluster computes the same bits.
+            // cluster computes the same bits.  Only warp 0 publishes, so only
+            // warp 0 arrives with release semantics.
             if (tid == 0) part[j & 1] = make_float4(M, S, zt, has_t ? 1.f : 0.f);
-            cluster_sync();
+            if (warp == 0)
+                cluster_arrive_release();
+            else
+                cluster_arrive_relaxed();
+            cluster_wait();
             if (warp == 0) {
                 float4 q = make_float4(-INFINITY, 0.f, 0.f, 0.f);
                 if (lane < K) q = ld_dsmem_f4(&part[j & 1], (uint32_t)lane);
@@ -255,7 +264,6 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
         const float g_t = -s_rest * scale;
         if (!failed) {
             unsigned char *gbase = p.grad + (g0 - lbase);  // grad byte of vector 0
-            const bool vec_store = p.grad_vec_ok != 0;
 #pragma unroll 2
             for (int v = vb + tid; v < ve; v += NT) {
                 float z[W];
@@ -263,29 +271,28 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
                 float g[W];
 #pragma unroll
                 for (int k = 0; k < W; ++k) g[k] = ex2(fmaf(z[k], kLog2e, -M)) * scale;
-                const long long d = t - (e0 + (long long)v * W);
-                if ((unsigned long long)d < (unsigned long long)W) {
+                const int d = tl - v * W;
+                if ((unsigned)d < (unsigned)W) {
 #pragma unroll
                     for (int k = 0; k < W; ++k)
                         if (k == d) g[k] = g_t;
                 }
                 if (vec_store) {
-                    stg128(gbase + 16 * (size_t)v, E::pack(g));
+                    *reinterpret_cast<uint4 *>(gbase + 16 * v) = E::pack(g);
                 } else {
 #pragma unroll
-                    for (int k = 0; k < W; ++k) E::store(gbase + 16 * (size_t)v + k * ES, g[k]);
+                    for (int k = 0; k < W; ++k) E::store(gbase + 16 * v + k * ES, g[k]);
                 }
             }
-            if ((tid == 0 && rv0 >= 0) || (tid == NT - 1 && rv1 >= 0)) {
-                const int v = tid == 0 ? rv0 : rv1;
+            if (ragged) {
                 float z[W];
-                E::unpack(lds128(slot + 16 * v), z);
+                E::unpack(lds128(slot + 16 * rv), z);
 #pragma unroll
                 for (int k = 0; k < W; ++k) {
-                    const long long e = e0 + (long long)v * W + k;
-                    if (e >= c0 && e < c1) {
-                        const float gv = e == t ? g_t : ex2(fmaf(z[k], kLog2e, -M)) * scale;
-                        E::store(gbase + 16 * (size_t)v + k * ES, gv);
+                    const int e = rv * W + k;
+                    if ((unsigned)(e - head) < (unsigned)slice_n) {
+                        const float gv = e == tl ? g_t : ex2(fmaf(z[k], kLog2e, -M)) * scale;
+                        E::store(gbase + 16 * rv + k * ES, gv);
                     }
                 }
             }
@@ -325,15 +332,15 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     finish_cta(p, &tail_flag, tail_scratch);
 }
 
-template <typename T, int K>
+template <typename T, int K, int NT>
 cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long long se,
                      int smem, cudaStream_t s) {
-    auto kern = row_split_kernel<T, K>;
+    auto kern = row_split_kernel<T, K, NT>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas, 1, 1);
-    cfg.blockDim = dim3(kSplitThreads, 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -348,9 +355,9 @@ cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long
     return cudaLaunchKernelEx(&cfg, kern, p, nslots, slot_bytes, se);
 }
 
-template <typename T, int K>
+template <typename T, int K, int NT>
 cudaError_t max_clusters_k(int smem, int *clusters) {
-    auto kern = row_split_kernel<T, K>;
+    auto kern = row_split_kernel<T, K, NT>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     if (K == 1) {
@@ -358,14 +365,14 @@ cudaError_t max_clusters_k(int smem, int *clusters) {
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSplitThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
         if (e != cudaSuccess) return e;
         *clusters = sms * per_sm;
         return cudaSuccess;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(K, 1, 1);
-    cfg.blockDim = dim3(kSplitThreads, 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -377,40 +384,56 @@ cudaError_t max_clusters_k(int smem, int *clusters) {
     return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
 }
 
-template <typename T>
-cudaError_t launch_t(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
+template <typename T, int NT>
+cudaError_t launch_n(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
                      int smem, cudaStream_t s) {
     switch (K) {
-        case 1: return launch_k<T, 1>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 2: return launch_k<T, 2>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 4: return launch_k<T, 4>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 8: return launch_k<T, 8>(p, ctas, nslots, slot_bytes, se, smem, s);
+        case 1: return launch_k<T, 1, NT>(p, ctas, nslots, slot_bytes, se, smem, s);
+        case 2: return launch_k<T, 2, NT>(p, ctas, nslots, slot_bytes, se, smem, s);
+        case 4: return launch_k<T, 4, NT>(p, ctas, nslots, slot_bytes, se, smem, s);
+        case 8: return launch_k<T, 8, NT>(p, ctas, nslots, slot_bytes, se, smem, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T, int NT>
+cudaError_t max_clusters_n(int K, int smem, int *clusters) {
+    switch (K) {
+        case 1: return max_clusters_k<T, 1, NT>(smem, clusters);
+        case 2: return max_clusters_k<T, 2, NT>(smem, clusters);
+        case 4: return max_clusters_k<T, 4, NT>(smem, clusters);
+        case 8: return max_clusters_k<T, 8, NT>(smem, clusters);
         default: return cudaErrorInvalidValue;
     }
 }
 
 template <typename T>
-cudaError_t max_clusters_t(int K, int smem, int *clusters) {
-    switch (K) {
-        case 1: return max_clusters_k<T, 1>(smem, clusters);
-        case 2: return max_clusters_k<T, 2>(smem, clusters);
-        case 4: return max_clusters_k<T, 4>(smem, clusters);
-        case 8: return max_clusters_k<T, 8>(smem, clusters);
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t launch_t(const Params &p, int K, int threads, int ctas, int nslots, int slot_bytes,
+                     long long se, int smem, cudaStream_t s) {
+    if (threads == 1024) return launch_n<T, 1024>(p, K, ctas, nslots, slot_bytes, se, smem, s);
+    if (threads == 512) return launch_n<T, 512>(p, K, ctas, nslots, slot_bytes, se, smem, s);
+    return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t max_clusters_t(int K, int threads, int smem, int *clusters) {
+    if (threads == 1024) return max_clusters_n<T, 1024>(K, smem, clusters);
+    if (threads == 512) return max_clusters_n<T, 512>(K, smem, clusters);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_split(const Params &p, int dtype, int K, int ctas, int nslots,
+cudaError_t launch_split(const Params &p, int dtype, int K, int threads, int ctas, int nslots,
                          int slot_bytes, long long slice_elems, int smem, cudaStream_t s) {
-    if (dtype == 0) return launch_t<float>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);
-    return launch_t<__nv_bfloat16>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);
+    if (dtype == 0)
+        return launch_t<float>(p, K, threads, ctas, nslots, slot_bytes, slice_elems, smem, s);
+    return launch_t<__nv_bfloat16>(p, K, threads, ctas, nslots, slot_bytes, slice_elems, smem, s);
 }
 
-cudaError_t split_max_clusters(int dtype, int K, int smem, int *clusters) {
-    if (dtype == 0) return max_clusters_t<float>(K, smem, clusters);
-    return max_clusters_t<__nv_bfloat16>(K, smem, clusters);
+cudaError_t split_max_clusters(int dtype, int K, int threads, int smem, int *clusters) {
+    if (dtype == 0) return max_clusters_t<float>(K, threads, smem, clusters);
+    return max_clusters_t<__nv_bfloat16>(K, threads, smem, clusters);
 }
 
 }  // namespace ce

@@ -1,12 +1,13 @@
-// Warp-per-row kernel for rows of at most a few KB (classifier heads).
+// Warp-per-row kernel for rows of at most 8 KB (classifier heads).
 //
 // Each warp owns a private ring of `slots` shared-memory tiles; a tile is
 // `rows_per_tile` consecutive rows of the logits, staged by one TMA bulk copy.
 // Warps act as their own producers, so no CTA-wide barrier is needed until
-// the fused batch-loss tail.  Per row the warp computes Steps 1-4 of Pass 1 of
-// rumus 0.1.1's cross_entropy.wgsl (max, sum of exponentials, row loss,
-// gradient) from the staged copy, with warp-shuffle reductions; the last CTA
-// to finish performs Pass 2 (the fixed-order batch-loss sum).
+// the fused batch-loss tail.  A row is read from shared memory once, into
+// registers (16-byte vectors, at most MAXV per lane), and every step runs
+// from there: Steps 1-4 of Pass 1 of rumus 0.1.1's cross_entropy.wgsl (max,
+// sum of exponentials, row loss, gradient) with warp-shuffle reductions; the
+// last CTA to finish performs Pass 2 (the fixed-order batch-loss sum).
 #include <math.h>
 
 #include "ce_launch.h"
@@ -14,12 +15,14 @@
 namespace ce {
 namespace {
 
-template <typename T>
+template <typename T, int MAXV>
 __global__ void __launch_bounds__(kWarpKernelWarps * 32)
     rows_warp_kernel(Params p, int slots, int rows_per_tile, int slot_bytes) {
     using E = Elem<T>;
     constexpr int NW = kWarpKernelWarps;
     constexpr int ES = E::kBytes;
+    constexpr int W = E::kVec;
+    constexpr bool kKeepExp = sizeof(T) == 4;  // fp32: exponentials replace the logits in place
 
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[NW * kMaxWarpSlots];
@@ -29,7 +32,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32)
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const long long B = p.B;
-    const long long C = p.C;
+    const int C = (int)p.C;  // at most 4096 on this path
     const long long R = rows_per_tile;
     const long long ntiles = (B + R - 1) / R;
     const long long gw = (long long)blockIdx.x * NW + warp;
@@ -38,6 +41,8 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32)
     const uint64_t lbase = reinterpret_cast<uint64_t>(p.logits);
     unsigned char *my_slots = smem + (size_t)warp * slots * slot_bytes;
     uint64_t *my_full = full + warp * kMaxWarpSlots;
+    const bool vec_store = p.grad_vec_ok != 0;
+    const float inv_b = p.inv_b;
 
     auto span = [&](long long tile, long long &r0, long long &r1, uint64_t &gs, uint64_t &ge,
                     uint64_t &g0, uint64_t &lo, uint64_t &hi) {
@@ -77,7 +82,6 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32)
 
     bool failed = false;
     long long consumed = 0;
-    const float inv_b = p.inv_b;
 
     for (long long i = 0; i < ntl; ++i) {
         const int s = (int)(i % slots);
@@ -86,6 +90,8 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32)
         long long r0, r1;
         uint64_t gs, ge, g0, lo, hi;
         span(gw + i * TW, r0, r1, gs, ge, g0, lo, hi);
+        // the tile's first targets, in flight while the copy lands
+        int tchunk = r0 + lane < r1 ? __ldg(p.targets + r0 + lane) : 0;
 
         if (!failed) {
             if (mbar_wait(&my_full[s], parity)) {
@@ -119,37 +125,107 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32)
         }
 
         for (long long r = r0; r < r1; ++r) {
-            const unsigned char *row = slot + (gs - g0) + (size_t)((r - r0) * C) * ES;
-            const long long t = __ldg(p.targets + r);
+            const int q = (int)(r - r0);
+            if (q > 0 && (q & 31) == 0) tchunk = r + lane < r1 ? __ldg(p.targets + r + lane) : 0;
+            const int t = __shfl_sync(0xffffffffu, tchunk, q & 31);
+            const bool has_t = t >= 0 && t < C;
+
+            // Row layout in shared memory: nh head elements up to the first
+            // 16-byte boundary, nvec whole vectors, nt tail elements.
+            const unsigned char *row = slot + (gs - g0) + (size_t)q * C * ES;
+            const uint32_t ph = smem_addr(row) & 15u;
+            const int nh = ph ? min((int)((16u - ph) / ES), C) : 0;
+            const int nvec = (C - nh) / W;
+            const int nt = C - nh - nvec * W;
+            const unsigned char *vrow = row + nh * ES;
+            const int tv = has_t ? t - nh : -0x40000000;  // target relative to vector 0
+
+            uint4 x[MAXV];
+#pragma unroll
+            for (int k = 0; k < MAXV; ++k) {
+                const int v = lane + 32 * k;
+                if (v < nvec) x[k] = lds128(vrow + 16 * v);
+            }
+            const float hz = lane < nh ? E::load(row + lane * ES) : -INFINITY;
+            const float tz = lane < nt ? E::load(vrow + (nvec * W + lane) * ES) : -INFINITY;
+
             // Step 1: max
-            float m = -INFINITY;
-            for (long long c = lane; c < C; c += 32) m = fmaxf(m, E::load(row + c * ES));
+            float m = fmaxf(hz, tz);
+#pragma unroll
+            for (int k = 0; k < MAXV; ++k)
+                if (lane + 32 * k < nvec) m = fmaxf(m, E::vmax(x[k]));
             m = warp_max(m);
             const float M = m * kLog2e;
-            // Step 2: sum of exponentials without the target's term (added
-            // back below, so that 1 - p_t keeps its relative precision)
+
+            // Step 2: sum of exponentials without the target's term
             float sa = 0.f, sb = 0.f;
-            long long c = lane;
-            for (; c + 32 < C; c += 64) {
-                const float ea = ex2(fmaf(E::load(row + c * ES), kLog2e, -M));
-                const float eb = ex2(fmaf(E::load(row + (c + 32) * ES), kLog2e, -M));
-                sa += c == t ? 0.f : ea;
-                sb += c + 32 == t ? 0.f : eb;
+#pragma unroll
+            for (int k = 0; k < MAXV; ++k) {
+                const int v = lane + 32 * k;
+                if (v < nvec) {
+                    float z[W];
+                    E::unpack(x[k], z);
+                    const int d = tv - v * W;
+#pragma unroll
+                    for (int j = 0; j < W; ++j) {
+                        const float e = ex2(fmaf(z[j], kLog2e, -M));
+                        if (kKeepExp) z[j] = e;
+                        if (j != d) {
+                            if (j & 1) sb += e; else sa += e;
+                        }
+                    }
+                    if (kKeepExp) x[k] = E::pack(z);
+                }
             }
-            if (c < C && c != t) sa += ex2(fmaf(E::load(row + c * ES), kLog2e, -M));
+            const float eh = lane < nh ? ex2(fmaf(hz, kLog2e, -M)) : 0.f;
+            const float et = lane < nt ? ex2(fmaf(tz, kLog2e, -M)) : 0.f;
+            if (lane != t) sa += eh;
+            if (nh + nvec * W + lane != t) sb += et;
             const float s_rest = warp_sum(sa + sb);
-            const bool has_t = t >= 0 && t < C;
             const float zt = has_t ? E::load(row + t * ES) : 0.f;
             const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
             const float S = s_rest + e_t;
+
             // Step 4: gradient; (p_t - 1) / B = -S_rest / (S B)
             const float scale = (1.0f / S) * inv_b;
             const float g_t = -s_rest * scale;
-            unsigned char *grow = p.grad + (size_t)(r * C) * ES;
-            for (long long k = lane; k < C; k += 32) {
-                const float ev = ex2(fmaf(E::load(row + k * ES), kLog2e, -M));
-                E::store(grow + k * ES, k == t ? g_t : ev * scale);
+            unsigned char *grow = p.grad + (size_t)r * C * ES;
+            unsigned char *gvec = grow + nh * ES;
+#pragma unroll
+            for (int k = 0; k < MAXV; ++k) {
+                const int v = lane + 32 * k;
+                if (v < nvec) {
+                    float g[W];
+                    if (kKeepExp) {
+                        E::unpack(x[k], g);
+#pragma unroll
+                        for (int j = 0; j < W; ++j) g[j] *= scale;
+                    } else {
+                        float z[W];
+                        E::unpack(x[k], z);
+#pragma unroll
+                        for (int j = 0; j < W; ++j) g[j] = ex2(fmaf(z[j], kLog2e, -M)) * scale;
+                    }
+                    const int d = tv - v * W;
+                    if ((unsigned)d < (unsigned)W) {
+#pragma unroll
+                        for (int j = 0; j < W; ++j)
+                            if (j == d) g[j] = g_t;
+                    }
+                    if (vec_store) {
+                        *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack(g);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < W; ++j) E::store(gvec + (v * W + j) * ES, g[j]);
+                    }
+                }
             }
+            if (lane < nh) E::store(grow + lane * ES, lane == t ? g_t : eh * scale);
+            if (lane < nt) {
+                const int c = nh + nvec * W + lane;
+                E::store(grow + c * ES, c == t ? g_t : et * scale);
+            }
+
             // Step 3: loss of the row, log(S / e_t)
             if (lane == 0) {
                 float l;
@@ -179,10 +255,10 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32)
     finish_cta(p, &tail_flag, tail_scratch);
 }
 
-template <typename T>
-cudaError_t launch_t(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
+template <typename T, int MAXV>
+cudaError_t launch_v(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
                      int smem, cudaStream_t s) {
-    auto kern = rows_warp_kernel<T>;
+    auto kern = rows_warp_kernel<T, MAXV>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -193,12 +269,40 @@ cudaError_t launch_t(const Params &p, int ctas, int slots, int rows_per_tile, in
     return cudaLaunchKernelEx(&cfg, kern, p, slots, rows_per_tile, slot_bytes);
 }
 
-template <typename T>
-cudaError_t occ_t(int smem, int *ctas) {
-    auto kern = rows_warp_kernel<T>;
+template <typename T, int MAXV>
+cudaError_t occ_v(int smem, int *ctas) {
+    auto kern = rows_warp_kernel<T, MAXV>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, kWarpKernelWarps * 32, smem);
+}
+
+// Vectors per lane: a row of C elements has at most C*ES/16 whole vectors.
+int maxv_for(long long C, int es) {
+    const long long nvec = C * es / 16;
+    const long long per_lane = (nvec + 31) / 32;
+    return per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8 : 16;
+}
+
+template <typename T>
+cudaError_t launch_t(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
+                     int smem, cudaStream_t s) {
+    switch (maxv_for(p.C, sizeof(T))) {
+        case 2: return launch_v<T, 2>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+        case 4: return launch_v<T, 4>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+        case 8: return launch_v<T, 8>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+        default: return launch_v<T, 16>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+    }
+}
+
+template <typename T>
+cudaError_t occ_t(long long C, int smem, int *ctas) {
+    switch (maxv_for(C, sizeof(T))) {
+        case 2: return occ_v<T, 2>(smem, ctas);
+        case 4: return occ_v<T, 4>(smem, ctas);
+        case 8: return occ_v<T, 8>(smem, ctas);
+        default: return occ_v<T, 16>(smem, ctas);
+    }
 }
 
 }  // namespace
@@ -209,9 +313,9 @@ cudaError_t launch_rows_warp(const Params &p, int dtype, int ctas, int slots, in
     return launch_t<__nv_bfloat16>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
 }
 
-cudaError_t rows_warp_max_ctas_per_sm(int dtype, int smem, int *ctas) {
-    if (dtype == 0) return occ_t<float>(smem, ctas);
-    return occ_t<__nv_bfloat16>(smem, ctas);
+cudaError_t rows_warp_max_ctas_per_sm(int dtype, long long C, int smem, int *ctas) {
+    if (dtype == 0) return occ_t<float>(C, smem, ctas);
+    return occ_t<__nv_bfloat16>(C, smem, ctas);
 }
 
 }  // namespace ce
