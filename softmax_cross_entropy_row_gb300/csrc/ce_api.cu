@@ -100,15 +100,25 @@ struct Plan {
     int slot_bytes = 0;
     long long slice = 0;  // classes per slice (split path)
     int rows_per_tile = 0;
+    int per_sm = 1;       // warp path: the build for 1 or 2 resident CTAs per SM
     long long chunks = 0; // stream path
 };
 
 constexpr int kStaticSmemReserve = 2048;       // static __shared__ of the kernels
 constexpr long long kWarpRowMax = 8192;        // bytes: warp-per-row path up to here
 constexpr long long kWarpTileTarget = 2048;    // bytes of rows per warp tile
-constexpr long long kSplitSliceTarget = 65536; // bytes per CTA slice when K allows
 
 int round_up(long long v, long long a) { return (int)((v + a - 1) / a * a); }
+
+// Tuning knob: CE_WARP_PER_SM=1 or 2 forces the warp path's CTAs per SM
+// (0 or unset: chosen from the shape).  Read once.
+int warp_per_sm_override() {
+    static const int n = [] {
+        const char *e = getenv("CE_WARP_PER_SM");
+        return e ? atoi(e) : 0;
+    }();
+    return n;
+}
 
 int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, Plan *pl) {
     const long long row_bytes = C * es;
@@ -117,86 +127,80 @@ int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, 
     if (R < 1) R = 1;
     if (R > B) R = B;
     const int slot_bytes = round_up(R * row_bytes + 32, 128);
-    const int budget = d.smem_optin - kStaticSmemReserve;
-    int slots = ce::kMaxWarpSlots;
-    while (slots > 1 && (long long)slots * slot_bytes * ce::kWarpKernelWarps > budget) --slots;
-    if ((long long)slots * slot_bytes * ce::kWarpKernelWarps > budget) return CE_ERR_PATH;
-    // Smaller rings than the budget allows when all tiles fit anyway.
     const long long ntiles = (B + R - 1) / R;
-    const int smem = slots * slot_bytes * ce::kWarpKernelWarps;
+    const int NW = ce::kWarpKernelWarps;
+    // Two CTAs per SM with one staged tile per warp when every tile then has
+    // a warp of its own (all copies in flight at once, twice the warps to hide
+    // latency); otherwise one CTA per SM with a ring of up to four tiles per warp.
+    int want = 1;
+    int slots = 1;
+    const int half_budget = d.smem_optin / 2 - kStaticSmemReserve;
+    const int force = warp_per_sm_override();
+    if (force != 1 && (force == 2 || ntiles <= 2LL * NW * d.sms) &&
+        (long long)slot_bytes * NW <= half_budget) {
+        want = 2;
+    } else {
+        const int budget = d.smem_optin - kStaticSmemReserve;
+        slots = ce::kMaxWarpSlots;
+        while (slots > 1 && (long long)slots * slot_bytes * NW > budget) --slots;
+        if ((long long)slots * slot_bytes * NW > budget) return CE_ERR_PATH;
+    }
+    const int smem = slots * slot_bytes * NW;
     int per_sm = 1;
-    int rc = cached_occupancy(dtype, CE_PATH_ROWS_WARP, (int)C, smem,
-                              [&](int *v) { return ce::rows_warp_max_ctas_per_sm(dtype, C, smem, v); },
-                              &per_sm);
+    int rc = cached_occupancy(
+        dtype, CE_PATH_ROWS_WARP, (int)C * 4 + want, smem,
+        [&](int *v) { return ce::rows_warp_max_ctas_per_sm(dtype, want, C, smem, v); }, &per_sm);
     if (rc != CE_OK) return rc;
     if (per_sm < 1) return CE_ERR_PATH;
-    long long ctas = (ntiles + ce::kWarpKernelWarps - 1) / ce::kWarpKernelWarps;
+    if (per_sm > want) per_sm = want;
+    long long ctas = (ntiles + NW - 1) / NW;
     const long long cap = (long long)d.sms * per_sm;
     if (ctas > cap) ctas = cap;
     pl->path = CE_PATH_ROWS_WARP;
     pl->split = 1;
     pl->ctas = (int)ctas;
-    pl->threads = ce::kWarpKernelWarps * 32;
+    pl->threads = NW * 32;
     pl->smem = smem;
     pl->launches = 1;
     pl->nslots = slots;
     pl->slot_bytes = slot_bytes;
     pl->rows_per_tile = (int)R;
+    pl->per_sm = want;
     return CE_OK;
-}
-
-// Threads per CTA of the split-row kernel: 1024, or 512 when the environment
-// variable CE_SPLIT_THREADS says so (a tuning knob, read once).
-int split_threads() {
-    static const int n = [] {
-        const char *e = getenv("CE_SPLIT_THREADS");
-        if (e && atoi(e) == 512) return 512;
-        return ce::kSplitThreads;
-    }();
-    return n;
 }
 
 int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype, int K_forced,
                Plan *pl) {
     const int budget = d.smem_optin - kStaticSmemReserve;
+    // A CTA holds a slice of at most kSplitThreads * kSplitVecs 16-byte vectors
+    // in registers; its slot is one such slice plus the alignment margin.
+    const long long max_slice_bytes = (long long)ce::kSplitThreads * ce::kSplitVecs * 16 - 16;
     auto slice_of = [&](int K) {
         long long se = (C + K - 1) / K;
         return (se + 7) / 8 * 8;  // slices start 16-byte aligned relative to the row
     };
-    auto slot_of = [&](long long se) { return (long long)round_up(se * es + 32, 128); };
+    auto fits = [&](int K) { return slice_of(K) * es <= max_slice_bytes; };
     int K = K_forced;
     if (K == 0) {
-        // Smallest cluster whose slices are at most the target size; else the
-        // smallest whose slice fits shared memory at all.
         for (int k : {1, 2, 4, 8}) {
-            if (slot_of(slice_of(k)) <= kSplitSliceTarget + 128 && slice_of(k) > 0) {
+            if (fits(k)) {
                 K = k;
                 break;
-            }
-        }
-        if (K == 0) {
-            for (int k : {1, 2, 4, 8}) {
-                if (slot_of(slice_of(k)) <= budget) {
-                    K = k;
-                    break;
-                }
             }
         }
         if (K == 0) return CE_ERR_PATH;
     }
     if (K != 1 && K != 2 && K != 4 && K != 8) return CE_ERR_PATH;
+    if (!fits(K)) return CE_ERR_PATH;
     const long long se = slice_of(K);
-    const long long slot_bytes = slot_of(se);
+    const long long slot_bytes = round_up(se * es + 32, 128);
     if (slot_bytes > budget) return CE_ERR_PATH;
     int nslots = (int)(budget / slot_bytes);
     if (nslots > ce::kMaxSplitSlots) nslots = ce::kMaxSplitSlots;
     const int smem = nslots * (int)slot_bytes;
     int clusters = 0;
-    const int threads = split_threads();
-    int rc = cached_occupancy(dtype, CE_PATH_ROW_SPLIT, K * 4096 + threads, smem,
-                              [&](int *v) {
-                                  return ce::split_max_clusters(dtype, K, threads, smem, v);
-                              },
+    int rc = cached_occupancy(dtype, CE_PATH_ROW_SPLIT, K, smem,
+                              [&](int *v) { return ce::split_max_clusters(dtype, K, smem, v); },
                               &clusters);
     if (rc != CE_OK) return rc;
     if (clusters < 1) return CE_ERR_PATH;
@@ -204,7 +208,7 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     pl->path = CE_PATH_ROW_SPLIT;
     pl->split = K;
     pl->ctas = clusters * K;
-    pl->threads = threads;
+    pl->threads = ce::kSplitThreads;
     pl->smem = smem;
     pl->launches = 1;
     pl->nslots = nslots;
@@ -380,12 +384,11 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
 
     switch (pl.path) {
         case CE_PATH_ROWS_WARP:
-            e = ce::launch_rows_warp(p, dtype, pl.ctas, pl.nslots, pl.rows_per_tile,
+            e = ce::launch_rows_warp(p, dtype, pl.per_sm, pl.ctas, pl.nslots, pl.rows_per_tile,
                                      pl.slot_bytes, pl.smem, s);
             break;
         case CE_PATH_ROW_SPLIT:
-            e = ce::launch_split(p, dtype, pl.split, pl.threads, pl.ctas, pl.nslots, pl.slot_bytes,
-                                 pl.slice,
+            e = ce::launch_split(p, dtype, pl.split, pl.ctas, pl.nslots, pl.slot_bytes, pl.slice,
                                  pl.smem, s);
             break;
         default:

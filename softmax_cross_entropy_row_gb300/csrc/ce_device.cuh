@@ -271,65 +271,66 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     e = (a - (s - bb)) + (b - bb);
 }
 
-// Number of lanes of the fixed-order tail reduction.  Every kernel launches at
-// least this many threads per CTA, so the summation order depends only on B.
+// The batch loss L = (1/B) * sum_b loss_rows[b] is summed in one fixed order
+// that depends only on B, with compensated (float, float) accumulators:
+//   virtual lane i (of 256) sums rows 4i..4i+3, 4i+1024..4i+1027, ... in order;
+//   virtual warp w (lanes 32w..32w+31) combines its lanes in a shuffle-down tree;
+//   the 8 virtual warps are added in order.
+// Any number of real warps may evaluate it: the bits are the same.
 constexpr int kTailThreads = 256;
+constexpr int kTailWarps = kTailThreads / 32;
 
-// L = (1/B) * sum_b loss_rows[b], summed in a fixed order with a compensated
-// (float, float) accumulator: lane i sums rows 4i..4i+3, 4i+1024.. in order,
-// then the lanes combine in a fixed tree.  Called by every thread of the last
-// CTA to finish; threads >= kTailThreads only take part in the barriers.
-__device__ __forceinline__ void batch_loss_tail(const Params &p, float2 *scratch /* [8] */) {
-    const int tid = threadIdx.x;
+// Total of virtual warp `vw`, valid in lane 0 of the calling warp.
+__device__ __forceinline__ float2 tail_virtual_warp(const Params &p, int vw, int lane) {
+    const int vl = vw * 32 + lane;
+    const long long B = p.B;
     float hi = 0.f, lo = 0.f;
-    if (tid < kTailThreads) {
-        const long long B = p.B;
-        for (long long base = 4LL * tid; base < B; base += 4LL * kTailThreads) {
-            float x[4];
-            if (base + 3 < B) {
-                float4 q = __ldcg(reinterpret_cast<const float4 *>(p.loss_rows + base));
-                x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
-            } else {
+    for (long long base = 4LL * vl; base < B; base += 4LL * kTailThreads) {
+        float x[4];
+        if (base + 3 < B) {
+            const float4 q = __ldcg(reinterpret_cast<const float4 *>(p.loss_rows + base));
+            x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+        } else {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) x[k] = base + k < B ? __ldcg(p.loss_rows + base + k) : 0.f;
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float s, e;
-                two_sum(hi, x[k], s, e);
-                hi = s;
-                lo += e;
-            }
+            for (int k = 0; k < 4; ++k) x[k] = base + k < B ? __ldcg(p.loss_rows + base + k) : 0.f;
         }
-        // fixed tree inside the warp (lane 0 ends with the warp's total)
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float h2 = __shfl_down_sync(0xffffffffu, hi, o);
-            float l2 = __shfl_down_sync(0xffffffffu, lo, o);
+        for (int k = 0; k < 4; ++k) {
             float s, e;
-            two_sum(hi, h2, s, e);
+            two_sum(hi, x[k], s, e);
             hi = s;
-            lo += l2 + e;
+            lo += e;
         }
-        if ((tid & 31) == 0) scratch[tid >> 5] = make_float2(hi, lo);
     }
-    __syncthreads();
-    if (tid == 0) {
-        float h = 0.f, l = 0.f;
-        for (int w = 0; w < kTailThreads / 32; ++w) {
-            float s, e;
-            two_sum(h, scratch[w].x, s, e);
-            h = s;
-            l += scratch[w].y + e;
-        }
-        const double total = static_cast<double>(h) + static_cast<double>(l);
-        *p.loss_out = static_cast<float>(total / static_cast<double>(p.B));
-        *p.ticket = 0u;  // ready for the next launch on this workspace
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_down_sync(0xffffffffu, hi, o);
+        const float l2 = __shfl_down_sync(0xffffffffu, lo, o);
+        float s, e;
+        two_sum(hi, h2, s, e);
+        hi = s;
+        lo += l2 + e;
     }
+    return make_float2(hi, lo);
 }
 
-// Called once per CTA after its last row loss is stored.  The CTA that
-// finishes last reduces the batch loss.  `flag` and `scratch` are shared.
+// Adds the 8 virtual-warp totals in order, writes L and re-arms the ticket.
+__device__ __forceinline__ void tail_write(const Params &p, const float2 *vw_totals) {
+    float h = 0.f, l = 0.f;
+    for (int w = 0; w < kTailWarps; ++w) {
+        float s, e;
+        two_sum(h, vw_totals[w].x, s, e);
+        h = s;
+        l += vw_totals[w].y + e;
+    }
+    const double total = static_cast<double>(h) + static_cast<double>(l);
+    *p.loss_out = static_cast<float>(total / static_cast<double>(p.B));
+    *p.ticket = 0u;  // ready for the next launch on this workspace
+}
+
+// CTA-wide completion: called by every thread once the CTA's row losses are
+// stored.  The CTA that finishes last evaluates the batch loss, one virtual
+// warp per real warp.  `flag` and `scratch` ([8]) live in shared memory.
 __device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *scratch) {
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -341,7 +342,43 @@ __device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *s
     __syncthreads();
     if (*flag) {
         __threadfence();
-        batch_loss_tail(p, scratch);
+        const int warp = threadIdx.x >> 5;
+        const int lane = threadIdx.x & 31;
+        for (int vw = warp; vw < kTailWarps; vw += blockDim.x >> 5) {
+            const float2 v = tail_virtual_warp(p, vw, lane);
+            if (lane == 0) scratch[vw] = v;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) tail_write(p, scratch);
+    }
+}
+
+// Warp-granular completion: called by every lane of a warp once the warp's
+// row losses are stored.  The last warp of each CTA (counted in shared memory
+// through `cta_count`, zeroed before any warp finishes) takes the CTA's global
+// ticket; the warp that takes the last ticket evaluates the batch loss alone.
+// No CTA-wide barrier: warps retire as soon as they are done.
+__device__ __forceinline__ void finish_warp(const Params &p, unsigned int *cta_count) {
+    const int lane = threadIdx.x & 31;
+    const unsigned int nwarps = blockDim.x >> 5;
+    unsigned int last = 0;
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence();
+        const unsigned int prev = atomicAdd(cta_count, 1u);
+        if (prev == nwarps - 1u) {
+            __threadfence();
+            const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
+            last = atomicAdd(p.ticket, 1u) == total - 1u;
+        }
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+        __threadfence();
+        float2 totals[kTailWarps];
+#pragma unroll
+        for (int vw = 0; vw < kTailWarps; ++vw) totals[vw] = tail_virtual_warp(p, vw, lane);
+        if (lane == 0) tail_write(p, totals);
     }
 }
 

@@ -13,7 +13,8 @@ namespace ce {
 cudaError_t ensure_smem_attr(const void *func, int smem);
 
 // Threads per CTA of each path.
-constexpr int kSplitThreads = 1024;  // default; 512 is also built
+constexpr int kSplitThreads = 512;
+constexpr int kSplitVecs = 8;  // 16-byte vectors per thread: slices of at most 64 KB
 constexpr int kWarpKernelWarps = 16;
 constexpr int kStreamThreads = 256;
 constexpr int kStreamPerThread = 16;  // elements each thread keeps in registers
@@ -25,17 +26,17 @@ constexpr int kMaxWarpSlots = 4;  // per warp
 
 // Split-row path: one row (K = 1) or one slice of a row per CTA of a cluster
 // of K CTAs; `nslots` staged slices of `slot_bytes` each per CTA.
-// `threads` is 512 or 1024.
-cudaError_t launch_split(const Params &p, int dtype, int K, int threads, int ctas, int nslots,
+cudaError_t launch_split(const Params &p, int dtype, int K, int ctas, int nslots,
                          int slot_bytes, long long slice_elems, int smem, cudaStream_t s);
 // Largest number of co-resident clusters of K CTAs with `smem` dynamic bytes.
-cudaError_t split_max_clusters(int dtype, int K, int threads, int smem, int *clusters);
+cudaError_t split_max_clusters(int dtype, int K, int smem, int *clusters);
 
 // Warp-per-row path: tiles of `rows_per_tile` consecutive rows, `slots` tiles
-// staged per warp.
-cudaError_t launch_rows_warp(const Params &p, int dtype, int ctas, int slots,
+// staged per warp; `per_sm` (1 or 2) selects the build made for that many
+// resident CTAs per SM.
+cudaError_t launch_rows_warp(const Params &p, int dtype, int per_sm, int ctas, int slots,
                              int rows_per_tile, int slot_bytes, int smem, cudaStream_t s);
-cudaError_t rows_warp_max_ctas_per_sm(int dtype, long long C, int smem, int *ctas);
+cudaError_t rows_warp_max_ctas_per_sm(int dtype, int per_sm, long long C, int smem, int *ctas);
 
 // Streaming path: pass A (chunk partials) and pass B (combine, gradient, loss).
 cudaError_t launch_stream(const Params &p, int dtype, long long chunks, cudaStream_t s);

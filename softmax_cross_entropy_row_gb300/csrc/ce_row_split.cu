@@ -1,17 +1,21 @@
 // Split-row kernel: each row of the logits crosses HBM exactly once.
 //
 // A cluster of K CTAs (K = 1, 2, 4 or 8) owns a row at a time; CTA `rank`
-// holds the slice [rank*SE, (rank+1)*SE) of the row's classes in its shared
-// memory, staged by one TMA bulk copy.  Each CTA keeps a ring of `nslots`
-// staged slices so the copies of the next rows are in flight while it
-// computes the current one (a persistent grid: cluster c takes rows c,
-// c + nclusters, ...).  From the staged copy it computes, per row,
+// holds the slice [rank*SE, (rank+1)*SE) of the row's classes.  Each CTA keeps
+// a ring of `nslots` shared-memory slots filled by TMA bulk copies, so the
+// copies of the next rows are in flight while it computes the current one (a
+// persistent grid: cluster c takes rows c, c + nclusters, ...).
 //
-//   Step 1  m_r = max over the slice                       (block max)
-//   Step 2  S_r = sum 2^(z*log2e - M_r), M_r = m_r*log2e   (block sum)
-//   combine M = max_r M_r,  S = sum_r S_r * 2^(M_r - M)    (over DSMEM, K > 1)
-//   Step 4  grad = (2^(z*log2e - M) / S - [c == t]) / B     (16-byte stores)
-//   Step 3  l_b = ln2 * (log2 S - (z_t*log2e - M))          (rank 0)
+// A slice is read from shared memory once, into registers (VPT 16-byte
+// vectors per thread); its slot is handed back to the copy engine right after
+// the first block reduction.  From the registers each CTA computes
+//
+//   Step 1  m_r = max over the slice                         (block max)
+//   Step 2  e = 2^(z*log2e - M_r), M_r = m_r*log2e, kept in registers;
+//           S_r = sum of e over the slice, the target left out (block sum)
+//   combine M = max_r M_r,  S = sum_r S_r * 2^(M_r - M)      (over DSMEM, K > 1)
+//   Step 4  grad = e * 2^(M_r - M) / (S B), target: -S_rest / (S B)
+//   Step 3  l_b = log(S / e_t)                                (rank 0)
 //
 // which are Steps 1-4 of Pass 1 of rumus 0.1.1's cross_entropy.wgsl, with the
 // split-row combine being the running-max / rescaled-sum recurrence the rumus
@@ -25,7 +29,7 @@
 namespace ce {
 namespace {
 
-template <typename T, int K, int NT>
+template <typename T, int K, int NT, int VPT>
 __global__ void __launch_bounds__(NT, 1)
     row_split_kernel(Params p, int nslots, int slot_bytes, long long SE) {
     using E = Elem<T>;
@@ -38,9 +42,10 @@ __global__ void __launch_bounds__(NT, 1)
     __shared__ uint64_t full[kMaxSplitSlots];
     __shared__ float red_a[NW];
     __shared__ float red_b[NW];
+    __shared__ float zt_sh;
     __shared__ float4 part[2];
     __shared__ float4 comb;
-    __shared__ float2 tail_scratch[kTailThreads / 32];
+    __shared__ float2 tail_scratch[kTailWarps];
     __shared__ int tail_flag;
 
     const int tid = threadIdx.x;
@@ -120,12 +125,6 @@ __global__ void __launch_bounds__(NT, 1)
         // v*W - head + W - 1; local element l is valid for 0 <= l < slice_n.
         const int head = (int)((gs - g0) / ES);
         const int nv = (int)((((ge + 15) & ~15ull) - g0) >> 4);
-        const bool head_part = head != 0;
-        const bool tail_part = (ge & 15ull) != 0;
-        const int vb = head_part ? 1 : 0;
-        const int ve = nv - (tail_part ? 1 : 0);
-        const int rv0 = head_part ? 0 : -1;
-        const int rv1 = (tail_part && nv - 1 != rv0) ? nv - 1 : -1;
         bool has_t = t >= c0 && t < c1;
         const int tl = has_t ? (int)(t - c0) + head : kNoTarget;  // target, vector-0 based
 
@@ -148,78 +147,93 @@ __global__ void __launch_bounds__(NT, 1)
             }
             __syncthreads();
         }
-        const bool ragged = (tid == 0 && rv0 >= 0) || (tid == NT - 1 && rv1 >= 0);
-        const int rv = tid == 0 ? rv0 : rv1;
 
-        // ---- Step 1: slice max
+        // ---- the slice into registers; elements outside it read as -inf
+        uint4 x[VPT];
         float mx = -INFINITY;
         if (!failed) {
-#pragma unroll 4
-            for (int v = vb + tid; v < ve; v += NT) mx = fmaxf(mx, E::vmax(lds128(slot + 16 * v)));
-            if (ragged) {
-                float z[W];
-                E::unpack(lds128(slot + 16 * rv), z);
 #pragma unroll
-                for (int k = 0; k < W; ++k)
-                    if ((unsigned)(rv * W + k - head) < (unsigned)slice_n) mx = fmaxf(mx, z[k]);
+            for (int k = 0; k < VPT; ++k) {
+                const int v = tid + k * NT;
+                if (v < nv) {
+                    x[k] = lds128(slot + 16 * v);
+                    const int l0 = v * W - head;
+                    if (l0 < 0 || l0 + W > slice_n) {  // a partial vector (at most two per slice)
+                        float z[W];
+                        E::unpack(x[k], z);
+#pragma unroll
+                        for (int i = 0; i < W; ++i)
+                            if ((unsigned)(l0 + i) >= (unsigned)slice_n) z[i] = -INFINITY;
+                        x[k] = E::pack(z);
+                    }
+                    const int d = tl - v * W;
+                    if ((unsigned)d < (unsigned)W) zt_sh = E::load(slot + (size_t)tl * ES);
+                    // ---- Step 1: slice max
+                    mx = fmaxf(mx, E::vmax(x[k]));
+                }
             }
         }
         mx = warp_max(mx);
         if (lane == 0) red_a[warp] = mx;
-        __syncthreads();
-        float m = red_a[0];
-#pragma unroll
-        for (int w = 1; w < NW; ++w) m = fmaxf(m, red_a[w]);
-        float M = m * kLog2e;
+        __syncthreads();  // the slot is no longer read: hand it back to the copy engine
+        if (tid == 0 && !failed && issued < nrows) {
+            fence_proxy_async();
+            issue(issued);
+            ++issued;
+        }
+        float m = lane < NW ? red_a[lane] : -INFINITY;
+        m = warp_max(m);
+        // An empty slice (C < K*SE) has m = -inf: it publishes M = -inf, S = 0
+        // and takes a finite offset for its (absent) exponentials.
+        const float M_loc = m * kLog2e;
+        const float M_off = m == -INFINITY ? 0.f : M_loc;
+        float zt = has_t ? zt_sh : 0.f;
 
-        // ---- Step 2: slice sum of exponentials, the target's term left out
-        // (it is added back after the combine, so that 1 - p_t keeps its
-        // relative precision when the target dominates the row)
+        // ---- Step 2: exponentials kept in registers; their sum without the
+        // target's term (added back after the combine, so that 1 - p_t keeps
+        // its relative precision when the target dominates the row)
+        float e[VPT][W];
         float sa = 0.f, sb = 0.f;
-        if (!failed) {
-#pragma unroll 2
-            for (int v = vb + tid; v < ve; v += NT) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = tid + k * NT;
+            if (v < nv && !failed) {
                 float z[W];
-                E::unpack(lds128(slot + 16 * v), z);
+                E::unpack(x[k], z);
+#pragma unroll
+                for (int i = 0; i < W; ++i) e[k][i] = ex2(fmaf(z[i], kLog2e, -M_off));
                 const int d = tl - v * W;
                 if ((unsigned)d < (unsigned)W) {
 #pragma unroll
-                    for (int k = 0; k < W; ++k)
-                        if (k != d) sa += ex2(fmaf(z[k], kLog2e, -M));
+                    for (int i = 0; i < W; ++i)
+                        if (i != d) sa += e[k][i];
                 } else {
+                    float pair[W / 2];
 #pragma unroll
-                    for (int k = 0; k < W; k += 2) {
-                        sa += ex2(fmaf(z[k], kLog2e, -M));
-                        sb += ex2(fmaf(z[k + 1], kLog2e, -M));
+                    for (int i = 0; i < W / 2; ++i) pair[i] = e[k][2 * i] + e[k][2 * i + 1];
+                    if (W == 8) {
+                        sa += pair[0] + pair[1];
+                        sb += pair[2] + pair[3];
+                    } else {
+                        sa += pair[0];
+                        sb += pair[1];
                     }
-                }
-            }
-            if (ragged) {
-                float z[W];
-                E::unpack(lds128(slot + 16 * rv), z);
-#pragma unroll
-                for (int k = 0; k < W; ++k) {
-                    const int e = rv * W + k;
-                    if ((unsigned)(e - head) < (unsigned)slice_n && e != tl)
-                        sa += ex2(fmaf(z[k], kLog2e, -M));
                 }
             }
         }
         float ssum = warp_sum(sa + sb);
         if (lane == 0) red_b[warp] = ssum;
         __syncthreads();
-        float S = red_b[0];
-#pragma unroll
-        for (int w = 1; w < NW; ++w) S += red_b[w];
+        float S = lane < NW ? red_b[lane] : 0.f;
+        S = warp_sum(S);
 
-        float zt = 0.f;
-        if (has_t && !failed) zt = E::load(slot + (size_t)tl * ES);
-
+        float M = M_loc;
+        float rescale = 1.f;  // 2^(M_loc - M): this slice's exponentials to the row's offset
         if (K > 1) {
             // Combine the K slices' (M_r, S_r) in rank order; every CTA of the
             // cluster computes the same bits.  Only warp 0 publishes, so only
             // warp 0 arrives with release semantics.
-            if (tid == 0) part[j & 1] = make_float4(M, S, zt, has_t ? 1.f : 0.f);
+            if (tid == 0) part[j & 1] = make_float4(M_loc, S, zt, has_t ? 1.f : 0.f);
             if (warp == 0)
                 cluster_arrive_release();
             else
@@ -238,7 +252,7 @@ __global__ void __launch_bounds__(NT, 1)
                     const float Sr = __shfl_sync(0xffffffffu, q.y, r);
                     const float zr = __shfl_sync(0xffffffffu, q.z, r);
                     const float hr = __shfl_sync(0xffffffffu, q.w, r);
-                    Sg += Sr * ex2(Mr - Mg);
+                    if (Sr != 0.f) Sg += Sr * ex2(Mr - Mg);
                     if (hr != 0.f) {
                         ztg = zr;
                         hg = 1.f;
@@ -252,48 +266,40 @@ __global__ void __launch_bounds__(NT, 1)
             S = cb.y;
             zt = cb.z;
             has_t = cb.w != 0.f;
+            rescale = ex2(M_off - M);
         }
-        // S holds the sum without the target's term: S_rest = S * (1 - p_t).
+        // S holds the row's sum without the target's term: S_rest = S (1 - p_t).
         const float s_rest = S;
         const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
         S = s_rest + e_t;
 
         // ---- Step 4: gradient of the slice
         const float scale = (1.0f / S) * p.inv_b;
+        const float escale = scale * rescale;
         // (p_t - 1) / B = -S_rest / (S B): no cancellation when p_t is near 1
         const float g_t = -s_rest * scale;
-        if (!failed) {
-            unsigned char *gbase = p.grad + (g0 - lbase);  // grad byte of vector 0
-#pragma unroll 2
-            for (int v = vb + tid; v < ve; v += NT) {
-                float z[W];
-                E::unpack(lds128(slot + 16 * v), z);
+        unsigned char *gbase = p.grad + (g0 - lbase);  // grad byte of vector 0
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = tid + k * NT;
+            if (v < nv && !failed) {
                 float g[W];
 #pragma unroll
-                for (int k = 0; k < W; ++k) g[k] = ex2(fmaf(z[k], kLog2e, -M)) * scale;
+                for (int i = 0; i < W; ++i) g[i] = e[k][i] * escale;
                 const int d = tl - v * W;
                 if ((unsigned)d < (unsigned)W) {
 #pragma unroll
-                    for (int k = 0; k < W; ++k)
-                        if (k == d) g[k] = g_t;
+                    for (int i = 0; i < W; ++i)
+                        if (i == d) g[i] = g_t;
                 }
-                if (vec_store) {
+                const int l0 = v * W - head;
+                if (vec_store && l0 >= 0 && l0 + W <= slice_n) {
                     *reinterpret_cast<uint4 *>(gbase + 16 * v) = E::pack(g);
                 } else {
 #pragma unroll
-                    for (int k = 0; k < W; ++k) E::store(gbase + 16 * v + k * ES, g[k]);
-                }
-            }
-            if (ragged) {
-                float z[W];
-                E::unpack(lds128(slot + 16 * rv), z);
-#pragma unroll
-                for (int k = 0; k < W; ++k) {
-                    const int e = rv * W + k;
-                    if ((unsigned)(e - head) < (unsigned)slice_n) {
-                        const float gv = e == tl ? g_t : ex2(fmaf(z[k], kLog2e, -M)) * scale;
-                        E::store(gbase + 16 * rv + k * ES, gv);
-                    }
+                    for (int i = 0; i < W; ++i)
+                        if ((unsigned)(l0 + i) < (unsigned)slice_n)
+                            E::store(gbase + 16 * v + i * ES, g[i]);
                 }
             }
         }
@@ -312,13 +318,6 @@ __global__ void __launch_bounds__(NT, 1)
             }
             p.loss_rows[row] = l;
         }
-
-        __syncthreads();  // every thread is done with this slot
-        if (tid == 0 && !failed && issued < nrows) {
-            fence_proxy_async();
-            issue(issued);
-            ++issued;
-        }
     }
 
     // A CTA that gave up still owns copies in flight: wait for them (bounded)
@@ -332,10 +331,10 @@ __global__ void __launch_bounds__(NT, 1)
     finish_cta(p, &tail_flag, tail_scratch);
 }
 
-template <typename T, int K, int NT>
+template <typename T, int K, int NT, int VPT>
 cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long long se,
                      int smem, cudaStream_t s) {
-    auto kern = row_split_kernel<T, K, NT>;
+    auto kern = row_split_kernel<T, K, NT, VPT>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -355,9 +354,9 @@ cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long
     return cudaLaunchKernelEx(&cfg, kern, p, nslots, slot_bytes, se);
 }
 
-template <typename T, int K, int NT>
+template <typename T, int K, int NT, int VPT>
 cudaError_t max_clusters_k(int smem, int *clusters) {
-    auto kern = row_split_kernel<T, K, NT>;
+    auto kern = row_split_kernel<T, K, NT, VPT>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     if (K == 1) {
@@ -384,56 +383,44 @@ cudaError_t max_clusters_k(int smem, int *clusters) {
     return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
 }
 
-template <typename T, int NT>
-cudaError_t launch_n(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
+template <typename T>
+cudaError_t launch_t(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
                      int smem, cudaStream_t s) {
+    constexpr int NT = kSplitThreads;
+    constexpr int V = kSplitVecs;
     switch (K) {
-        case 1: return launch_k<T, 1, NT>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 2: return launch_k<T, 2, NT>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 4: return launch_k<T, 4, NT>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 8: return launch_k<T, 8, NT>(p, ctas, nslots, slot_bytes, se, smem, s);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-template <typename T, int NT>
-cudaError_t max_clusters_n(int K, int smem, int *clusters) {
-    switch (K) {
-        case 1: return max_clusters_k<T, 1, NT>(smem, clusters);
-        case 2: return max_clusters_k<T, 2, NT>(smem, clusters);
-        case 4: return max_clusters_k<T, 4, NT>(smem, clusters);
-        case 8: return max_clusters_k<T, 8, NT>(smem, clusters);
+        case 1: return launch_k<T, 1, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
+        case 2: return launch_k<T, 2, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
+        case 4: return launch_k<T, 4, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
+        case 8: return launch_k<T, 8, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 template <typename T>
-cudaError_t launch_t(const Params &p, int K, int threads, int ctas, int nslots, int slot_bytes,
-                     long long se, int smem, cudaStream_t s) {
-    if (threads == 1024) return launch_n<T, 1024>(p, K, ctas, nslots, slot_bytes, se, smem, s);
-    if (threads == 512) return launch_n<T, 512>(p, K, ctas, nslots, slot_bytes, se, smem, s);
-    return cudaErrorInvalidValue;
-}
-
-template <typename T>
-cudaError_t max_clusters_t(int K, int threads, int smem, int *clusters) {
-    if (threads == 1024) return max_clusters_n<T, 1024>(K, smem, clusters);
-    if (threads == 512) return max_clusters_n<T, 512>(K, smem, clusters);
-    return cudaErrorInvalidValue;
+cudaError_t max_clusters_t(int K, int smem, int *clusters) {
+    constexpr int NT = kSplitThreads;
+    constexpr int V = kSplitVecs;
+    switch (K) {
+        case 1: return max_clusters_k<T, 1, NT, V>(smem, clusters);
+        case 2: return max_clusters_k<T, 2, NT, V>(smem, clusters);
+        case 4: return max_clusters_k<T, 4, NT, V>(smem, clusters);
+        case 8: return max_clusters_k<T, 8, NT, V>(smem, clusters);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_split(const Params &p, int dtype, int K, int threads, int ctas, int nslots,
-                         int slot_bytes, long long slice_elems, int smem, cudaStream_t s) {
-    if (dtype == 0)
-        return launch_t<float>(p, K, threads, ctas, nslots, slot_bytes, slice_elems, smem, s);
-    return launch_t<__nv_bfloat16>(p, K, threads, ctas, nslots, slot_bytes, slice_elems, smem, s);
+cudaError_t launch_split(const Params &p, int dtype, int K, int ctas, int nslots, int slot_bytes,
+                         long long slice_elems, int smem, cudaStream_t s) {
+    if (dtype == 0) return launch_t<float>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);
+    return launch_t<__nv_bfloat16>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);
 }
 
-cudaError_t split_max_clusters(int dtype, int K, int threads, int smem, int *clusters) {
-    if (dtype == 0) return max_clusters_t<float>(K, threads, smem, clusters);
-    return max_clusters_t<__nv_bfloat16>(K, threads, smem, clusters);
+cudaError_t split_max_clusters(int dtype, int K, int smem, int *clusters) {
+    if (dtype == 0) return max_clusters_t<float>(K, smem, clusters);
+    return max_clusters_t<__nv_bfloat16>(K, smem, clusters);
 }
 
 }  // namespace ce

@@ -15,8 +15,8 @@
 namespace ce {
 namespace {
 
-template <typename T, int MAXV>
-__global__ void __launch_bounds__(kWarpKernelWarps * 32)
+template <typename T, int MAXV, int MINB>
+__global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     rows_warp_kernel(Params p, int slots, int rows_per_tile, int slot_bytes) {
     using E = Elem<T>;
     constexpr int NW = kWarpKernelWarps;
@@ -26,8 +26,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32)
 
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[NW * kMaxWarpSlots];
-    __shared__ float2 tail_scratch[kTailThreads / 32];
-    __shared__ int tail_flag;
+    __shared__ unsigned int warps_done;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -74,7 +73,8 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32)
         for (int s = 0; s < slots; ++s) mbar_init(&my_full[s], 1);
         fence_mbar_init();
     }
-    __syncwarp();
+    if (threadIdx.x == 0) warps_done = 0u;
+    __syncthreads();
     long long issued = 0;
     if (lane == 0) {
         for (; issued < ntl && issued < slots; ++issued) issue(issued);
@@ -252,13 +252,13 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32)
             if (!mbar_wait(&my_full[i % slots], (uint32_t)((i / slots) & 1))) break;
         }
     }
-    finish_cta(p, &tail_flag, tail_scratch);
+    finish_warp(p, &warps_done);
 }
 
-template <typename T, int MAXV>
+template <typename T, int MAXV, int MINB>
 cudaError_t launch_v(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
                      int smem, cudaStream_t s) {
-    auto kern = rows_warp_kernel<T, MAXV>;
+    auto kern = rows_warp_kernel<T, MAXV, MINB>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -269,9 +269,9 @@ cudaError_t launch_v(const Params &p, int ctas, int slots, int rows_per_tile, in
     return cudaLaunchKernelEx(&cfg, kern, p, slots, rows_per_tile, slot_bytes);
 }
 
-template <typename T, int MAXV>
+template <typename T, int MAXV, int MINB>
 cudaError_t occ_v(int smem, int *ctas) {
-    auto kern = rows_warp_kernel<T, MAXV>;
+    auto kern = rows_warp_kernel<T, MAXV, MINB>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, kWarpKernelWarps * 32, smem);
@@ -284,38 +284,52 @@ int maxv_for(long long C, int es) {
     return per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8 : 16;
 }
 
-template <typename T>
-cudaError_t launch_t(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
+template <typename T, int MINB>
+cudaError_t launch_m(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
                      int smem, cudaStream_t s) {
     switch (maxv_for(p.C, sizeof(T))) {
-        case 2: return launch_v<T, 2>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
-        case 4: return launch_v<T, 4>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
-        case 8: return launch_v<T, 8>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
-        default: return launch_v<T, 16>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+        case 2: return launch_v<T, 2, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+        case 4: return launch_v<T, 4, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+        case 8: return launch_v<T, 8, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+        default: return launch_v<T, 16, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+    }
+}
+
+template <typename T, int MINB>
+cudaError_t occ_m(long long C, int smem, int *ctas) {
+    switch (maxv_for(C, sizeof(T))) {
+        case 2: return occ_v<T, 2, MINB>(smem, ctas);
+        case 4: return occ_v<T, 4, MINB>(smem, ctas);
+        case 8: return occ_v<T, 8, MINB>(smem, ctas);
+        default: return occ_v<T, 16, MINB>(smem, ctas);
     }
 }
 
 template <typename T>
-cudaError_t occ_t(long long C, int smem, int *ctas) {
-    switch (maxv_for(C, sizeof(T))) {
-        case 2: return occ_v<T, 2>(smem, ctas);
-        case 4: return occ_v<T, 4>(smem, ctas);
-        case 8: return occ_v<T, 8>(smem, ctas);
-        default: return occ_v<T, 16>(smem, ctas);
-    }
+cudaError_t launch_t(const Params &p, int per_sm, int ctas, int slots, int rows_per_tile,
+                     int slot_bytes, int smem, cudaStream_t s) {
+    if (per_sm >= 2) return launch_m<T, 2>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+    return launch_m<T, 1>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+}
+
+template <typename T>
+cudaError_t occ_t(int per_sm, long long C, int smem, int *ctas) {
+    if (per_sm >= 2) return occ_m<T, 2>(C, smem, ctas);
+    return occ_m<T, 1>(C, smem, ctas);
 }
 
 }  // namespace
 
-cudaError_t launch_rows_warp(const Params &p, int dtype, int ctas, int slots, int rows_per_tile,
-                             int slot_bytes, int smem, cudaStream_t s) {
-    if (dtype == 0) return launch_t<float>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
-    return launch_t<__nv_bfloat16>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+cudaError_t launch_rows_warp(const Params &p, int dtype, int per_sm, int ctas, int slots,
+                             int rows_per_tile, int slot_bytes, int smem, cudaStream_t s) {
+    if (dtype == 0)
+        return launch_t<float>(p, per_sm, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+    return launch_t<__nv_bfloat16>(p, per_sm, ctas, slots, rows_per_tile, slot_bytes, smem, s);
 }
 
-cudaError_t rows_warp_max_ctas_per_sm(int dtype, long long C, int smem, int *ctas) {
-    if (dtype == 0) return occ_t<float>(C, smem, ctas);
-    return occ_t<__nv_bfloat16>(C, smem, ctas);
+cudaError_t rows_warp_max_ctas_per_sm(int dtype, int per_sm, long long C, int smem, int *ctas) {
+    if (dtype == 0) return occ_t<float>(per_sm, C, smem, ctas);
+    return occ_t<__nv_bfloat16>(per_sm, C, smem, ctas);
 }
 
 }  // namespace ce
