@@ -169,12 +169,24 @@ int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, 
     return CE_OK;
 }
 
+// Tuning knob: CE_SPLIT_THREADS=256 selects the split-row build with two
+// 256-thread CTAs per SM (slices of at most 32 KB); default 512, one CTA per SM.
+int split_threads() {
+    static const int n = [] {
+        const char *e = getenv("CE_SPLIT_THREADS");
+        return (e && atoi(e) == 256) ? 256 : ce::kSplitThreads;
+    }();
+    return n;
+}
+
 int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype, int K_forced,
                Plan *pl) {
-    const int budget = d.smem_optin - kStaticSmemReserve;
-    // A CTA holds a slice of at most kSplitThreads * kSplitVecs 16-byte vectors
-    // in registers; its slot is one such slice plus the alignment margin.
-    const long long max_slice_bytes = (long long)ce::kSplitThreads * ce::kSplitVecs * 16 - 16;
+    const int threads = split_threads();
+    const int per_sm = 512 / threads;
+    const int budget = d.smem_optin / per_sm - kStaticSmemReserve;
+    // A CTA holds a slice of at most threads * kSplitVecs 16-byte vectors in
+    // registers; its slot is one such slice plus the alignment margin.
+    const long long max_slice_bytes = (long long)threads * ce::kSplitVecs * 16 - 16;
     auto slice_of = [&](int K) {
         long long se = (C + K - 1) / K;
         return (se + 7) / 8 * 8;  // slices start 16-byte aligned relative to the row
@@ -199,16 +211,16 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     if (nslots > ce::kMaxSplitSlots) nslots = ce::kMaxSplitSlots;
     const int smem = nslots * (int)slot_bytes;
     int clusters = 0;
-    int rc = cached_occupancy(dtype, CE_PATH_ROW_SPLIT, K, smem,
-                              [&](int *v) { return ce::split_max_clusters(dtype, K, smem, v); },
-                              &clusters);
+    int rc = cached_occupancy(
+        dtype, CE_PATH_ROW_SPLIT, K * 1024 + threads, smem,
+        [&](int *v) { return ce::split_max_clusters(dtype, K, threads, smem, v); }, &clusters);
     if (rc != CE_OK) return rc;
     if (clusters < 1) return CE_ERR_PATH;
     if ((long long)clusters > B) clusters = (int)B;
     pl->path = CE_PATH_ROW_SPLIT;
     pl->split = K;
     pl->ctas = clusters * K;
-    pl->threads = ce::kSplitThreads;
+    pl->threads = threads;
     pl->smem = smem;
     pl->launches = 1;
     pl->nslots = nslots;
@@ -388,7 +400,8 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
                                      pl.slot_bytes, pl.smem, s);
             break;
         case CE_PATH_ROW_SPLIT:
-            e = ce::launch_split(p, dtype, pl.split, pl.ctas, pl.nslots, pl.slot_bytes, pl.slice,
+            e = ce::launch_split(p, dtype, pl.split, pl.threads, pl.ctas, pl.nslots, pl.slot_bytes,
+                                 pl.slice,
                                  pl.smem, s);
             break;
         default:

@@ -356,8 +356,9 @@ __device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *s
 // Warp-granular completion: called by every lane of a warp once the warp's
 // row losses are stored.  The last warp of each CTA (counted in shared memory
 // through `cta_count`, zeroed before any warp finishes) takes the CTA's global
-// ticket; the warp that takes the last ticket evaluates the batch loss alone.
-// No CTA-wide barrier: warps retire as soon as they are done.
+// ticket; the warp that takes the last ticket evaluates the batch loss alone,
+// in the same order as the CTA-wide tail (all eight virtual warps' loads are
+// issued together, then each virtual warp's tree runs).
 __device__ __forceinline__ void finish_warp(const Params &p, unsigned int *cta_count) {
     const int lane = threadIdx.x & 31;
     const unsigned int nwarps = blockDim.x >> 5;
@@ -373,13 +374,56 @@ __device__ __forceinline__ void finish_warp(const Params &p, unsigned int *cta_c
         }
     }
     last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-        __threadfence();
-        float2 totals[kTailWarps];
+    if (!last) return;
+    __threadfence();
+    const long long B = p.B;
+    float hi[kTailWarps], lo[kTailWarps];
 #pragma unroll
-        for (int vw = 0; vw < kTailWarps; ++vw) totals[vw] = tail_virtual_warp(p, vw, lane);
-        if (lane == 0) tail_write(p, totals);
+    for (int vw = 0; vw < kTailWarps; ++vw) hi[vw] = lo[vw] = 0.f;
+    for (long long m = 0; 4LL * lane + 4LL * kTailThreads * m < B; ++m) {
+        float x[kTailWarps][4];
+#pragma unroll
+        for (int vw = 0; vw < kTailWarps; ++vw) {
+            const long long base = 4LL * (vw * 32 + lane) + 4LL * kTailThreads * m;
+            if (base + 3 < B) {
+                const float4 q = __ldcg(reinterpret_cast<const float4 *>(p.loss_rows + base));
+                x[vw][0] = q.x; x[vw][1] = q.y; x[vw][2] = q.z; x[vw][3] = q.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    x[vw][k] = base + k < B ? __ldcg(p.loss_rows + base + k) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int vw = 0; vw < kTailWarps; ++vw) {
+            const long long base = 4LL * (vw * 32 + lane) + 4LL * kTailThreads * m;
+            if (base < B) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float s, e;
+                    two_sum(hi[vw], x[vw][k], s, e);
+                    hi[vw] = s;
+                    lo[vw] += e;
+                }
+            }
+        }
     }
+    float2 totals[kTailWarps];
+#pragma unroll
+    for (int vw = 0; vw < kTailWarps; ++vw) {
+        float h = hi[vw], l = lo[vw];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float h2 = __shfl_down_sync(0xffffffffu, h, o);
+            const float l2 = __shfl_down_sync(0xffffffffu, l, o);
+            float s, e;
+            two_sum(h, h2, s, e);
+            h = s;
+            l += l2 + e;
+        }
+        totals[vw] = make_float2(h, l);
+    }
+    if (lane == 0) tail_write(p, totals);
 }
 
 }  // namespace ce

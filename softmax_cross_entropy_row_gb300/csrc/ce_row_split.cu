@@ -30,7 +30,7 @@ namespace ce {
 namespace {
 
 template <typename T, int K, int NT, int VPT>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NT, 512 / NT)
     row_split_kernel(Params p, int nslots, int slot_bytes, long long SE) {
     using E = Elem<T>;
     constexpr int NW = NT / 32;
@@ -383,10 +383,9 @@ cudaError_t max_clusters_k(int smem, int *clusters) {
     return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
 }
 
-template <typename T>
-cudaError_t launch_t(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
+template <typename T, int NT>
+cudaError_t launch_n(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
                      int smem, cudaStream_t s) {
-    constexpr int NT = kSplitThreads;
     constexpr int V = kSplitVecs;
     switch (K) {
         case 1: return launch_k<T, 1, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
@@ -397,9 +396,8 @@ cudaError_t launch_t(const Params &p, int K, int ctas, int nslots, int slot_byte
     }
 }
 
-template <typename T>
-cudaError_t max_clusters_t(int K, int smem, int *clusters) {
-    constexpr int NT = kSplitThreads;
+template <typename T, int NT>
+cudaError_t max_clusters_n(int K, int smem, int *clusters) {
     constexpr int V = kSplitVecs;
     switch (K) {
         case 1: return max_clusters_k<T, 1, NT, V>(smem, clusters);
@@ -410,17 +408,33 @@ cudaError_t max_clusters_t(int K, int smem, int *clusters) {
     }
 }
 
-}  // namespace
-
-cudaError_t launch_split(const Params &p, int dtype, int K, int ctas, int nslots, int slot_bytes,
-                         long long slice_elems, int smem, cudaStream_t s) {
-    if (dtype == 0) return launch_t<float>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);
-    return launch_t<__nv_bfloat16>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);
+template <typename T>
+cudaError_t launch_t(const Params &p, int K, int threads, int ctas, int nslots, int slot_bytes,
+                     long long se, int smem, cudaStream_t s) {
+    if (threads == 256) return launch_n<T, 256>(p, K, ctas, nslots, slot_bytes, se, smem, s);
+    if (threads == 512) return launch_n<T, 512>(p, K, ctas, nslots, slot_bytes, se, smem, s);
+    return cudaErrorInvalidValue;
 }
 
-cudaError_t split_max_clusters(int dtype, int K, int smem, int *clusters) {
-    if (dtype == 0) return max_clusters_t<float>(K, smem, clusters);
-    return max_clusters_t<__nv_bfloat16>(K, smem, clusters);
+template <typename T>
+cudaError_t max_clusters_t(int K, int threads, int smem, int *clusters) {
+    if (threads == 256) return max_clusters_n<T, 256>(K, smem, clusters);
+    if (threads == 512) return max_clusters_n<T, 512>(K, smem, clusters);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_split(const Params &p, int dtype, int K, int threads, int ctas, int nslots,
+                         int slot_bytes, long long slice_elems, int smem, cudaStream_t s) {
+    if (dtype == 0)
+        return launch_t<float>(p, K, threads, ctas, nslots, slot_bytes, slice_elems, smem, s);
+    return launch_t<__nv_bfloat16>(p, K, threads, ctas, nslots, slot_bytes, slice_elems, smem, s);
+}
+
+cudaError_t split_max_clusters(int dtype, int K, int threads, int smem, int *clusters) {
+    if (dtype == 0) return max_clusters_t<float>(K, threads, smem, clusters);
+    return max_clusters_t<__nv_bfloat16>(K, threads, smem, clusters);
 }
 
 }  // namespace ce

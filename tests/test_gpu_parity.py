@@ -25,6 +25,7 @@ import oracle  # noqa: E402
 
 AUTO, WARP, SPLIT, STREAM = (ce.CE_PATH_AUTO, ce.CE_PATH_ROWS_WARP, ce.CE_PATH_ROW_SPLIT,
                              ce.CE_PATH_STREAM)
+SPLIT_MAX_SLICE_BYTES = 512 * 8 * 16 - 16  # threads x vectors x 16 bytes, less the alignment margin
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -76,6 +77,13 @@ def test_warp_path_shapes(B, C, dtype):
 def test_split_path_shapes(B, C, dtype, K):
     inp = _case(B, C, dtype, seed=B * 104729 + C + K, sigma=3.0)
     z, t = device_inputs(inp)
+    slice_bytes = -(-(-(-C // K)) // 8) * 8 * inp.workload.elem_bytes
+    if slice_bytes > SPLIT_MAX_SLICE_BYTES:
+        # a CTA holds at most 64 KB of a row in registers: the forced split is refused
+        with pytest.raises(ce.CEError) as ei:
+            run(z, t, SPLIT, K)
+        assert ei.value.status == 9
+        return
     loss, grad = run(z, t, SPLIT, K)
     torch.cuda.synchronize()
     check_full(inp, loss, grad, f"split K={K} {B}x{C} {dtype}")
@@ -93,7 +101,7 @@ def test_stream_path_shapes(B, C, dtype):
 
 def test_many_rows_per_cluster():
     """More rows than clusters: the shared-memory rings wrap several times."""
-    for dtype, C, K in [("f32", 3000, 1), ("bf16", 9000, 2), ("f32", 20000, 4)]:
+    for dtype, C, K in [("f32", 3000, 1), ("bf16", 9000, 2), ("f32", 20000, 2)]:
         inp = _case(1500, C, dtype, seed=C + K, sigma=2.0)
         z, t = device_inputs(inp)
         loss, grad = run(z, t, SPLIT, K)
@@ -176,7 +184,7 @@ def test_structured_rows_small():
     stress = wl.Workload("stress_small", 400, 5003, "f32", seed=4, sigma=30.0,
                          uniform_frac=0.01, spike=80.0)
     peaked = wl.Workload("peaked_small", 256, 12829, "bf16", seed=3, sigma=3.0, peak=8.0)
-    for w, paths in [(stress, [(AUTO, 0), (SPLIT, 2), (SPLIT, 4), (STREAM, 0)]),
+    for w, paths in [(stress, [(AUTO, 0), (SPLIT, 1), (SPLIT, 2), (SPLIT, 4), (STREAM, 0)]),
                      (peaked, [(AUTO, 0), (SPLIT, 1), (SPLIT, 8), (STREAM, 0)])]:
         inp = wl.make_inputs(w)
         z, t = device_inputs(inp)
