@@ -19,6 +19,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 // second at 2 GHz), records a timeout in the device error word and the kernel
 // skips the rest of its work instead of hanging the GPU.
 constexpr long long kWaitLimitCycles = 2000000000LL;
+// Upper bound on one suspended try_wait (ns); the thread wakes as soon as the
+// phase completes, so this only limits how often a waiting warp re-polls.
+constexpr uint32_t kSuspendHintNs = 20000u;
 
 // Device error word layout (two int32 counters in the workspace).
 constexpr int kErrBadTarget = 0;
@@ -52,6 +55,7 @@ template <>
 struct Elem<float> {
     static constexpr int kBytes = 4;
     static constexpr int kVec = 4;  // elements per 16-byte vector
+    static constexpr uint32_t kNegInfWord = 0xff800000u;  // -inf in every element of a word
     __device__ __forceinline__ static float load(const unsigned char *p) {
         return *reinterpret_cast<const float *>(p);
     }
@@ -82,6 +86,7 @@ template <>
 struct Elem<__nv_bfloat16> {
     static constexpr int kBytes = 2;
     static constexpr int kVec = 8;
+    static constexpr uint32_t kNegInfWord = 0xff80ff80u;
     __device__ __forceinline__ static float widen(uint16_t b) {
         return __uint_as_float(static_cast<uint32_t>(b) << 16);
     }
@@ -178,10 +183,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return done != 0;
 }

@@ -109,9 +109,53 @@ __global__ void __launch_bounds__(NT, 512 / NT)
         const long long t = t_next;
         if (j + 1 < nrows) t_next = __ldg(p.targets + row + ncl);
 
+        uint64_t gs, ge, g0, lo, hi;
+        span(row, gs, ge, g0, lo, hi);
+        // Vector v of the slot holds the slice's local elements v*W - head ..
+        // v*W - head + W - 1; local element l is valid for 0 <= l < slice_n.
+        const int head = (int)((gs - g0) / ES);
+        const int nv = (int)((((ge + 15) & ~15ull) - g0) >> 4);
+        const int vf0 = head != 0 ? 1 : 0;                     // whole vectors: [vf0, vf1)
+        const int vf1 = (ge & 15ull) != 0 ? nv - 1 : nv;
+        bool has_t = t >= c0 && t < c1;
+        const int tl = has_t ? (int)(t - c0) + head : kNoTarget;  // target, vector-0 based
+        const int v_t = has_t ? tl / W : -1;                       // the target's vector
+
         if (!failed) {
             if (mbar_wait(&full[s], parity)) {
                 consumed = j + 1;
+                // Elements the copy could not cover (only at the very beginning
+                // or end of an unaligned tensor) come from plain loads; the
+                // bytes of the first and last vectors outside the slice become
+                // -inf, so every vector can be reduced without masks.
+                if (g0 < p.lo_clip || ((ge + 15) & ~15ull) > p.hi_clip) {
+                    if (tid < 16) {
+                        const int l = tid < 8 ? tid : slice_n - 16 + tid;
+                        if (l >= 0 && l < slice_n) {
+                            const uint64_t a = gs + (uint64_t)l * ES;
+                            if (a < lo || a + ES > hi) {
+                                if (ES == 4)
+                                    *reinterpret_cast<uint32_t *>(slot + (a - g0)) =
+                                        __ldg(reinterpret_cast<const unsigned int *>(a));
+                                else
+                                    *reinterpret_cast<uint16_t *>(slot + (a - g0)) =
+                                        __ldg(reinterpret_cast<const unsigned short *>(a));
+                            }
+                        }
+                    }
+                }
+                if (tid == 32) {
+                    for (int i = 0; i < head; ++i)
+                        if (ES == 4)
+                            reinterpret_cast<uint32_t *>(slot)[i] = E::kNegInfWord;
+                        else
+                            reinterpret_cast<uint16_t *>(slot)[i] = (uint16_t)E::kNegInfWord;
+                    for (int i = head + slice_n; i < nv * W; ++i)
+                        if (ES == 4)
+                            reinterpret_cast<uint32_t *>(slot)[i] = E::kNegInfWord;
+                        else
+                            reinterpret_cast<uint16_t *>(slot)[i] = (uint16_t)E::kNegInfWord;
+                }
             } else {
                 failed = true;
                 atomicAdd(&p.err[kErrTimeout], 1);
@@ -119,60 +163,25 @@ __global__ void __launch_bounds__(NT, 512 / NT)
         }
         failed = __syncthreads_or(failed);
 
-        uint64_t gs, ge, g0, lo, hi;
-        span(row, gs, ge, g0, lo, hi);
-        // Vector v of the slot holds the slice's local elements v*W - head ..
-        // v*W - head + W - 1; local element l is valid for 0 <= l < slice_n.
-        const int head = (int)((gs - g0) / ES);
-        const int nv = (int)((((ge + 15) & ~15ull) - g0) >> 4);
-        bool has_t = t >= c0 && t < c1;
-        const int tl = has_t ? (int)(t - c0) + head : kNoTarget;  // target, vector-0 based
-
-        // Elements whose bytes the copy could not cover (only at the very
-        // beginning or end of an unaligned tensor): plain loads.
-        if (!failed && (g0 < p.lo_clip || ((ge + 15) & ~15ull) > p.hi_clip)) {
-            if (tid < 16) {
-                const int l = tid < 8 ? tid : slice_n - 16 + tid;
-                if (l >= 0 && l < slice_n) {
-                    const uint64_t a = gs + (uint64_t)l * ES;
-                    if (a < lo || a + ES > hi) {
-                        if (ES == 4)
-                            *reinterpret_cast<uint32_t *>(slot + (a - g0)) =
-                                __ldg(reinterpret_cast<const unsigned int *>(a));
-                        else
-                            *reinterpret_cast<uint16_t *>(slot + (a - g0)) =
-                                __ldg(reinterpret_cast<const unsigned short *>(a));
-                    }
-                }
-            }
-            __syncthreads();
-        }
-
-        // ---- the slice into registers; elements outside it read as -inf
+        // ---- the slice into registers (vectors past the slice read as -inf)
+        const uint4 kNeg = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord,
+                                      E::kNegInfWord);
         uint4 x[VPT];
+        uint4 xt = kNeg;  // thread 0: the target's vector
         float mx = -INFINITY;
-        if (!failed) {
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = tid + k * NT;
-                if (v < nv) {
-                    x[k] = lds128(slot + 16 * v);
-                    const int l0 = v * W - head;
-                    if (l0 < 0 || l0 + W > slice_n) {  // a partial vector (at most two per slice)
-                        float z[W];
-                        E::unpack(x[k], z);
-#pragma unroll
-                        for (int i = 0; i < W; ++i)
-                            if ((unsigned)(l0 + i) >= (unsigned)slice_n) z[i] = -INFINITY;
-                        x[k] = E::pack(z);
-                    }
-                    const int d = tl - v * W;
-                    if ((unsigned)d < (unsigned)W) zt_sh = E::load(slot + (size_t)tl * ES);
-                    // ---- Step 1: slice max
-                    mx = fmaxf(mx, E::vmax(x[k]));
-                }
-            }
+        for (int k = 0; k < VPT; ++k) {
+            const int v = tid + k * NT;
+            x[k] = kNeg;
+            if (v < nv && !failed) x[k] = lds128(slot + 16 * v);
         }
+        if (tid == 0 && has_t && !failed) {
+            xt = lds128(slot + 16 * v_t);
+            zt_sh = E::load(slot + (size_t)tl * ES);
+        }
+        // ---- Step 1: slice max
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) mx = fmaxf(mx, E::vmax(x[k]));
         mx = warp_max(mx);
         if (lane == 0) red_a[warp] = mx;
         __syncthreads();  // the slot is no longer read: hand it back to the copy engine
@@ -191,35 +200,31 @@ __global__ void __launch_bounds__(NT, 512 / NT)
 
         // ---- Step 2: exponentials kept in registers; their sum without the
         // target's term (added back after the combine, so that 1 - p_t keeps
-        // its relative precision when the target dominates the row)
+        // its relative precision when the target dominates the row).  The
+        // target's vector is left out whole; thread 0 adds its other elements.
         float e[VPT][W];
         float sa = 0.f, sb = 0.f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = tid + k * NT;
-            if (v < nv && !failed) {
-                float z[W];
-                E::unpack(x[k], z);
+            float z[W];
+            E::unpack(x[k], z);
 #pragma unroll
-                for (int i = 0; i < W; ++i) e[k][i] = ex2(fmaf(z[i], kLog2e, -M_off));
-                const int d = tl - v * W;
-                if ((unsigned)d < (unsigned)W) {
+            for (int i = 0; i < W; ++i) e[k][i] = ex2(fmaf(z[i], kLog2e, -M_off));
+            float lo4 = (e[k][0] + e[k][1]) + (e[k][2] + e[k][3]);
+            float hi4 = 0.f;
+            if (W == 8) hi4 = (e[k][4] + e[k][5]) + (e[k][6] + e[k][7]);
+            const bool keep = v != v_t;
+            sa += keep ? lo4 : 0.f;
+            sb += keep ? hi4 : 0.f;
+        }
+        if (tid == 0 && has_t) {
+            float z[W];
+            E::unpack(xt, z);
+            const int d = tl - v_t * W;
 #pragma unroll
-                    for (int i = 0; i < W; ++i)
-                        if (i != d) sa += e[k][i];
-                } else {
-                    float pair[W / 2];
-#pragma unroll
-                    for (int i = 0; i < W / 2; ++i) pair[i] = e[k][2 * i] + e[k][2 * i + 1];
-                    if (W == 8) {
-                        sa += pair[0] + pair[1];
-                        sb += pair[2] + pair[3];
-                    } else {
-                        sa += pair[0];
-                        sb += pair[1];
-                    }
-                }
-            }
+            for (int i = 0; i < W; ++i)
+                if (i != d) sa += ex2(fmaf(z[i], kLog2e, -M_off));
         }
         float ssum = warp_sum(sa + sb);
         if (lane == 0) red_b[warp] = ssum;
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(NT, 512 / NT)
         S = warp_sum(S);
 
         float M = M_loc;
-        float rescale = 1.f;  // 2^(M_loc - M): this slice's exponentials to the row's offset
+        float rescale = 1.f;  // 2^(M_off - M): this slice's exponentials to the row's offset
         if (K > 1) {
             // Combine the K slices' (M_r, S_r) in rank order; every CTA of the
             // cluster computes the same bits.  Only warp 0 publishes, so only
@@ -279,27 +284,40 @@ __global__ void __launch_bounds__(NT, 512 / NT)
         // (p_t - 1) / B = -S_rest / (S B): no cancellation when p_t is near 1
         const float g_t = -s_rest * scale;
         unsigned char *gbase = p.grad + (g0 - lbase);  // grad byte of vector 0
+        const int tl_own = v_t >= vf0 && v_t < vf1 ? tl : kNoTarget;  // target in a whole vector
+        if (!failed) {
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = tid + k * NT;
-            if (v < nv && !failed) {
-                float g[W];
+            for (int k = 0; k < VPT; ++k) {
+                const int v = tid + k * NT;
+                if (v >= vf0 && v < vf1) {
+                    float g[W];
 #pragma unroll
-                for (int i = 0; i < W; ++i) g[i] = e[k][i] * escale;
-                const int d = tl - v * W;
-                if ((unsigned)d < (unsigned)W) {
+                    for (int i = 0; i < W; ++i) g[i] = e[k][i] * escale;
+                    if (vec_store) {
+                        *reinterpret_cast<uint4 *>(gbase + 16 * v) = E::pack(g);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < W; ++i)
-                        if (i == d) g[i] = g_t;
+                        for (int i = 0; i < W; ++i) E::store(gbase + 16 * v + i * ES, g[i]);
+                    }
+                    // the owner of the target's vector overwrites the target
+                    if (v == v_t && tl_own != kNoTarget) E::store(gbase + (size_t)tl * ES, g_t);
                 }
-                const int l0 = v * W - head;
-                if (vec_store && l0 >= 0 && l0 + W <= slice_n) {
-                    *reinterpret_cast<uint4 *>(gbase + 16 * v) = E::pack(g);
-                } else {
+            }
+            // The (at most two) partial vectors: element by element, by their owners.
+            const bool head_partial = vf0 == 1;
+            const bool tail_partial = vf1 == nv - 1 && nv - 1 >= vf0;
 #pragma unroll
-                    for (int i = 0; i < W; ++i)
-                        if ((unsigned)(l0 + i) < (unsigned)slice_n)
-                            E::store(gbase + 16 * v + i * ES, g[i]);
+            for (int k = 0; k < VPT; ++k) {
+                const int v = tid + k * NT;
+                if ((v == 0 && head_partial) || (v == nv - 1 && tail_partial)) {
+                    const int l0 = v * W - head;
+#pragma unroll
+                    for (int i = 0; i < W; ++i) {
+                        if ((unsigned)(l0 + i) < (unsigned)slice_n) {
+                            const float gv = v * W + i == tl ? g_t : e[k][i] * escale;
+                            E::store(gbase + 16 * v + i * ES, gv);
+                        }
+                    }
                 }
             }
         }

@@ -3,10 +3,11 @@
 // Each warp owns a private ring of `slots` shared-memory tiles; a tile is
 // `rows_per_tile` consecutive rows of the logits, staged by one TMA bulk copy.
 // Warps act as their own producers, so no CTA-wide barrier is needed until
-// the fused batch-loss tail.  A row is read from shared memory once, into
-// registers (16-byte vectors, at most MAXV per lane), and every step runs
-// from there: Steps 1-4 of Pass 1 of rumus 0.1.1's cross_entropy.wgsl (max,
-// sum of exponentials, row loss, gradient) with warp-shuffle reductions; the
+// the fused batch-loss tail.  A warp makes three passes of 16-byte vectors
+// over its staged row -- Steps 1-4 of Pass 1 of rumus 0.1.1's
+// cross_entropy.wgsl (max, sum of exponentials, row loss, gradient) -- with
+// warp-shuffle reductions; fp32 rows keep their exponentials in place in
+// shared memory, so every element is exponentiated once.  The
 // last CTA to finish performs Pass 2 (the fixed-order batch-loss sum).
 #include <math.h>
 
@@ -15,7 +16,7 @@
 namespace ce {
 namespace {
 
-template <typename T, int MAXV, int MINB>
+template <typename T, int MINB>
 __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     rows_warp_kernel(Params p, int slots, int rows_per_tile, int slot_bytes) {
     using E = Elem<T>;
@@ -139,50 +140,52 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
             const int nt = C - nh - nvec * W;
             const unsigned char *vrow = row + nh * ES;
             const int tv = has_t ? t - nh : -0x40000000;  // target relative to vector 0
-
-            uint4 x[MAXV];
-#pragma unroll
-            for (int k = 0; k < MAXV; ++k) {
-                const int v = lane + 32 * k;
-                if (v < nvec) x[k] = lds128(vrow + 16 * v);
-            }
+            const int v_t = has_t && tv >= 0 && tv < nvec * W ? tv / W : -1;  // its vector
+            const float zt = has_t ? E::load(row + t * ES) : 0.f;
             const float hz = lane < nh ? E::load(row + lane * ES) : -INFINITY;
             const float tz = lane < nt ? E::load(vrow + (nvec * W + lane) * ES) : -INFINITY;
 
             // Step 1: max
             float m = fmaxf(hz, tz);
-#pragma unroll
-            for (int k = 0; k < MAXV; ++k)
-                if (lane + 32 * k < nvec) m = fmaxf(m, E::vmax(x[k]));
+#pragma unroll 4
+            for (int v = lane; v < nvec; v += 32) m = fmaxf(m, E::vmax(lds128(vrow + 16 * v)));
             m = warp_max(m);
             const float M = m * kLog2e;
 
-            // Step 2: sum of exponentials without the target's term
+            // Step 2: sum of exponentials without the target's term.  The
+            // target's vector is left out whole; lane 0 adds its other elements.
+            // fp32 rows get their exponentials written back in place.
             float sa = 0.f, sb = 0.f;
+#pragma unroll 4
+            for (int v = lane; v < nvec; v += 32) {
+                float z[W];
+                E::unpack(lds128(vrow + 16 * v), z);
 #pragma unroll
-            for (int k = 0; k < MAXV; ++k) {
-                const int v = lane + 32 * k;
-                if (v < nvec) {
-                    float z[W];
-                    E::unpack(x[k], z);
-                    const int d = tv - v * W;
+                for (int j = 0; j < W; ++j) z[j] = ex2(fmaf(z[j], kLog2e, -M));
+                if (kKeepExp)
+                    *reinterpret_cast<uint4 *>(const_cast<unsigned char *>(vrow) + 16 * v) =
+                        E::pack(z);
+                float a4 = (z[0] + z[1]) + (z[2] + z[3]);
+                float b4 = 0.f;
+                if (W == 8) b4 = (z[4] + z[5]) + (z[6] + z[7]);
+                const bool keep = v != v_t;
+                sa += keep ? a4 : 0.f;
+                sb += keep ? b4 : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0 && v_t >= 0) {
+                float z[W];
+                E::unpack(lds128(vrow + 16 * v_t), z);
+                const int d = tv - v_t * W;
 #pragma unroll
-                    for (int j = 0; j < W; ++j) {
-                        const float e = ex2(fmaf(z[j], kLog2e, -M));
-                        if (kKeepExp) z[j] = e;
-                        if (j != d) {
-                            if (j & 1) sb += e; else sa += e;
-                        }
-                    }
-                    if (kKeepExp) x[k] = E::pack(z);
-                }
+                for (int j = 0; j < W; ++j)
+                    if (j != d) sa += kKeepExp ? z[j] : ex2(fmaf(z[j], kLog2e, -M));
             }
             const float eh = lane < nh ? ex2(fmaf(hz, kLog2e, -M)) : 0.f;
             const float et = lane < nt ? ex2(fmaf(tz, kLog2e, -M)) : 0.f;
             if (lane != t) sa += eh;
             if (nh + nvec * W + lane != t) sb += et;
             const float s_rest = warp_sum(sa + sb);
-            const float zt = has_t ? E::load(row + t * ES) : 0.f;
             const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
             const float S = s_rest + e_t;
 
@@ -191,34 +194,21 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
             const float g_t = -s_rest * scale;
             unsigned char *grow = p.grad + (size_t)r * C * ES;
             unsigned char *gvec = grow + nh * ES;
+#pragma unroll 4
+            for (int v = lane; v < nvec; v += 32) {
+                float g[W];
+                E::unpack(lds128(vrow + 16 * v), g);
 #pragma unroll
-            for (int k = 0; k < MAXV; ++k) {
-                const int v = lane + 32 * k;
-                if (v < nvec) {
-                    float g[W];
-                    if (kKeepExp) {
-                        E::unpack(x[k], g);
+                for (int j = 0; j < W; ++j)
+                    g[j] = (kKeepExp ? g[j] : ex2(fmaf(g[j], kLog2e, -M))) * scale;
+                if (vec_store) {
+                    *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack(g);
+                } else {
 #pragma unroll
-                        for (int j = 0; j < W; ++j) g[j] *= scale;
-                    } else {
-                        float z[W];
-                        E::unpack(x[k], z);
-#pragma unroll
-                        for (int j = 0; j < W; ++j) g[j] = ex2(fmaf(z[j], kLog2e, -M)) * scale;
-                    }
-                    const int d = tv - v * W;
-                    if ((unsigned)d < (unsigned)W) {
-#pragma unroll
-                        for (int j = 0; j < W; ++j)
-                            if (j == d) g[j] = g_t;
-                    }
-                    if (vec_store) {
-                        *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack(g);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < W; ++j) E::store(gvec + (v * W + j) * ES, g[j]);
-                    }
+                    for (int j = 0; j < W; ++j) E::store(gvec + (v * W + j) * ES, g[j]);
                 }
+                // the owner of the target's vector overwrites the target
+                if (v == v_t) E::store(grow + (size_t)t * ES, g_t);
             }
             if (lane < nh) E::store(grow + lane * ES, lane == t ? g_t : eh * scale);
             if (lane < nt) {
@@ -255,10 +245,10 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     finish_warp(p, &warps_done);
 }
 
-template <typename T, int MAXV, int MINB>
-cudaError_t launch_v(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
+template <typename T, int MINB>
+cudaError_t launch_m(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
                      int smem, cudaStream_t s) {
-    auto kern = rows_warp_kernel<T, MAXV, MINB>;
+    auto kern = rows_warp_kernel<T, MINB>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -269,40 +259,12 @@ cudaError_t launch_v(const Params &p, int ctas, int slots, int rows_per_tile, in
     return cudaLaunchKernelEx(&cfg, kern, p, slots, rows_per_tile, slot_bytes);
 }
 
-template <typename T, int MAXV, int MINB>
-cudaError_t occ_v(int smem, int *ctas) {
-    auto kern = rows_warp_kernel<T, MAXV, MINB>;
+template <typename T, int MINB>
+cudaError_t occ_m(int smem, int *ctas) {
+    auto kern = rows_warp_kernel<T, MINB>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, kWarpKernelWarps * 32, smem);
-}
-
-// Vectors per lane: a row of C elements has at most C*ES/16 whole vectors.
-int maxv_for(long long C, int es) {
-    const long long nvec = C * es / 16;
-    const long long per_lane = (nvec + 31) / 32;
-    return per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8 : 16;
-}
-
-template <typename T, int MINB>
-cudaError_t launch_m(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
-                     int smem, cudaStream_t s) {
-    switch (maxv_for(p.C, sizeof(T))) {
-        case 2: return launch_v<T, 2, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
-        case 4: return launch_v<T, 4, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
-        case 8: return launch_v<T, 8, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
-        default: return launch_v<T, 16, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
-    }
-}
-
-template <typename T, int MINB>
-cudaError_t occ_m(long long C, int smem, int *ctas) {
-    switch (maxv_for(C, sizeof(T))) {
-        case 2: return occ_v<T, 2, MINB>(smem, ctas);
-        case 4: return occ_v<T, 4, MINB>(smem, ctas);
-        case 8: return occ_v<T, 8, MINB>(smem, ctas);
-        default: return occ_v<T, 16, MINB>(smem, ctas);
-    }
 }
 
 template <typename T>
@@ -314,8 +276,9 @@ cudaError_t launch_t(const Params &p, int per_sm, int ctas, int slots, int rows_
 
 template <typename T>
 cudaError_t occ_t(int per_sm, long long C, int smem, int *ctas) {
-    if (per_sm >= 2) return occ_m<T, 2>(C, smem, ctas);
-    return occ_m<T, 1>(C, smem, ctas);
+    (void)C;
+    if (per_sm >= 2) return occ_m<T, 2>(smem, ctas);
+    return occ_m<T, 1>(smem, ctas);
 }
 
 }  // namespace
