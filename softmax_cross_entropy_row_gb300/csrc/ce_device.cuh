@@ -46,6 +46,33 @@ struct Params {
     int grad_vec_ok;              // grad and logits share their address mod 16
 };
 
+// Packed fp32 pairs (Blackwell f32x2 arithmetic: each half is rounded exactly
+// as the scalar instruction would round it).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // ------------------------------------------------------------ element types
 
 template <typename T>
@@ -71,6 +98,15 @@ struct Elem<float> {
     __device__ __forceinline__ static uint4 pack(const float (&v)[4]) {
         return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
                           __float_as_uint(v[2]), __float_as_uint(v[3]));
+    }
+    // The vector as fp32 pairs (elements 2i, 2i+1 in pair i).
+    __device__ __forceinline__ static void unpack2(const uint4 &w, unsigned long long (&v)[2]) {
+        v[0] = (unsigned long long)w.x | ((unsigned long long)w.y << 32);
+        v[1] = (unsigned long long)w.z | ((unsigned long long)w.w << 32);
+    }
+    __device__ __forceinline__ static uint4 pack2(const unsigned long long (&v)[2]) {
+        return make_uint4((uint32_t)v[0], (uint32_t)(v[0] >> 32), (uint32_t)v[1],
+                          (uint32_t)(v[1] >> 32));
     }
     __device__ __forceinline__ static void store(unsigned char *p, float v) {
         *reinterpret_cast<float *>(p) = v;
@@ -113,6 +149,21 @@ struct Elem<__nv_bfloat16> {
     __device__ __forceinline__ static uint4 pack(const float (&v)[8]) {
         return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]),
                           pack2(v[6], v[7]));
+    }
+    // The vector as fp32 pairs (elements 2i, 2i+1 in pair i).
+    __device__ __forceinline__ static void unpack2(const uint4 &w, unsigned long long (&v)[4]) {
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v[i] = (unsigned long long)(q[i] << 16) | ((unsigned long long)(q[i] & 0xffff0000u) << 32);
+    }
+    __device__ __forceinline__ static uint32_t pack_pair(unsigned long long v) {
+        float lo, hi;
+        f2_unpack(v, lo, hi);
+        return pack2(lo, hi);
+    }
+    __device__ __forceinline__ static uint4 pack2(const unsigned long long (&v)[4]) {
+        return make_uint4(pack_pair(v[0]), pack_pair(v[1]), pack_pair(v[2]), pack_pair(v[3]));
     }
     __device__ __forceinline__ static void store(unsigned char *p, float v) {
         *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
@@ -264,6 +315,16 @@ __device__ __forceinline__ float4 ld_dsmem_f4(const void *local, uint32_t rank) 
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "r"(remote)
                  : "memory");
+    return v;
+}
+
+// Read a float from the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ float ld_dsmem_f32(const void *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)),
+                 "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
     return v;
 }
 

@@ -35,16 +35,17 @@ __global__ void __launch_bounds__(NT, 512 / NT)
     using E = Elem<T>;
     constexpr int NW = NT / 32;
     constexpr int W = E::kVec;
+    constexpr int W2 = W / 2;  // fp32 pairs per vector
     constexpr int ES = E::kBytes;
     constexpr int kNoTarget = -0x40000000;
+    constexpr int kPartRegs = (NW * K + 31) / 32;  // cluster partial sums held per lane
 
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[kMaxSplitSlots];
-    __shared__ float red_a[NW];
-    __shared__ float red_b[NW];
-    __shared__ float zt_sh;
-    __shared__ float4 part[2];
-    __shared__ float4 comb;
+    __shared__ float red_max[2][NW];   // per warp, by row parity
+    __shared__ float red_sum[2][NW];
+    __shared__ float zt_sh[2];
+    __shared__ float4 part[2];         // this CTA's (M, -, z_t, has_t) for the cluster
     __shared__ float2 tail_scratch[kTailWarps];
     __shared__ int tail_flag;
 
@@ -61,6 +62,7 @@ __global__ void __launch_bounds__(NT, 512 / NT)
     const long long nrows = cid < p.B ? (p.B - cid + ncl - 1) / ncl : 0;
     const uint64_t lbase = reinterpret_cast<uint64_t>(p.logits);
     const bool vec_store = p.grad_vec_ok != 0;
+    const unsigned long long kL2E2 = f2_pack(kLog2e, kLog2e);
 
     // Byte range [gs, ge) of this CTA's slice of row `row`, and the aligned
     // span that the TMA copy can cover inside the tensor.
@@ -104,6 +106,7 @@ __global__ void __launch_bounds__(NT, 512 / NT)
     for (long long j = 0; j < nrows; ++j) {
         const long long row = cid + j * ncl;
         const int s = (int)(j % nslots);
+        const int par = (int)(j & 1);
         const uint32_t parity = (uint32_t)((j / nslots) & 1);
         unsigned char *slot = smem + (size_t)s * slot_bytes;
         const long long t = t_next;
@@ -117,6 +120,8 @@ __global__ void __launch_bounds__(NT, 512 / NT)
         const int nv = (int)((((ge + 15) & ~15ull) - g0) >> 4);
         const int vf0 = head != 0 ? 1 : 0;                     // whole vectors: [vf0, vf1)
         const int vf1 = (ge & 15ull) != 0 ? nv - 1 : nv;
+        const bool head_partial = vf0 == 1;
+        const bool tail_partial = vf1 == nv - 1 && nv - 1 >= vf0;
         bool has_t = t >= c0 && t < c1;
         const int tl = has_t ? (int)(t - c0) + head : kNoTarget;  // target, vector-0 based
         const int v_t = has_t ? tl / W : -1;                       // the target's vector
@@ -124,100 +129,117 @@ __global__ void __launch_bounds__(NT, 512 / NT)
         if (!failed) {
             if (mbar_wait(&full[s], parity)) {
                 consumed = j + 1;
-                // Elements the copy could not cover (only at the very beginning
-                // or end of an unaligned tensor) come from plain loads; the
-                // bytes of the first and last vectors outside the slice become
-                // -inf, so every vector can be reduced without masks.
-                if (g0 < p.lo_clip || ((ge + 15) & ~15ull) > p.hi_clip) {
-                    if (tid < 16) {
-                        const int l = tid < 8 ? tid : slice_n - 16 + tid;
-                        if (l >= 0 && l < slice_n) {
-                            const uint64_t a = gs + (uint64_t)l * ES;
-                            if (a < lo || a + ES > hi) {
-                                if (ES == 4)
-                                    *reinterpret_cast<uint32_t *>(slot + (a - g0)) =
-                                        __ldg(reinterpret_cast<const unsigned int *>(a));
-                                else
-                                    *reinterpret_cast<uint16_t *>(slot + (a - g0)) =
-                                        __ldg(reinterpret_cast<const unsigned short *>(a));
-                            }
-                        }
-                    }
-                }
-                if (tid == 32) {
-                    for (int i = 0; i < head; ++i)
-                        if (ES == 4)
-                            reinterpret_cast<uint32_t *>(slot)[i] = E::kNegInfWord;
-                        else
-                            reinterpret_cast<uint16_t *>(slot)[i] = (uint16_t)E::kNegInfWord;
-                    for (int i = head + slice_n; i < nv * W; ++i)
-                        if (ES == 4)
-                            reinterpret_cast<uint32_t *>(slot)[i] = E::kNegInfWord;
-                        else
-                            reinterpret_cast<uint16_t *>(slot)[i] = (uint16_t)E::kNegInfWord;
-                }
             } else {
                 failed = true;
                 atomicAdd(&p.err[kErrTimeout], 1);
             }
         }
-        failed = __syncthreads_or(failed);
+        // Elements the copy could not cover (only at the very beginning or end
+        // of an unaligned tensor): plain loads, then a barrier before use.
+        if (g0 < p.lo_clip || ((ge + 15) & ~15ull) > p.hi_clip) {
+            if (tid < 16 && !failed) {
+                const int l = tid < 8 ? tid : slice_n - 16 + tid;
+                if (l >= 0 && l < slice_n) {
+                    const uint64_t a = gs + (uint64_t)l * ES;
+                    if (a < lo || a + ES > hi) {
+                        if (ES == 4)
+                            *reinterpret_cast<uint32_t *>(slot + (a - g0)) =
+                                __ldg(reinterpret_cast<const unsigned int *>(a));
+                        else
+                            *reinterpret_cast<uint16_t *>(slot + (a - g0)) =
+                                __ldg(reinterpret_cast<const unsigned short *>(a));
+                    }
+                }
+            }
+            __syncthreads();
+        }
 
-        // ---- the slice into registers (vectors past the slice read as -inf)
+        // ---- the slice into registers; vectors past it and the elements of
+        // the (at most two) partial vectors outside it read as -inf
         const uint4 kNeg = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord,
                                       E::kNegInfWord);
         uint4 x[VPT];
-        uint4 xt = kNeg;  // thread 0: the target's vector
-        float mx = -INFINITY;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = tid + k * NT;
             x[k] = kNeg;
-            if (v < nv && !failed) x[k] = lds128(slot + 16 * v);
+            if (v < nv) x[k] = lds128(slot + 16 * v);
         }
-        if (tid == 0 && has_t && !failed) {
+        if ((head_partial || tail_partial) && (tid == 0 || tid == (nv - 1) % NT)) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = tid + k * NT;
+                if ((v == 0 && head_partial) || (v == nv - 1 && tail_partial)) {
+                    float z[W];
+                    E::unpack(x[k], z);
+                    const int l0 = v * W - head;
+#pragma unroll
+                    for (int i = 0; i < W; ++i)
+                        if ((unsigned)(l0 + i) >= (unsigned)slice_n) z[i] = -INFINITY;
+                    x[k] = E::pack(z);
+                }
+            }
+        }
+        // thread 0 also takes the target's vector (masked the same way)
+        uint4 xt = kNeg;
+        if (tid == 0 && has_t) {
             xt = lds128(slot + 16 * v_t);
-            zt_sh = E::load(slot + (size_t)tl * ES);
+            float z[W];
+            E::unpack(xt, z);
+            const int l0 = v_t * W - head;
+#pragma unroll
+            for (int i = 0; i < W; ++i)
+                if ((unsigned)(l0 + i) >= (unsigned)slice_n) z[i] = -INFINITY;
+            xt = E::pack(z);
+            zt_sh[par] = E::load(slot + (size_t)tl * ES);
         }
+
         // ---- Step 1: slice max
+        float mx = -INFINITY;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) mx = fmaxf(mx, E::vmax(x[k]));
         mx = warp_max(mx);
-        if (lane == 0) red_a[warp] = mx;
-        __syncthreads();  // the slot is no longer read: hand it back to the copy engine
+        if (lane == 0) red_max[par][warp] = mx;
+        failed = __syncthreads_or(failed);  // the slot is no longer read: back to the copy engine
         if (tid == 0 && !failed && issued < nrows) {
             fence_proxy_async();
             issue(issued);
             ++issued;
         }
-        float m = lane < NW ? red_a[lane] : -INFINITY;
+        float m = lane < NW ? red_max[par][lane] : -INFINITY;
         m = warp_max(m);
         // An empty slice (C < K*SE) has m = -inf: it publishes M = -inf, S = 0
         // and takes a finite offset for its (absent) exponentials.
         const float M_loc = m * kLog2e;
         const float M_off = m == -INFINITY ? 0.f : M_loc;
-        float zt = has_t ? zt_sh : 0.f;
+        float zt = has_t ? zt_sh[par] : 0.f;
 
-        // ---- Step 2: exponentials kept in registers; their sum without the
-        // target's term (added back after the combine, so that 1 - p_t keeps
-        // its relative precision when the target dominates the row).  The
-        // target's vector is left out whole; thread 0 adds its other elements.
-        float e[VPT][W];
-        float sa = 0.f, sb = 0.f;
+        // ---- Step 2: exponentials kept in registers (fp32 pairs); their sum
+        // without the target's term (added back after the combine, so that
+        // 1 - p_t keeps its relative precision when the target dominates the
+        // row).  The target's vector is left out whole; thread 0 adds its other
+        // elements.
+        const unsigned long long nM2 = f2_pack(-M_off, -M_off);
+        unsigned long long e2[VPT][W2];
+        unsigned long long acc = 0ull;  // (0.f, 0.f)
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = tid + k * NT;
-            float z[W];
-            E::unpack(x[k], z);
+            unsigned long long z2[W2];
+            E::unpack2(x[k], z2);
 #pragma unroll
-            for (int i = 0; i < W; ++i) e[k][i] = ex2(fmaf(z[i], kLog2e, -M_off));
-            float lo4 = (e[k][0] + e[k][1]) + (e[k][2] + e[k][3]);
-            float hi4 = 0.f;
-            if (W == 8) hi4 = (e[k][4] + e[k][5]) + (e[k][6] + e[k][7]);
-            const bool keep = v != v_t;
-            sa += keep ? lo4 : 0.f;
-            sb += keep ? hi4 : 0.f;
+            for (int i = 0; i < W2; ++i) {
+                float a, b;
+                f2_unpack(f2_fma(z2[i], kL2E2, nM2), a, b);
+                e2[k][i] = f2_pack(ex2(a), ex2(b));
+            }
+            unsigned long long vs = W2 == 4 ? f2_add(f2_add(e2[k][0], e2[k][1]),
+                                                     f2_add(e2[k][W2 - 2], e2[k][W2 - 1]))
+                                            : f2_add(e2[k][0], e2[k][W2 - 1]);
+            if (v != v_t) acc = f2_add(acc, vs);
         }
+        float sa, sb;
+        f2_unpack(acc, sa, sb);
         if (tid == 0 && has_t) {
             float z[W];
             E::unpack(xt, z);
@@ -226,52 +248,58 @@ __global__ void __launch_bounds__(NT, 512 / NT)
             for (int i = 0; i < W; ++i)
                 if (i != d) sa += ex2(fmaf(z[i], kLog2e, -M_off));
         }
-        float ssum = warp_sum(sa + sb);
-        if (lane == 0) red_b[warp] = ssum;
-        __syncthreads();
-        float S = lane < NW ? red_b[lane] : 0.f;
-        S = warp_sum(S);
+        const float ssum = warp_sum(sa + sb);
+        if (lane == 0) red_sum[par][warp] = ssum;
 
         float M = M_loc;
-        float rescale = 1.f;  // 2^(M_off - M): this slice's exponentials to the row's offset
-        if (K > 1) {
-            // Combine the K slices' (M_r, S_r) in rank order; every CTA of the
-            // cluster computes the same bits.  Only warp 0 publishes, so only
-            // warp 0 arrives with release semantics.
-            if (tid == 0) part[j & 1] = make_float4(M_loc, S, zt, has_t ? 1.f : 0.f);
-            if (warp == 0)
-                cluster_arrive_release();
-            else
-                cluster_arrive_relaxed();
-            cluster_wait();
-            if (warp == 0) {
-                float4 q = make_float4(-INFINITY, 0.f, 0.f, 0.f);
-                if (lane < K) q = ld_dsmem_f4(&part[j & 1], (uint32_t)lane);
-                float Mg = -INFINITY;
-#pragma unroll
-                for (int r = 0; r < K; ++r) Mg = fmaxf(Mg, __shfl_sync(0xffffffffu, q.x, r));
-                float Sg = 0.f, ztg = 0.f, hg = 0.f;
-#pragma unroll
-                for (int r = 0; r < K; ++r) {
-                    const float Mr = __shfl_sync(0xffffffffu, q.x, r);
-                    const float Sr = __shfl_sync(0xffffffffu, q.y, r);
-                    const float zr = __shfl_sync(0xffffffffu, q.z, r);
-                    const float hr = __shfl_sync(0xffffffffu, q.w, r);
-                    if (Sr != 0.f) Sg += Sr * ex2(Mr - Mg);
-                    if (hr != 0.f) {
-                        ztg = zr;
-                        hg = 1.f;
-                    }
-                }
-                if (lane == 0) comb = make_float4(Mg, Sg, ztg, hg);
-            }
+        float S;
+        if (K == 1) {
             __syncthreads();
-            const float4 cb = comb;
-            M = cb.x;
-            S = cb.y;
-            zt = cb.z;
-            has_t = cb.w != 0.f;
-            rescale = ex2(M_off - M);
+            S = lane < NW ? red_sum[par][lane] : 0.f;
+            S = warp_sum(S);
+        } else {
+            // Publish (M_r, z_t) and the per-warp sums to the cluster; one
+            // cluster barrier; every warp then combines all K ranks in rank
+            // order (the same bits in every warp of every CTA).
+            if (tid == 0) part[par] = make_float4(M_loc, 0.f, zt, has_t ? 1.f : 0.f);
+            cluster_arrive_release();
+            cluster_wait();
+            float4 q = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+            if (lane < K) q = ld_dsmem_f4(&part[par], (uint32_t)lane);
+            float Mg = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < K; ++r) Mg = fmaxf(Mg, __shfl_sync(0xffffffffu, q.x, r));
+            // lane l reads the sums of warps l, l + 32, ... (rank-major order)
+            float sv[kPartRegs];
+#pragma unroll
+            for (int q2 = 0; q2 < kPartRegs; ++q2) {
+                const int i = lane + 32 * q2;
+                sv[q2] = i < K * NW ? ld_dsmem_f32(&red_sum[par][i % NW], (uint32_t)(i / NW)) : 0.f;
+            }
+            float Sg = 0.f, ztg = 0.f;
+            bool hg = false;
+#pragma unroll
+            for (int r = 0; r < K; ++r) {
+                const float Mr = __shfl_sync(0xffffffffu, q.x, r);
+                const float zr = __shfl_sync(0xffffffffu, q.z, r);
+                const float hr = __shfl_sync(0xffffffffu, q.w, r);
+                // the rank's total: its warps' sums in warp order
+                float Sr = 0.f;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    const int i = r * NW + w;
+                    Sr += __shfl_sync(0xffffffffu, sv[i >> 5], i & 31);
+                }
+                if (Sr != 0.f) Sg += Sr * ex2(Mr - Mg);
+                if (hr != 0.f) {
+                    ztg = zr;
+                    hg = true;
+                }
+            }
+            M = Mg;
+            S = Sg;
+            zt = ztg;
+            has_t = hg;
         }
         // S holds the row's sum without the target's term: S_rest = S (1 - p_t).
         const float s_rest = S;
@@ -280,42 +308,51 @@ __global__ void __launch_bounds__(NT, 512 / NT)
 
         // ---- Step 4: gradient of the slice
         const float scale = (1.0f / S) * p.inv_b;
-        const float escale = scale * rescale;
+        const float escale = K > 1 ? scale * ex2(M_off - M) : scale;
+        const unsigned long long esc2 = f2_pack(escale, escale);
         // (p_t - 1) / B = -S_rest / (S B): no cancellation when p_t is near 1
         const float g_t = -s_rest * scale;
         unsigned char *gbase = p.grad + (g0 - lbase);  // grad byte of vector 0
-        const int tl_own = v_t >= vf0 && v_t < vf1 ? tl : kNoTarget;  // target in a whole vector
         if (!failed) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = tid + k * NT;
                 if (v >= vf0 && v < vf1) {
-                    float g[W];
+                    unsigned long long g2[W2];
 #pragma unroll
-                    for (int i = 0; i < W; ++i) g[i] = e[k][i] * escale;
+                    for (int i = 0; i < W2; ++i) g2[i] = f2_mul(e2[k][i], esc2);
                     if (vec_store) {
-                        *reinterpret_cast<uint4 *>(gbase + 16 * v) = E::pack(g);
+                        *reinterpret_cast<uint4 *>(gbase + 16 * v) = E::pack2(g2);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < W; ++i) E::store(gbase + 16 * v + i * ES, g[i]);
+                        for (int i = 0; i < W2; ++i) {
+                            float a, b;
+                            f2_unpack(g2[i], a, b);
+                            E::store(gbase + 16 * v + (2 * i) * ES, a);
+                            E::store(gbase + 16 * v + (2 * i + 1) * ES, b);
+                        }
                     }
                     // the owner of the target's vector overwrites the target
-                    if (v == v_t && tl_own != kNoTarget) E::store(gbase + (size_t)tl * ES, g_t);
+                    if (v == v_t) E::store(gbase + (size_t)tl * ES, g_t);
                 }
             }
-            // The (at most two) partial vectors: element by element, by their owners.
-            const bool head_partial = vf0 == 1;
-            const bool tail_partial = vf1 == nv - 1 && nv - 1 >= vf0;
+            // the partial vectors: element by element, by their owners
+            if ((head_partial || tail_partial) && (tid == 0 || tid == (nv - 1) % NT)) {
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = tid + k * NT;
-                if ((v == 0 && head_partial) || (v == nv - 1 && tail_partial)) {
-                    const int l0 = v * W - head;
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = tid + k * NT;
+                    if ((v == 0 && head_partial) || (v == nv - 1 && tail_partial)) {
+                        const int l0 = v * W - head;
 #pragma unroll
-                    for (int i = 0; i < W; ++i) {
-                        if ((unsigned)(l0 + i) < (unsigned)slice_n) {
-                            const float gv = v * W + i == tl ? g_t : e[k][i] * escale;
-                            E::store(gbase + 16 * v + i * ES, gv);
+                        for (int i = 0; i < W2; ++i) {
+                            float a, b;
+                            f2_unpack(f2_mul(e2[k][i], esc2), a, b);
+                            if ((unsigned)(l0 + 2 * i) < (unsigned)slice_n)
+                                E::store(gbase + 16 * v + (2 * i) * ES,
+                                         v * W + 2 * i == tl ? g_t : a);
+                            if ((unsigned)(l0 + 2 * i + 1) < (unsigned)slice_n)
+                                E::store(gbase + 16 * v + (2 * i + 1) * ES,
+                                         v * W + 2 * i + 1 == tl ? g_t : b);
                         }
                     }
                 }
