@@ -38,14 +38,14 @@ __global__ void __launch_bounds__(NT, 512 / NT)
     constexpr int W2 = W / 2;  // fp32 pairs per vector
     constexpr int ES = E::kBytes;
     constexpr int kNoTarget = -0x40000000;
-    constexpr int kPartRegs = (NW * K + 31) / 32;  // cluster partial sums held per lane
 
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[kMaxSplitSlots];
     __shared__ float red_max[2][NW];   // per warp, by row parity
     __shared__ float red_sum[2][NW];
     __shared__ float zt_sh[2];
-    __shared__ float4 part[2];         // this CTA's (M, -, z_t, has_t) for the cluster
+    __shared__ float4 part[2];         // this CTA's (M, S, z_t, has_t) for the cluster
+    __shared__ unsigned int warps_summed[2];
     __shared__ float2 tail_scratch[kTailWarps];
     __shared__ int tail_flag;
 
@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(NT, 512 / NT)
     if (tid == 0) {
         for (int s = 0; s < nslots; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
+        warps_summed[0] = warps_summed[1] = 0u;
     }
     __syncthreads();
     long long issued = 0;
@@ -249,47 +250,54 @@ __global__ void __launch_bounds__(NT, 512 / NT)
                 if (i != d) sa += ex2(fmaf(z[i], kLog2e, -M_off));
         }
         const float ssum = warp_sum(sa + sb);
-        if (lane == 0) red_sum[par][warp] = ssum;
 
         float M = M_loc;
         float S;
         if (K == 1) {
+            if (lane == 0) red_sum[par][warp] = ssum;
             __syncthreads();
             S = lane < NW ? red_sum[par][lane] : 0.f;
             S = warp_sum(S);
         } else {
-            // Publish (M_r, z_t) and the per-warp sums to the cluster; one
-            // cluster barrier; every warp then combines all K ranks in rank
-            // order (the same bits in every warp of every CTA).
-            if (tid == 0) part[par] = make_float4(M_loc, 0.f, zt, has_t ? 1.f : 0.f);
-            cluster_arrive_release();
+            // The last warp of the CTA to finish its sum (a shared-memory
+            // ticket) forms the CTA's total and publishes (M_r, S_r, z_t) to the
+            // cluster; it alone arrives with release semantics.  After one
+            // cluster barrier every warp combines the K ranks in rank order
+            // (the same bits in every warp of every CTA).
+            unsigned int last = 0;
+            if (lane == 0) {
+                red_sum[par][warp] = ssum;
+                __threadfence_block();
+                last = atomicAdd(&warps_summed[par], 1u) == NW - 1u;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence_block();
+                float v = lane < NW ? *reinterpret_cast<volatile float *>(&red_sum[par][lane]) : 0.f;
+                v = warp_sum(v);
+                if (lane == 0) {
+                    part[par] = make_float4(M_loc, v, zt, has_t ? 1.f : 0.f);
+                    warps_summed[par] = 0u;
+                }
+                __syncwarp();
+                cluster_arrive_release();
+            } else {
+                cluster_arrive_relaxed();
+            }
             cluster_wait();
             float4 q = make_float4(-INFINITY, 0.f, 0.f, 0.f);
             if (lane < K) q = ld_dsmem_f4(&part[par], (uint32_t)lane);
             float Mg = -INFINITY;
 #pragma unroll
             for (int r = 0; r < K; ++r) Mg = fmaxf(Mg, __shfl_sync(0xffffffffu, q.x, r));
-            // lane l reads the sums of warps l, l + 32, ... (rank-major order)
-            float sv[kPartRegs];
-#pragma unroll
-            for (int q2 = 0; q2 < kPartRegs; ++q2) {
-                const int i = lane + 32 * q2;
-                sv[q2] = i < K * NW ? ld_dsmem_f32(&red_sum[par][i % NW], (uint32_t)(i / NW)) : 0.f;
-            }
             float Sg = 0.f, ztg = 0.f;
             bool hg = false;
 #pragma unroll
             for (int r = 0; r < K; ++r) {
                 const float Mr = __shfl_sync(0xffffffffu, q.x, r);
+                const float Sr = __shfl_sync(0xffffffffu, q.y, r);
                 const float zr = __shfl_sync(0xffffffffu, q.z, r);
                 const float hr = __shfl_sync(0xffffffffu, q.w, r);
-                // the rank's total: its warps' sums in warp order
-                float Sr = 0.f;
-#pragma unroll
-                for (int w = 0; w < NW; ++w) {
-                    const int i = r * NW + w;
-                    Sr += __shfl_sync(0xffffffffu, sv[i >> 5], i & 31);
-                }
                 if (Sr != 0.f) Sg += Sr * ex2(Mr - Mg);
                 if (hr != 0.f) {
                     ztg = zr;
