@@ -346,26 +346,40 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
 constexpr int kTailThreads = 256;
 constexpr int kTailWarps = kTailThreads / 32;
 
-// Total of virtual warp `vw`, valid in lane 0 of the calling warp.
+// Total of virtual warp `vw`, valid in lane 0 of the calling warp.  The
+// lane's row losses are fetched kTailDepth float4s at a time, all loads in
+// flight before the ordered additions.
+constexpr int kTailDepth = 4;
 __device__ __forceinline__ float2 tail_virtual_warp(const Params &p, int vw, int lane) {
     const int vl = vw * 32 + lane;
     const long long B = p.B;
     float hi = 0.f, lo = 0.f;
-    for (long long base = 4LL * vl; base < B; base += 4LL * kTailThreads) {
-        float x[4];
-        if (base + 3 < B) {
-            const float4 q = __ldcg(reinterpret_cast<const float4 *>(p.loss_rows + base));
-            x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
-        } else {
+    for (long long base0 = 4LL * vl; base0 < B; base0 += 4LL * kTailThreads * kTailDepth) {
+        float4 q[kTailDepth];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) x[k] = base + k < B ? __ldcg(p.loss_rows + base + k) : 0.f;
+        for (int m = 0; m < kTailDepth; ++m) {
+            const long long base = base0 + 4LL * kTailThreads * m;
+            if (base + 3 < B) {
+                q[m] = __ldcg(reinterpret_cast<const float4 *>(p.loss_rows + base));
+            } else {
+                q[m].x = base + 0 < B ? __ldcg(p.loss_rows + base + 0) : 0.f;
+                q[m].y = base + 1 < B ? __ldcg(p.loss_rows + base + 1) : 0.f;
+                q[m].z = base + 2 < B ? __ldcg(p.loss_rows + base + 2) : 0.f;
+                q[m].w = 0.f;
+            }
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float s, e;
-            two_sum(hi, x[k], s, e);
-            hi = s;
-            lo += e;
+        for (int m = 0; m < kTailDepth; ++m) {
+            if (base0 + 4LL * kTailThreads * m < B) {
+                const float x[4] = {q[m].x, q[m].y, q[m].z, q[m].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float s, e;
+                    two_sum(hi, x[k], s, e);
+                    hi = s;
+                    lo += e;
+                }
+            }
         }
     }
 #pragma unroll
@@ -417,79 +431,6 @@ __device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *s
         __syncthreads();
         if (threadIdx.x == 0) tail_write(p, scratch);
     }
-}
-
-// Warp-granular completion: called by every lane of a warp once the warp's
-// row losses are stored.  The last warp of each CTA (counted in shared memory
-// through `cta_count`, zeroed before any warp finishes) takes the CTA's global
-// ticket; the warp that takes the last ticket evaluates the batch loss alone,
-// in the same order as the CTA-wide tail (all eight virtual warps' loads are
-// issued together, then each virtual warp's tree runs).
-__device__ __forceinline__ void finish_warp(const Params &p, unsigned int *cta_count) {
-    const int lane = threadIdx.x & 31;
-    const unsigned int nwarps = blockDim.x >> 5;
-    unsigned int last = 0;
-    __syncwarp();
-    if (lane == 0) {
-        __threadfence();
-        const unsigned int prev = atomicAdd(cta_count, 1u);
-        if (prev == nwarps - 1u) {
-            __threadfence();
-            const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
-            last = atomicAdd(p.ticket, 1u) == total - 1u;
-        }
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence();
-    const long long B = p.B;
-    float hi[kTailWarps], lo[kTailWarps];
-#pragma unroll
-    for (int vw = 0; vw < kTailWarps; ++vw) hi[vw] = lo[vw] = 0.f;
-    for (long long m = 0; 4LL * lane + 4LL * kTailThreads * m < B; ++m) {
-        float x[kTailWarps][4];
-#pragma unroll
-        for (int vw = 0; vw < kTailWarps; ++vw) {
-            const long long base = 4LL * (vw * 32 + lane) + 4LL * kTailThreads * m;
-            if (base + 3 < B) {
-                const float4 q = __ldcg(reinterpret_cast<const float4 *>(p.loss_rows + base));
-                x[vw][0] = q.x; x[vw][1] = q.y; x[vw][2] = q.z; x[vw][3] = q.w;
-            } else {
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    x[vw][k] = base + k < B ? __ldcg(p.loss_rows + base + k) : 0.f;
-            }
-        }
-#pragma unroll
-        for (int vw = 0; vw < kTailWarps; ++vw) {
-            const long long base = 4LL * (vw * 32 + lane) + 4LL * kTailThreads * m;
-            if (base < B) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float s, e;
-                    two_sum(hi[vw], x[vw][k], s, e);
-                    hi[vw] = s;
-                    lo[vw] += e;
-                }
-            }
-        }
-    }
-    float2 totals[kTailWarps];
-#pragma unroll
-    for (int vw = 0; vw < kTailWarps; ++vw) {
-        float h = hi[vw], l = lo[vw];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float h2 = __shfl_down_sync(0xffffffffu, h, o);
-            const float l2 = __shfl_down_sync(0xffffffffu, l, o);
-            float s, e;
-            two_sum(h, h2, s, e);
-            h = s;
-            l += l2 + e;
-        }
-        totals[vw] = make_float2(h, l);
-    }
-    if (lane == 0) tail_write(p, totals);
 }
 
 }  // namespace ce

@@ -3,12 +3,14 @@
 // Each warp owns a private ring of `slots` shared-memory tiles; a tile is
 // `rows_per_tile` consecutive rows of the logits, staged by one TMA bulk copy.
 // Warps act as their own producers, so no CTA-wide barrier is needed until
-// the fused batch-loss tail.  A warp makes three passes of 16-byte vectors
-// over its staged row -- Steps 1-4 of Pass 1 of rumus 0.1.1's
-// cross_entropy.wgsl (max, sum of exponentials, row loss, gradient) -- with
-// warp-shuffle reductions; fp32 rows keep their exponentials in place in
-// shared memory, so every element is exponentiated once.  The
-// last CTA to finish performs Pass 2 (the fixed-order batch-loss sum).
+// the fused batch-loss tail.  A warp reads its staged row from shared memory
+// once, into registers (at most MAXV 16-byte vectors per lane; vectors past
+// the row read as -inf), and computes Steps 1-4 of Pass 1 of rumus 0.1.1's
+// cross_entropy.wgsl (max, sum of exponentials, row loss, gradient) from
+// there with warp-shuffle reductions and packed fp32 pair arithmetic.  fp32
+// rows keep their exponentials in registers, so every element is
+// exponentiated once.  The last CTA to finish performs Pass 2 (the
+// fixed-order batch-loss sum).
 #include <math.h>
 
 #include "ce_launch.h"
@@ -16,18 +18,20 @@
 namespace ce {
 namespace {
 
-template <typename T, int MINB>
+template <typename T, int MAXV, int MINB>
 __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     rows_warp_kernel(Params p, int slots, int rows_per_tile, int slot_bytes) {
     using E = Elem<T>;
     constexpr int NW = kWarpKernelWarps;
     constexpr int ES = E::kBytes;
     constexpr int W = E::kVec;
+    constexpr int W2 = W / 2;
     constexpr bool kKeepExp = sizeof(T) == 4;  // fp32: exponentials replace the logits in place
 
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[NW * kMaxWarpSlots];
-    __shared__ unsigned int warps_done;
+    __shared__ float2 tail_scratch[kTailWarps];
+    __shared__ int tail_flag;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -43,6 +47,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     uint64_t *my_full = full + warp * kMaxWarpSlots;
     const bool vec_store = p.grad_vec_ok != 0;
     const float inv_b = p.inv_b;
+    const unsigned long long kL2E2 = f2_pack(kLog2e, kLog2e);
 
     auto span = [&](long long tile, long long &r0, long long &r1, uint64_t &gs, uint64_t &ge,
                     uint64_t &g0, uint64_t &lo, uint64_t &hi) {
@@ -74,8 +79,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
         for (int s = 0; s < slots; ++s) mbar_init(&my_full[s], 1);
         fence_mbar_init();
     }
-    if (threadIdx.x == 0) warps_done = 0u;
-    __syncthreads();
+    __syncwarp();
     long long issued = 0;
     if (lane == 0) {
         for (; issued < ntl && issued < slots; ++issued) issue(issued);
@@ -141,45 +145,59 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
             const unsigned char *vrow = row + nh * ES;
             const int tv = has_t ? t - nh : -0x40000000;  // target relative to vector 0
             const int v_t = has_t && tv >= 0 && tv < nvec * W ? tv / W : -1;  // its vector
-            const float zt = has_t ? E::load(row + t * ES) : 0.f;
+
+            const uint4 kNeg = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord,
+                                          E::kNegInfWord);
+            uint4 x[MAXV];
+#pragma unroll
+            for (int k = 0; k < MAXV; ++k) {
+                const int v = lane + 32 * k;
+                x[k] = kNeg;
+                if (v < nvec) x[k] = lds128(vrow + 16 * v);
+            }
             const float hz = lane < nh ? E::load(row + lane * ES) : -INFINITY;
             const float tz = lane < nt ? E::load(vrow + (nvec * W + lane) * ES) : -INFINITY;
+            const float zt = has_t ? E::load(row + t * ES) : 0.f;
+            // lane 0 also takes the target's vector
+            const uint4 xt = lane == 0 && v_t >= 0 ? lds128(vrow + 16 * v_t) : kNeg;
 
             // Step 1: max
             float m = fmaxf(hz, tz);
-#pragma unroll 4
-            for (int v = lane; v < nvec; v += 32) m = fmaxf(m, E::vmax(lds128(vrow + 16 * v)));
+#pragma unroll
+            for (int k = 0; k < MAXV; ++k) m = fmaxf(m, E::vmax(x[k]));
             m = warp_max(m);
             const float M = m * kLog2e;
+            const unsigned long long nM2 = f2_pack(-M, -M);
 
             // Step 2: sum of exponentials without the target's term.  The
             // target's vector is left out whole; lane 0 adds its other elements.
-            // fp32 rows get their exponentials written back in place.
-            float sa = 0.f, sb = 0.f;
-#pragma unroll 4
-            for (int v = lane; v < nvec; v += 32) {
-                float z[W];
-                E::unpack(lds128(vrow + 16 * v), z);
+            unsigned long long acc = 0ull;
 #pragma unroll
-                for (int j = 0; j < W; ++j) z[j] = ex2(fmaf(z[j], kLog2e, -M));
-                if (kKeepExp)
-                    *reinterpret_cast<uint4 *>(const_cast<unsigned char *>(vrow) + 16 * v) =
-                        E::pack(z);
-                float a4 = (z[0] + z[1]) + (z[2] + z[3]);
-                float b4 = 0.f;
-                if (W == 8) b4 = (z[4] + z[5]) + (z[6] + z[7]);
-                const bool keep = v != v_t;
-                sa += keep ? a4 : 0.f;
-                sb += keep ? b4 : 0.f;
+            for (int k = 0; k < MAXV; ++k) {
+                const int v = lane + 32 * k;
+                unsigned long long e2[W2];
+                E::unpack2(x[k], e2);
+#pragma unroll
+                for (int j = 0; j < W2; ++j) {
+                    float a, b;
+                    f2_unpack(f2_fma(e2[j], kL2E2, nM2), a, b);
+                    e2[j] = f2_pack(ex2(a), ex2(b));
+                }
+                if (kKeepExp) x[k] = E::pack2(e2);
+                unsigned long long vs = W2 == 4 ? f2_add(f2_add(e2[0], e2[1]),
+                                                         f2_add(e2[W2 - 2], e2[W2 - 1]))
+                                                : f2_add(e2[0], e2[W2 - 1]);
+                if (v != v_t) acc = f2_add(acc, vs);
             }
-            __syncwarp();
+            float sa, sb;
+            f2_unpack(acc, sa, sb);
             if (lane == 0 && v_t >= 0) {
                 float z[W];
-                E::unpack(lds128(vrow + 16 * v_t), z);
+                E::unpack(xt, z);
                 const int d = tv - v_t * W;
 #pragma unroll
                 for (int j = 0; j < W; ++j)
-                    if (j != d) sa += kKeepExp ? z[j] : ex2(fmaf(z[j], kLog2e, -M));
+                    if (j != d) sa += ex2(fmaf(z[j], kLog2e, -M));
             }
             const float eh = lane < nh ? ex2(fmaf(hz, kLog2e, -M)) : 0.f;
             const float et = lane < nt ? ex2(fmaf(tz, kLog2e, -M)) : 0.f;
@@ -191,24 +209,39 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
 
             // Step 4: gradient; (p_t - 1) / B = -S_rest / (S B)
             const float scale = (1.0f / S) * inv_b;
+            const unsigned long long sc2 = f2_pack(scale, scale);
             const float g_t = -s_rest * scale;
             unsigned char *grow = p.grad + (size_t)r * C * ES;
             unsigned char *gvec = grow + nh * ES;
-#pragma unroll 4
-            for (int v = lane; v < nvec; v += 32) {
-                float g[W];
-                E::unpack(lds128(vrow + 16 * v), g);
 #pragma unroll
-                for (int j = 0; j < W; ++j)
-                    g[j] = (kKeepExp ? g[j] : ex2(fmaf(g[j], kLog2e, -M))) * scale;
-                if (vec_store) {
-                    *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack(g);
-                } else {
+            for (int k = 0; k < MAXV; ++k) {
+                const int v = lane + 32 * k;
+                if (v < nvec) {
+                    unsigned long long g2[W2];
+                    E::unpack2(x[k], g2);
 #pragma unroll
-                    for (int j = 0; j < W; ++j) E::store(gvec + (v * W + j) * ES, g[j]);
+                    for (int j = 0; j < W2; ++j) {
+                        if (!kKeepExp) {
+                            float a, b;
+                            f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
+                            g2[j] = f2_pack(ex2(a), ex2(b));
+                        }
+                        g2[j] = f2_mul(g2[j], sc2);
+                    }
+                    if (vec_store) {
+                        *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack2(g2);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < W2; ++j) {
+                            float a, b;
+                            f2_unpack(g2[j], a, b);
+                            E::store(gvec + (v * W + 2 * j) * ES, a);
+                            E::store(gvec + (v * W + 2 * j + 1) * ES, b);
+                        }
+                    }
+                    // the owner of the target's vector overwrites the target
+                    if (v == v_t) E::store(grow + (size_t)t * ES, g_t);
                 }
-                // the owner of the target's vector overwrites the target
-                if (v == v_t) E::store(grow + (size_t)t * ES, g_t);
             }
             if (lane < nh) E::store(grow + lane * ES, lane == t ? g_t : eh * scale);
             if (lane < nt) {
@@ -242,13 +275,13 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
             if (!mbar_wait(&my_full[i % slots], (uint32_t)((i / slots) & 1))) break;
         }
     }
-    finish_warp(p, &warps_done);
+    finish_cta(p, &tail_flag, tail_scratch);
 }
 
-template <typename T, int MINB>
-cudaError_t launch_m(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
+template <typename T, int MAXV, int MINB>
+cudaError_t launch_v(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
                      int smem, cudaStream_t s) {
-    auto kern = rows_warp_kernel<T, MINB>;
+    auto kern = rows_warp_kernel<T, MAXV, MINB>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -259,12 +292,40 @@ cudaError_t launch_m(const Params &p, int ctas, int slots, int rows_per_tile, in
     return cudaLaunchKernelEx(&cfg, kern, p, slots, rows_per_tile, slot_bytes);
 }
 
-template <typename T, int MINB>
-cudaError_t occ_m(int smem, int *ctas) {
-    auto kern = rows_warp_kernel<T, MINB>;
+template <typename T, int MAXV, int MINB>
+cudaError_t occ_v(int smem, int *ctas) {
+    auto kern = rows_warp_kernel<T, MAXV, MINB>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, kWarpKernelWarps * 32, smem);
+}
+
+// Vectors per lane: a row of C elements holds at most C*ES/16 whole vectors.
+int vectors_per_lane(long long C, int es) {
+    const long long nvec = C * es / 16;
+    const long long per_lane = (nvec + 31) / 32;
+    return per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8 : 16;
+}
+
+template <typename T, int MINB>
+cudaError_t launch_m(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
+                     int smem, cudaStream_t s) {
+    switch (vectors_per_lane(p.C, sizeof(T))) {
+        case 2: return launch_v<T, 2, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+        case 4: return launch_v<T, 4, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+        case 8: return launch_v<T, 8, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+        default: return launch_v<T, 16, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+    }
+}
+
+template <typename T, int MINB>
+cudaError_t occ_m(long long C, int smem, int *ctas) {
+    switch (vectors_per_lane(C, sizeof(T))) {
+        case 2: return occ_v<T, 2, MINB>(smem, ctas);
+        case 4: return occ_v<T, 4, MINB>(smem, ctas);
+        case 8: return occ_v<T, 8, MINB>(smem, ctas);
+        default: return occ_v<T, 16, MINB>(smem, ctas);
+    }
 }
 
 template <typename T>
@@ -276,9 +337,8 @@ cudaError_t launch_t(const Params &p, int per_sm, int ctas, int slots, int rows_
 
 template <typename T>
 cudaError_t occ_t(int per_sm, long long C, int smem, int *ctas) {
-    (void)C;
-    if (per_sm >= 2) return occ_m<T, 2>(smem, ctas);
-    return occ_m<T, 1>(smem, ctas);
+    if (per_sm >= 2) return occ_m<T, 2>(C, smem, ctas);
+    return occ_m<T, 1>(C, smem, ctas);
 }
 
 }  // namespace
