@@ -7,7 +7,7 @@
 // once, into registers (at most MAXV 16-byte vectors per lane; vectors past
 // the row read as -inf), and computes Steps 1-4 of Pass 1 of rumus 0.1.1's
 // cross_entropy.wgsl (max, sum of exponentials, row loss, gradient) from
-// there with warp-shuffle reductions.  fp32
+// there with warp-shuffle reductions and packed fp32 pair arithmetic.  fp32
 // rows keep their exponentials in registers, so every element is
 // exponentiated once.  The last CTA to finish performs Pass 2 (the
 // fixed-order batch-loss sum).
@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     constexpr int NW = kWarpKernelWarps;
     constexpr int ES = E::kBytes;
     constexpr int W = E::kVec;
+    constexpr int W2 = W / 2;
     constexpr bool kKeepExp = sizeof(T) == 4;  // fp32: exponentials replace the logits in place
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     uint64_t *my_full = full + warp * kMaxWarpSlots;
     const bool vec_store = p.grad_vec_ok != 0;
     const float inv_b = p.inv_b;
+    const unsigned long long kL2E2 = f2_pack(kLog2e, kLog2e);
 
     auto span = [&](long long tile, long long &r0, long long &r1, uint64_t &gs, uint64_t &ge,
                     uint64_t &g0, uint64_t &lo, uint64_t &hi) {
@@ -144,45 +146,51 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
             const int tv = has_t ? t - nh : -0x40000000;  // target relative to vector 0
             const int v_t = has_t && tv >= 0 && tv < nvec * W ? tv / W : -1;  // its vector
 
-            // Lanes past the last whole vector re-read it: harmless for the max,
-            // and they are left out of the sum and the stores.
-            const int vlast = nvec > 0 ? nvec - 1 : 0;
+            const uint4 kNeg = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord,
+                                          E::kNegInfWord);
             uint4 x[MAXV];
 #pragma unroll
-            for (int k = 0; k < MAXV; ++k) x[k] = lds128(vrow + 16 * min(lane + 32 * k, vlast));
+            for (int k = 0; k < MAXV; ++k) {
+                const int v = lane + 32 * k;
+                x[k] = kNeg;
+                if (v < nvec) x[k] = lds128(vrow + 16 * v);
+            }
             const float hz = lane < nh ? E::load(row + lane * ES) : -INFINITY;
             const float tz = lane < nt ? E::load(vrow + (nvec * W + lane) * ES) : -INFINITY;
             const float zt = has_t ? E::load(row + t * ES) : 0.f;
             // lane 0 also takes the target's vector
-            const uint4 xt = lane == 0 && v_t >= 0 ? lds128(vrow + 16 * v_t) : x[0];
+            const uint4 xt = lane == 0 && v_t >= 0 ? lds128(vrow + 16 * v_t) : kNeg;
 
             // Step 1: max
             float m = fmaxf(hz, tz);
-            if (nvec > 0) {
 #pragma unroll
-                for (int k = 0; k < MAXV; ++k) m = fmaxf(m, E::vmax(x[k]));
-            }
+            for (int k = 0; k < MAXV; ++k) m = fmaxf(m, E::vmax(x[k]));
             m = warp_max(m);
             const float M = m * kLog2e;
+            const unsigned long long nM2 = f2_pack(-M, -M);
 
             // Step 2: sum of exponentials without the target's term.  The
             // target's vector is left out whole; lane 0 adds its other elements.
-            float sa = 0.f, sb = 0.f;
+            unsigned long long acc = 0ull;
 #pragma unroll
             for (int k = 0; k < MAXV; ++k) {
                 const int v = lane + 32 * k;
-                float z[W];
-                E::unpack(x[k], z);
+                unsigned long long e2[W2];
+                E::unpack2(x[k], e2);
 #pragma unroll
-                for (int j = 0; j < W; ++j) z[j] = ex2(fmaf(z[j], kLog2e, -M));
-                if (kKeepExp) x[k] = E::pack(z);
-                const float a4 = (z[0] + z[1]) + (z[2] + z[3]);
-                float b4 = 0.f;
-                if (W == 8) b4 = (z[W - 4] + z[W - 3]) + (z[W - 2] + z[W - 1]);
-                const bool keep = v < nvec && v != v_t;
-                sa += keep ? a4 : 0.f;
-                if (W == 8) sb += keep ? b4 : 0.f;
+                for (int j = 0; j < W2; ++j) {
+                    float a, b;
+                    f2_unpack(f2_fma(e2[j], kL2E2, nM2), a, b);
+                    e2[j] = f2_pack(ex2(a), ex2(b));
+                }
+                if (kKeepExp) x[k] = E::pack2(e2);
+                unsigned long long vs = W2 == 4 ? f2_add(f2_add(e2[0], e2[1]),
+                                                         f2_add(e2[W2 - 2], e2[W2 - 1]))
+                                                : f2_add(e2[0], e2[W2 - 1]);
+                if (v != v_t) acc = f2_add(acc, vs);
             }
+            float sa, sb;
+            f2_unpack(acc, sa, sb);
             if (lane == 0 && v_t >= 0) {
                 float z[W];
                 E::unpack(xt, z);
@@ -201,6 +209,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
 
             // Step 4: gradient; (p_t - 1) / B = -S_rest / (S B)
             const float scale = (1.0f / S) * inv_b;
+            const unsigned long long sc2 = f2_pack(scale, scale);
             const float g_t = -s_rest * scale;
             unsigned char *grow = p.grad + (size_t)r * C * ES;
             unsigned char *gvec = grow + nh * ES;
@@ -208,16 +217,27 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
             for (int k = 0; k < MAXV; ++k) {
                 const int v = lane + 32 * k;
                 if (v < nvec) {
-                    float g[W];
-                    E::unpack(x[k], g);
+                    unsigned long long g2[W2];
+                    E::unpack2(x[k], g2);
 #pragma unroll
-                    for (int j = 0; j < W; ++j)
-                        g[j] = (kKeepExp ? g[j] : ex2(fmaf(g[j], kLog2e, -M))) * scale;
+                    for (int j = 0; j < W2; ++j) {
+                        if (!kKeepExp) {
+                            float a, b;
+                            f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
+                            g2[j] = f2_pack(ex2(a), ex2(b));
+                        }
+                        g2[j] = f2_mul(g2[j], sc2);
+                    }
                     if (vec_store) {
-                        *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack(g);
+                        *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack2(g2);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < W; ++j) E::store(gvec + (v * W + j) * ES, g[j]);
+                        for (int j = 0; j < W2; ++j) {
+                            float a, b;
+                            f2_unpack(g2[j], a, b);
+                            E::store(gvec + (v * W + 2 * j) * ES, a);
+                            E::store(gvec + (v * W + 2 * j + 1) * ES, b);
+                        }
                     }
                     // the owner of the target's vector overwrites the target
                     if (v == v_t) E::store(grow + (size_t)t * ES, g_t);
