@@ -41,7 +41,9 @@ typedef enum {
     CE_ERR_POINTER = 7,  /* a pointer is not accessible from the current device */
     CE_ERR_CAPTURE = 8,  /* the call needs to grow its workspace while the
                             stream is being captured; call once uncaptured first */
-    CE_ERR_PATH = 9      /* a forced path/split cannot run this shape           */
+    CE_ERR_PATH = 9,     /* a forced path/split cannot run this shape           */
+    CE_ERR_SCRATCH = 10  /* ce_fwd_bwd_noalloc: the shape needs more scratch than
+                            its static array holds                               */
 } ce_status;
 
 /* Kernel paths (for ce_fwd_bwd_path and ce_query_plan). */
@@ -118,6 +120,34 @@ int ce_get_device_errors(void *stream, int32_t *bad_targets, int32_t *timeouts);
 
 /* Free every cached workspace of every device (after their streams are idle). */
 int ce_release_workspaces(void);
+
+/*
+ * ce_fwd_bwd_noalloc -- ce_fwd_bwd for callers that cannot allocate device
+ * memory.  The pages have no counterpart; this entry point exists for the
+ * library's users.  Some callers may not call cudaMalloc at all: code that
+ * runs under a memory manager which owns the whole device, code with a device
+ * memory budget fixed at start-up, and code that must never stall on the
+ * implicit device synchronisation cudaMalloc and cudaFree can cause.  This
+ * entry point allocates nothing: its scratch (a completion ticket, two error
+ * counters and one fp32 loss per row, 1 MiB + 256 bytes in all) lives in a
+ * statically sized device array of the library, which every GPU that loads
+ * the library holds until the process exits.
+ *
+ *   Arguments, layout, ownership and results are those of ce_fwd_bwd.
+ *   Limits: B <= 262144, and rows short enough to be staged in shared memory
+ *   (under 64 KB per CTA of a cluster of up to 8: C <= 131008 fp32 or 262080
+ *   bf16 classes); anything larger returns CE_ERR_SCRATCH before any launch.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.  Every call shares the one array and clears its
+ *   ticket and counters on `stream` first, so calls whose kernels overlap on
+ *   the GPU (other streams, other host threads) race and must be serialised
+ *   by the caller.  The device error counters of this entry point are not
+ *   readable through ce_get_device_errors; an out-of-range target still makes
+ *   the loss NaN.
+ */
+int ce_fwd_bwd_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C,
+                       int dtype, float *loss_out, void *grad_out, void *stream);
 
 /* Static text for a ce_status value. */
 const char *ce_status_string(int status);

@@ -34,11 +34,12 @@ PATH_NAMES = {CE_PATH_ROWS_WARP: "rows_warp", CE_PATH_ROW_SPLIT: "row_split",
 
 STATUS = {0: "CE_OK", 1: "CE_ERR_NULL", 2: "CE_ERR_SHAPE", 3: "CE_ERR_DTYPE",
           4: "CE_ERR_ALIGN", 5: "CE_ERR_CUDA", 6: "CE_ERR_OVERLAP", 7: "CE_ERR_POINTER",
-          8: "CE_ERR_CAPTURE", 9: "CE_ERR_PATH"}
+          8: "CE_ERR_CAPTURE", 9: "CE_ERR_PATH", 10: "CE_ERR_SCRATCH"}
 
 # Symbols declared in include/ce.h.
 EXPORTS = ("ce_fwd_bwd", "ce_fwd_bwd_path", "ce_query_plan", "ce_get_device_errors",
-           "ce_release_workspaces", "ce_status_string", "ce_last_cuda_error")
+           "ce_release_workspaces", "ce_status_string", "ce_last_cuda_error",
+           "ce_fwd_bwd_noalloc")
 
 
 class CEError(RuntimeError):
@@ -78,6 +79,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.ce_status_string.restype = ctypes.c_char_p
     lib.ce_last_cuda_error.argtypes = []
     lib.ce_last_cuda_error.restype = ctypes.c_char_p
+    lib.ce_fwd_bwd_noalloc.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp]
+    lib.ce_fwd_bwd_noalloc.restype = ci
     if path is None:
         _lib = lib
     return lib
@@ -148,6 +151,23 @@ def ce_fwd_bwd_raw(logits_ptr: int, targets_ptr: int, B: int, C: int, dtype: int
     """The C call with raw integer pointers; returns the ce_status (no raise)."""
     return load_library().ce_fwd_bwd_path(logits_ptr, targets_ptr, B, C, dtype, loss_ptr,
                                           grad_ptr, stream, path, split)
+
+
+def ce_fwd_bwd_noalloc(logits, targets, loss_out, grad_out, stream=None) -> None:
+    """ce_fwd_bwd without any device allocation, for callers that cannot call
+    cudaMalloc (a memory manager owns the device, a fixed memory budget, or no
+    tolerance for the synchronisation an allocation can cause).  Its scratch
+    is a static device array of the library (B <= 262144); calls that overlap
+    on the GPU share it and race.  Make the first call on a device before any
+    stream capture."""
+    lib = load_library()
+    if logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous [B, C] tensor")
+    if grad_out.shape != logits.shape or grad_out.dtype != logits.dtype or not grad_out.is_contiguous():
+        raise ValueError("grad_out must be a contiguous tensor of the logits' shape and dtype")
+    B, C = logits.shape
+    _check(lib.ce_fwd_bwd_noalloc(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
+                                  _ptr(loss_out), _ptr(grad_out), _stream_handle(stream)))
 
 
 def ce_query_plan(B: int, C: int, dtype: int) -> dict:

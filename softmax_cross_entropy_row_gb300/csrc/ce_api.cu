@@ -416,6 +416,114 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     return CE_OK;
 }
 
+// ------------------------------------------------- allocation-free entry point
+//
+// ce_fwd_bwd_noalloc keeps its scratch (the CTA ticket, the error counters
+// and one fp32 loss per row) in a statically sized device array of this
+// file instead of a cudaMalloc'd per-stream workspace.  Every device that
+// loads the library holds the array until the process exits.
+
+constexpr long long kNoAllocMaxRows = 262144;
+constexpr size_t kNoAllocScratchBytes = kHeaderBytes + (size_t)kNoAllocMaxRows * sizeof(float);
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+std::map<int, unsigned char *> g_noalloc_base;  // device -> address of g_noalloc_scratch
+
+// The device address of the static scratch on device `dev` (which must be
+// current), looked up once per device.  In host code the array's name is only
+// a stand-in, so the address has to come from cudaGetSymbolAddress.
+int noalloc_scratch(int dev, unsigned char **out) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    auto it = g_noalloc_base.find(dev);
+    if (it != g_noalloc_base.end()) {
+        *out = it->second;
+        return CE_OK;
+    }
+    void *ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_noalloc_base[dev] = static_cast<unsigned char *>(ptr);
+    *out = static_cast<unsigned char *>(ptr);
+    return CE_OK;
+}
+
+int run_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
+                float *loss_out, void *grad_out, void *stream) {
+    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_DTYPE;
+    if (!logits || !targets || !loss_out || !grad_out) return CE_ERR_NULL;
+    if (B < 1 || C < 1 || B > 0x7fffffffLL || C > 0x7fffffffLL) return CE_ERR_SHAPE;
+    if (B > kNoAllocMaxRows) return CE_ERR_SCRATCH;
+    const int es = dtype == CE_F32 ? 4 : 2;
+    if ((unsigned long long)B * (unsigned long long)C > (1ull << 61) / (unsigned)es)
+        return CE_ERR_SHAPE;
+    const uintptr_t lz = reinterpret_cast<uintptr_t>(logits);
+    const uintptr_t gz = reinterpret_cast<uintptr_t>(grad_out);
+    const uintptr_t tz = reinterpret_cast<uintptr_t>(targets);
+    const uintptr_t oz = reinterpret_cast<uintptr_t>(loss_out);
+    if (lz % es || gz % es || tz % 4 || oz % 4) return CE_ERR_ALIGN;
+    const size_t nbytes = (size_t)B * (size_t)C * es;
+    if (ranges_overlap(gz, nbytes, lz, nbytes) || ranges_overlap(gz, nbytes, tz, (size_t)B * 4) ||
+        ranges_overlap(gz, nbytes, oz, 4))
+        return CE_ERR_OVERLAP;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DeviceInfo d;
+    int rc = device_info(dev, &d);
+    if (rc != CE_OK) return rc;
+    for (const void *ptr : {logits, (const void *)targets, (const void *)loss_out,
+                            (const void *)grad_out}) {
+        if ((rc = check_pointer(ptr, d)) != CE_OK) return rc;
+    }
+    Plan pl;
+    if ((rc = make_plan(B, C, dtype, CE_PATH_AUTO, 0, &pl)) != CE_OK) return rc;
+    // the streaming path needs per-chunk partials the static scratch does not hold
+    if (pl.path == CE_PATH_STREAM) return CE_ERR_SCRATCH;
+
+    unsigned char *base = nullptr;
+    if ((rc = noalloc_scratch(dev, &base)) != CE_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The array keeps the last call's contents: the ticket and the error
+    // counters must start at zero, the row losses are all rewritten.
+    if ((e = cudaMemsetAsync(base, 0, kHeaderBytes, s)) != cudaSuccess) return cuda_fail(e);
+
+    Params p;
+    p.logits = static_cast<const unsigned char *>(logits);
+    p.targets = targets;
+    p.grad = static_cast<unsigned char *>(grad_out);
+    p.loss_out = loss_out;
+    p.ticket = reinterpret_cast<unsigned int *>(base);
+    p.err = reinterpret_cast<int *>(base + 4);
+    p.loss_rows = reinterpret_cast<float *>(base + kHeaderBytes);
+    p.parts = nullptr;
+    p.zt = nullptr;
+    p.B = B;
+    p.C = C;
+    p.inv_b = (float)(1.0 / (double)B);
+    p.lo_clip = (uint64_t)((lz + 15) & ~(uintptr_t)15);
+    p.hi_clip = (uint64_t)((lz + nbytes) & ~(uintptr_t)15);
+    if (p.hi_clip < p.lo_clip) p.hi_clip = p.lo_clip;
+    p.grad_vec_ok = ((gz - lz) % 16) == 0;
+
+    if (pl.path == CE_PATH_ROWS_WARP)
+        e = ce::launch_rows_warp(p, dtype, pl.per_sm, pl.ctas, pl.nslots, pl.rows_per_tile,
+                                 pl.slot_bytes, pl.smem, s);
+    else
+        e = ce::launch_split(p, dtype, pl.split, pl.threads, pl.ctas, pl.nslots, pl.slot_bytes,
+                             pl.slice, pl.smem, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CE_OK;
+}
+
 }  // namespace
 
 namespace ce {
@@ -515,10 +623,18 @@ const char *ce_status_string(int status) {
         case CE_ERR_POINTER: return "pointer not accessible from the current device";
         case CE_ERR_CAPTURE: return "workspace must grow while the stream is being captured";
         case CE_ERR_PATH: return "the forced path cannot run this shape";
+        case CE_ERR_SCRATCH:
+            return "shape exceeds the static scratch of ce_fwd_bwd_noalloc (B <= 262144, "
+                   "rows held in shared memory)";
         default: return "unknown status";
     }
 }
 
 const char *ce_last_cuda_error(void) { return g_cuda_error; }
+
+int ce_fwd_bwd_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C,
+                       int dtype, float *loss_out, void *grad_out, void *stream) {
+    return run_noalloc(logits, targets, B, C, dtype, loss_out, grad_out, stream);
+}
 
 }  // extern "C"

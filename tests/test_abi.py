@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_need_no_gpu(lib):
-    for code in range(10):
+    for code in range(11):
         s = lib.ce_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.ce_status_string(99).decode() == "unknown status"
