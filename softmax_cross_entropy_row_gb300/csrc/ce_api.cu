@@ -101,6 +101,7 @@ struct Plan {
     long long slice = 0;  // classes per slice (split path)
     int rows_per_tile = 0;
     int per_sm = 1;       // warp path: the build for 1 or 2 resident CTAs per SM
+    int vecs = 8;         // split path: 16-byte vectors per thread (8 or 16)
     long long chunks = 0; // stream path
 };
 
@@ -171,58 +172,62 @@ int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, 
     return CE_OK;
 }
 
-// Tuning knob: CE_SPLIT_THREADS=256 selects the split-row build with two
-// 256-thread CTAs per SM (slices of at most 32 KB); default 512, one CTA per SM.
-int split_threads() {
-    static const int n = [] {
-        const char *e = getenv("CE_SPLIT_THREADS");
-        return (e && atoi(e) == 256) ? 256 : ce::kSplitThreads;
-    }();
-    return n;
-}
-
+// Split-row path: K CTAs per row (a cluster when K > 1), each holding a
+// slice of SE classes in registers (at most kSplitThreads x 16 vectors, i.e.
+// 128 KB) with a ring of at least two shared-memory slots.  The smallest such
+// K is chosen: fewer CTAs per row means fewer cluster barriers per byte.
 int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype, int K_forced,
                Plan *pl) {
-    const int threads = split_threads();
-    const int per_sm = 512 / threads;
-    const int budget = d.smem_optin / per_sm - kStaticSmemReserve;
-    // A CTA holds a slice of at most threads * kSplitVecs 16-byte vectors in
-    // registers; its slot is one such slice plus the alignment margin.
-    const long long max_slice_bytes = (long long)threads * ce::kSplitVecs * 16 - 16;
+    const int budget = d.smem_optin - kStaticSmemReserve;
+    const long long per_vec_cap = (long long)ce::kSplitThreads * 16;  // bytes per vector slot
     auto slice_of = [&](int K) {
         long long se = (C + K - 1) / K;
         return (se + 7) / 8 * 8;  // slices start 16-byte aligned relative to the row
     };
-    auto fits = [&](int K) { return slice_of(K) * es <= max_slice_bytes; };
+    // vectors per thread for a slice (its bytes plus the two partial vectors)
+    auto vecs_of = [&](long long se) {
+        const long long need = se * es + 32;
+        return need <= 8 * per_vec_cap ? 8 : need <= 16 * per_vec_cap ? 16 : 0;
+    };
+    auto slot_of = [&](long long se) { return (long long)round_up(se * es + 32, 128); };
+    auto nslots_of = [&](long long se) {
+        long long n = budget / slot_of(se);
+        return (int)(n > ce::kMaxSplitSlots ? ce::kMaxSplitSlots : n);
+    };
+    // bf16 slices re-evaluate their exponentials for the gradient: with 16
+    // vectors per thread that build spills, so bf16 prefers 8 (64 KB slices).
+    const int auto_max_vecs = es == 2 ? 8 : 16;
     int K = K_forced;
     if (K == 0) {
-        for (int k : {1, 2, 4, 8}) {
-            if (fits(k)) {
+        for (int k : {1, 2, 3, 4, 6, 8}) {
+            const long long se = slice_of(k);
+            const int v = vecs_of(se);
+            if (v && v <= auto_max_vecs && nslots_of(se) >= 2) {
                 K = k;
                 break;
             }
         }
         if (K == 0) return CE_ERR_PATH;
     }
-    if (K != 1 && K != 2 && K != 4 && K != 8) return CE_ERR_PATH;
-    if (!fits(K)) return CE_ERR_PATH;
+    if (K != 1 && K != 2 && K != 3 && K != 4 && K != 6 && K != 8) return CE_ERR_PATH;
     const long long se = slice_of(K);
-    const long long slot_bytes = round_up(se * es + 32, 128);
-    if (slot_bytes > budget) return CE_ERR_PATH;
-    int nslots = (int)(budget / slot_bytes);
-    if (nslots > ce::kMaxSplitSlots) nslots = ce::kMaxSplitSlots;
+    const int vecs = vecs_of(se);
+    const int nslots = nslots_of(se);
+    if (vecs == 0 || nslots < 1) return CE_ERR_PATH;
+    const long long slot_bytes = slot_of(se);
     const int smem = nslots * (int)slot_bytes;
     int clusters = 0;
     int rc = cached_occupancy(
-        dtype, CE_PATH_ROW_SPLIT, K * 1024 + threads, smem,
-        [&](int *v) { return ce::split_max_clusters(dtype, K, threads, smem, v); }, &clusters);
+        dtype, CE_PATH_ROW_SPLIT, K * 64 + vecs, smem,
+        [&](int *v) { return ce::split_max_clusters(dtype, K, vecs, smem, v); }, &clusters);
     if (rc != CE_OK) return rc;
     if (clusters < 1) return CE_ERR_PATH;
     if ((long long)clusters > B) clusters = (int)B;
     pl->path = CE_PATH_ROW_SPLIT;
     pl->split = K;
     pl->ctas = clusters * K;
-    pl->threads = threads;
+    pl->threads = ce::kSplitThreads;
+    pl->vecs = vecs;
     pl->smem = smem;
     pl->launches = 1;
     pl->nslots = nslots;
@@ -402,9 +407,8 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
                                      pl.slot_bytes, pl.smem, s);
             break;
         case CE_PATH_ROW_SPLIT:
-            e = ce::launch_split(p, dtype, pl.split, pl.threads, pl.ctas, pl.nslots, pl.slot_bytes,
-                                 pl.slice,
-                                 pl.smem, s);
+            e = ce::launch_split(p, dtype, pl.split, pl.vecs, pl.ctas, pl.nslots, pl.slot_bytes,
+                                 pl.slice, pl.smem, s);
             break;
         default:
             e = ce::launch_stream(p, dtype, pl.chunks, s);
@@ -516,7 +520,7 @@ int run_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C
         e = ce::launch_rows_warp(p, dtype, pl.per_sm, pl.ctas, pl.nslots, pl.rows_per_tile,
                                  pl.slot_bytes, pl.smem, s);
     else
-        e = ce::launch_split(p, dtype, pl.split, pl.threads, pl.ctas, pl.nslots, pl.slot_bytes,
+        e = ce::launch_split(p, dtype, pl.split, pl.vecs, pl.ctas, pl.nslots, pl.slot_bytes,
                              pl.slice, pl.smem, s);
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaGetLastError();

@@ -14,7 +14,7 @@ cudaError_t ensure_smem_attr(const void *func, int smem);
 
 // Threads per CTA of each path.
 constexpr int kSplitThreads = 512;
-constexpr int kSplitVecs = 8;  // 16-byte vectors per thread: slices of at most 64 KB
+constexpr int kSplitMaxVecs = 16;  // 16-byte vectors per thread: slices of at most 128 KB
 constexpr int kWarpKernelWarps = 16;
 constexpr int kStreamThreads = 256;
 constexpr int kStreamPerThread = 16;  // elements each thread keeps in registers
@@ -26,12 +26,12 @@ constexpr int kMaxWarpSlots = 4;  // per warp
 
 // Split-row path: one row (K = 1) or one slice of a row per CTA of a cluster
 // of K CTAs; `nslots` staged slices of `slot_bytes` each per CTA.
-// `threads` is 512 (one CTA per SM) or 256 (two CTAs per SM); a CTA holds a
-// slice of at most threads * kSplitVecs 16-byte vectors.
-cudaError_t launch_split(const Params &p, int dtype, int K, int threads, int ctas, int nslots,
+// K CTAs per row (1, 2, 3, 4, 6 or 8), each holding a slice of at most
+// kSplitThreads * vecs 16-byte vectors (vecs = 8 or 16) in registers.
+cudaError_t launch_split(const Params &p, int dtype, int K, int vecs, int ctas, int nslots,
                          int slot_bytes, long long slice_elems, int smem, cudaStream_t s);
 // Largest number of co-resident clusters of K CTAs with `smem` dynamic bytes.
-cudaError_t split_max_clusters(int dtype, int K, int threads, int smem, int *clusters);
+cudaError_t split_max_clusters(int dtype, int K, int vecs, int smem, int *clusters);
 
 // Warp-per-row path: tiles of `rows_per_tile` consecutive rows, `slots` tiles
 // staged per warp; `per_sm` (1 or 2) selects the build made for that many

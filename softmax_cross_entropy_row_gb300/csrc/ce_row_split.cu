@@ -8,10 +8,12 @@
 //
 // A slice is read from shared memory once, into registers (VPT 16-byte
 // vectors per thread); its slot is handed back to the copy engine right after
-// the first block reduction.  From the registers each CTA computes
+// the first block reduction.  fp32 exponentials then replace the logits in
+// those registers; bf16 rows keep their logits and evaluate each exponential
+// again for the gradient.  From the registers each CTA computes
 //
 //   Step 1  m_r = max over the slice                         (block max)
-//   Step 2  e = 2^(z*log2e - M_r), M_r = m_r*log2e, kept in registers;
+//   Step 2  e = 2^(z*log2e - M_r), M_r = m_r*log2e;
 //           S_r = sum of e over the slice, the target left out (block sum)
 //   combine M = max_r M_r,  S = sum_r S_r * 2^(M_r - M)      (over DSMEM, K > 1)
 //   Step 4  grad = e * 2^(M_r - M) / (S B), target: -S_rest / (S B)
@@ -30,7 +32,7 @@ namespace ce {
 namespace {
 
 template <typename T, int K, int NT, int VPT>
-__global__ void __launch_bounds__(NT, 512 / NT)
+__global__ void __launch_bounds__(NT, 1)
     row_split_kernel(Params p, int nslots, int slot_bytes, long long SE) {
     using E = Elem<T>;
     constexpr int NW = NT / 32;
@@ -38,6 +40,7 @@ __global__ void __launch_bounds__(NT, 512 / NT)
     constexpr int W2 = W / 2;  // fp32 pairs per vector
     constexpr int ES = E::kBytes;
     constexpr int kNoTarget = -0x40000000;
+    constexpr bool kKeepExp = sizeof(T) == 4;  // fp32: exponentials overwrite the logits in registers
 
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[kMaxSplitSlots];
@@ -221,22 +224,21 @@ __global__ void __launch_bounds__(NT, 512 / NT)
         // row).  The target's vector is left out whole; thread 0 adds its other
         // elements.
         const unsigned long long nM2 = f2_pack(-M_off, -M_off);
-        unsigned long long e2[VPT][W2];
         unsigned long long acc = 0ull;  // (0.f, 0.f)
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = tid + k * NT;
-            unsigned long long z2[W2];
-            E::unpack2(x[k], z2);
+            unsigned long long e2[W2];
+            E::unpack2(x[k], e2);
 #pragma unroll
             for (int i = 0; i < W2; ++i) {
                 float a, b;
-                f2_unpack(f2_fma(z2[i], kL2E2, nM2), a, b);
-                e2[k][i] = f2_pack(ex2(a), ex2(b));
+                f2_unpack(f2_fma(e2[i], kL2E2, nM2), a, b);
+                e2[i] = f2_pack(ex2(a), ex2(b));
             }
-            unsigned long long vs = W2 == 4 ? f2_add(f2_add(e2[k][0], e2[k][1]),
-                                                     f2_add(e2[k][W2 - 2], e2[k][W2 - 1]))
-                                            : f2_add(e2[k][0], e2[k][W2 - 1]);
+            if (kKeepExp) x[k] = E::pack2(e2);  // fp32: the exponentials replace the logits
+            unsigned long long vs = W2 == 4 ? f2_add(f2_add(e2[0], e2[1]), f2_add(e2[W2 - 2], e2[W2 - 1]))
+                                            : f2_add(e2[0], e2[W2 - 1]);
             if (v != v_t) acc = f2_add(acc, vs);
         }
         float sa, sb;
@@ -321,14 +323,28 @@ __global__ void __launch_bounds__(NT, 512 / NT)
         // (p_t - 1) / B = -S_rest / (S B): no cancellation when p_t is near 1
         const float g_t = -s_rest * scale;
         unsigned char *gbase = p.grad + (g0 - lbase);  // grad byte of vector 0
+        // The slice's exponentials as fp32 pairs: held in x for fp32 rows,
+        // evaluated again from the raw bf16 logits otherwise.
+        auto exps = [&](const uint4 &xv, unsigned long long (&e2)[W2]) {
+            E::unpack2(xv, e2);
+            if (!kKeepExp) {
+#pragma unroll
+                for (int i = 0; i < W2; ++i) {
+                    float a, b;
+                    f2_unpack(f2_fma(e2[i], kL2E2, nM2), a, b);
+                    e2[i] = f2_pack(ex2(a), ex2(b));
+                }
+            }
+        };
         if (!failed) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = tid + k * NT;
                 if (v >= vf0 && v < vf1) {
                     unsigned long long g2[W2];
+                    exps(x[k], g2);
 #pragma unroll
-                    for (int i = 0; i < W2; ++i) g2[i] = f2_mul(e2[k][i], esc2);
+                    for (int i = 0; i < W2; ++i) g2[i] = f2_mul(g2[i], esc2);
                     if (vec_store) {
                         *reinterpret_cast<uint4 *>(gbase + 16 * v) = E::pack2(g2);
                     } else {
@@ -351,10 +367,12 @@ __global__ void __launch_bounds__(NT, 512 / NT)
                     const int v = tid + k * NT;
                     if ((v == 0 && head_partial) || (v == nv - 1 && tail_partial)) {
                         const int l0 = v * W - head;
+                        unsigned long long e2[W2];
+                        exps(x[k], e2);
 #pragma unroll
                         for (int i = 0; i < W2; ++i) {
                             float a, b;
-                            f2_unpack(f2_mul(e2[k][i], esc2), a, b);
+                            f2_unpack(f2_mul(e2[i], esc2), a, b);
                             if ((unsigned)(l0 + 2 * i) < (unsigned)slice_n)
                                 E::store(gbase + 16 * v + (2 * i) * ES,
                                          v * W + 2 * i == tl ? g_t : a);
@@ -446,58 +464,62 @@ cudaError_t max_clusters_k(int smem, int *clusters) {
     return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
 }
 
-template <typename T, int NT>
-cudaError_t launch_n(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
+template <typename T, int V>
+cudaError_t launch_v(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
                      int smem, cudaStream_t s) {
-    constexpr int V = kSplitVecs;
+    constexpr int NT = kSplitThreads;
     switch (K) {
         case 1: return launch_k<T, 1, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
         case 2: return launch_k<T, 2, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
+        case 3: return launch_k<T, 3, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
         case 4: return launch_k<T, 4, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
+        case 6: return launch_k<T, 6, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
         case 8: return launch_k<T, 8, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <typename T, int NT>
-cudaError_t max_clusters_n(int K, int smem, int *clusters) {
-    constexpr int V = kSplitVecs;
+template <typename T, int V>
+cudaError_t max_clusters_v(int K, int smem, int *clusters) {
+    constexpr int NT = kSplitThreads;
     switch (K) {
         case 1: return max_clusters_k<T, 1, NT, V>(smem, clusters);
         case 2: return max_clusters_k<T, 2, NT, V>(smem, clusters);
+        case 3: return max_clusters_k<T, 3, NT, V>(smem, clusters);
         case 4: return max_clusters_k<T, 4, NT, V>(smem, clusters);
+        case 6: return max_clusters_k<T, 6, NT, V>(smem, clusters);
         case 8: return max_clusters_k<T, 8, NT, V>(smem, clusters);
         default: return cudaErrorInvalidValue;
     }
 }
 
 template <typename T>
-cudaError_t launch_t(const Params &p, int K, int threads, int ctas, int nslots, int slot_bytes,
+cudaError_t launch_t(const Params &p, int K, int vecs, int ctas, int nslots, int slot_bytes,
                      long long se, int smem, cudaStream_t s) {
-    if (threads == 256) return launch_n<T, 256>(p, K, ctas, nslots, slot_bytes, se, smem, s);
-    if (threads == 512) return launch_n<T, 512>(p, K, ctas, nslots, slot_bytes, se, smem, s);
+    if (vecs == 16) return launch_v<T, 16>(p, K, ctas, nslots, slot_bytes, se, smem, s);
+    if (vecs == 8) return launch_v<T, 8>(p, K, ctas, nslots, slot_bytes, se, smem, s);
     return cudaErrorInvalidValue;
 }
 
 template <typename T>
-cudaError_t max_clusters_t(int K, int threads, int smem, int *clusters) {
-    if (threads == 256) return max_clusters_n<T, 256>(K, smem, clusters);
-    if (threads == 512) return max_clusters_n<T, 512>(K, smem, clusters);
+cudaError_t max_clusters_t(int K, int vecs, int smem, int *clusters) {
+    if (vecs == 16) return max_clusters_v<T, 16>(K, smem, clusters);
+    if (vecs == 8) return max_clusters_v<T, 8>(K, smem, clusters);
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_split(const Params &p, int dtype, int K, int threads, int ctas, int nslots,
+cudaError_t launch_split(const Params &p, int dtype, int K, int vecs, int ctas, int nslots,
                          int slot_bytes, long long slice_elems, int smem, cudaStream_t s) {
     if (dtype == 0)
-        return launch_t<float>(p, K, threads, ctas, nslots, slot_bytes, slice_elems, smem, s);
-    return launch_t<__nv_bfloat16>(p, K, threads, ctas, nslots, slot_bytes, slice_elems, smem, s);
+        return launch_t<float>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem, s);
+    return launch_t<__nv_bfloat16>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem, s);
 }
 
-cudaError_t split_max_clusters(int dtype, int K, int threads, int smem, int *clusters) {
-    if (dtype == 0) return max_clusters_t<float>(K, threads, smem, clusters);
-    return max_clusters_t<__nv_bfloat16>(K, threads, smem, clusters);
+cudaError_t split_max_clusters(int dtype, int K, int vecs, int smem, int *clusters) {
+    if (dtype == 0) return max_clusters_t<float>(K, vecs, smem, clusters);
+    return max_clusters_t<__nv_bfloat16>(K, vecs, smem, clusters);
 }
 
 }  // namespace ce
