@@ -187,7 +187,8 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     // vectors per thread for a slice (its bytes plus the two partial vectors)
     auto vecs_of = [&](long long se) {
         const long long need = se * es + 32;
-        return need <= 8 * per_vec_cap ? 8 : need <= 16 * per_vec_cap ? 16 : 0;
+        return need <= 8 * per_vec_cap ? 8 : need <= 12 * per_vec_cap ? 12
+                                           : need <= 16 * per_vec_cap ? 16 : 0;
     };
     auto slot_of = [&](long long se) { return (long long)round_up(se * es + 32, 128); };
     auto nslots_of = [&](long long se) {
@@ -195,8 +196,8 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
         return (int)(n > ce::kMaxSplitSlots ? ce::kMaxSplitSlots : n);
     };
     // bf16 slices re-evaluate their exponentials for the gradient: with 16
-    // vectors per thread that build spills, so bf16 prefers 8 (64 KB slices).
-    const int auto_max_vecs = es == 2 ? 8 : 16;
+    // vectors per thread that build spills, so bf16 stops at 12 (96 KB slices).
+    const int auto_max_vecs = es == 2 ? 12 : 16;
     int K = K_forced;
     if (K == 0) {
         for (int k : {1, 2, 3, 4, 6, 8}) {

@@ -188,11 +188,20 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Warp-wide max in one instruction (NaN inputs are ignored, as fmaxf does);
+// every lane gets the same value.
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
+
+// Programmatic dependent launch: the next kernel on the stream may start its
+// prologue once every CTA of this one has called pdl_trigger(); pdl_wait()
+// returns once the previous grid has completed and its memory is visible, so
+// a kernel calls it before its first access to global memory.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 
 // Butterfly sum: every lane ends with the same bits.
 __device__ __forceinline__ float warp_sum(float v) {

@@ -27,7 +27,7 @@ constexpr int kMaxWarpSlots = 4;  // per warp
 // Split-row path: one row (K = 1) or one slice of a row per CTA of a cluster
 // of K CTAs; `nslots` staged slices of `slot_bytes` each per CTA.
 // K CTAs per row (1, 2, 3, 4, 6 or 8), each holding a slice of at most
-// kSplitThreads * vecs 16-byte vectors (vecs = 8 or 16) in registers.
+// kSplitThreads * vecs 16-byte vectors (vecs = 8, 12 or 16) in registers.
 cudaError_t launch_split(const Params &p, int dtype, int K, int vecs, int ctas, int nslots,
                          int slot_bytes, long long slice_elems, int smem, cudaStream_t s);
 // Largest number of co-resident clusters of K CTAs with `smem` dynamic bytes.

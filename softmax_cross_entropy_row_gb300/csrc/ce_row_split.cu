@@ -97,6 +97,8 @@ __global__ void __launch_bounds__(NT, 1)
         fence_mbar_init();
         warps_summed[0] = warps_summed[1] = 0u;
     }
+    pdl_trigger();
+    pdl_wait();  // nothing above touched global memory
     __syncthreads();
     long long issued = 0;
     if (tid == 0) {
@@ -423,14 +425,17 @@ cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long
     cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (K > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = K;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = K;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, kern, p, nslots, slot_bytes, se);
 }
@@ -497,6 +502,7 @@ template <typename T>
 cudaError_t launch_t(const Params &p, int K, int vecs, int ctas, int nslots, int slot_bytes,
                      long long se, int smem, cudaStream_t s) {
     if (vecs == 16) return launch_v<T, 16>(p, K, ctas, nslots, slot_bytes, se, smem, s);
+    if (vecs == 12) return launch_v<T, 12>(p, K, ctas, nslots, slot_bytes, se, smem, s);
     if (vecs == 8) return launch_v<T, 8>(p, K, ctas, nslots, slot_bytes, se, smem, s);
     return cudaErrorInvalidValue;
 }
@@ -504,6 +510,7 @@ cudaError_t launch_t(const Params &p, int K, int vecs, int ctas, int nslots, int
 template <typename T>
 cudaError_t max_clusters_t(int K, int vecs, int smem, int *clusters) {
     if (vecs == 16) return max_clusters_v<T, 16>(K, smem, clusters);
+    if (vecs == 12) return max_clusters_v<T, 12>(K, smem, clusters);
     if (vecs == 8) return max_clusters_v<T, 8>(K, smem, clusters);
     return cudaErrorInvalidValue;
 }

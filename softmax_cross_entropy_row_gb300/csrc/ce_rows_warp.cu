@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
         for (int s = 0; s < slots; ++s) mbar_init(&my_full[s], 1);
         fence_mbar_init();
     }
+    pdl_trigger();
+    pdl_wait();  // nothing above touched global memory
     __syncwarp();
     long long issued = 0;
     if (lane == 0) {
@@ -289,6 +291,11 @@ cudaError_t launch_v(const Params &p, int ctas, int slots, int rows_per_tile, in
     cfg.blockDim = dim3(kWarpKernelWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p, slots, rows_per_tile, slot_bytes);
 }
 
