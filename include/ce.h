@@ -90,7 +90,7 @@ int ce_fwd_bwd(const void *logits, const int32_t *targets, int64_t B, int64_t C,
 /*
  * ce_fwd_bwd_path -- ce_fwd_bwd with the kernel path forced (tests, tuning).
  *   path   a ce_path; CE_PATH_AUTO behaves exactly as ce_fwd_bwd.
- *   split  CE_PATH_ROW_SPLIT: CTAs per row (1, 2, 4 or 8; 0 = choose);
+ *   split  CE_PATH_ROW_SPLIT: CTAs per row (1, 2, 3, 4, 6 or 8; 0 = choose);
  *          CE_PATH_STREAM: classes per chunk (multiple of 8; 0 = choose);
  *          ignored otherwise.
  * Returns CE_ERR_PATH when the forced path cannot hold the row in shared

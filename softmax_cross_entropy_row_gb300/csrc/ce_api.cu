@@ -195,9 +195,10 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
         long long n = budget / slot_of(se);
         return (int)(n > ce::kMaxSplitSlots ? ce::kMaxSplitSlots : n);
     };
-    // bf16 slices re-evaluate their exponentials for the gradient: with 16
-    // vectors per thread that build spills, so bf16 stops at 12 (96 KB slices).
-    const int auto_max_vecs = es == 2 ? 12 : 16;
+    // bf16 slices re-evaluate their exponentials for the gradient, so their
+    // per-thread work grows twice as fast with the slice: on 128k-class bf16
+    // rows, 4 CTAs of 64 KB ran faster than 3 of 96 KB, so bf16 stops at 8.
+    const int auto_max_vecs = es == 2 ? 8 : 16;
     int K = K_forced;
     if (K == 0) {
         for (int k : {1, 2, 3, 4, 6, 8}) {

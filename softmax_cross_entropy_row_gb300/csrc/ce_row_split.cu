@@ -1,6 +1,6 @@
 // Split-row kernel: each row of the logits crosses HBM exactly once.
 //
-// A cluster of K CTAs (K = 1, 2, 4 or 8) owns a row at a time; CTA `rank`
+// A cluster of K CTAs (K = 1, 2, 3, 4, 6 or 8) owns a row at a time; CTA `rank`
 // holds the slice [rank*SE, (rank+1)*SE) of the row's classes.  Each CTA keeps
 // a ring of `nslots` shared-memory slots filled by TMA bulk copies, so the
 // copies of the next rows are in flight while it computes the current one (a
