@@ -101,7 +101,8 @@ struct Plan {
     long long slice = 0;  // classes per slice (split path)
     int rows_per_tile = 0;
     int per_sm = 1;       // warp path: the build for 1 or 2 resident CTAs per SM
-    int vecs = 8;         // split path: 16-byte vectors per thread (8 or 16)
+    int vecs = 8;         // split path: 16-byte vectors per thread (8, 12 or 16)
+    bool pipe = false;    // split path, K > 1: the pipelined kernel
     long long chunks = 0; // stream path
 };
 
@@ -119,6 +120,16 @@ int warp_per_sm_override() {
         return e ? atoi(e) : 0;
     }();
     return n;
+}
+
+// Tuning knob: CE_SPLIT_PIPE=0 keeps split rows of K > 1 on the
+// barrier-per-row kernel even where the pipelined one applies.  Read once.
+bool split_pipe_enabled() {
+    static const bool on = [] {
+        const char *e = getenv("CE_SPLIT_PIPE");
+        return !(e && atoi(e) == 0);
+    }();
+    return on;
 }
 
 int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, Plan *pl) {
@@ -218,10 +229,16 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     if (vecs == 0 || nslots < 1) return CE_ERR_PATH;
     const long long slot_bytes = slot_of(se);
     const int smem = nslots * (int)slot_bytes;
+    // K > 1 with slices of at most 8 vectors per thread: the pipelined kernel
+    const bool pipe = K > 1 && vecs <= ce::kPipeVecs && split_pipe_enabled();
     int clusters = 0;
     int rc = cached_occupancy(
-        dtype, CE_PATH_ROW_SPLIT, K * 64 + vecs, smem,
-        [&](int *v) { return ce::split_max_clusters(dtype, K, vecs, smem, v); }, &clusters);
+        dtype, CE_PATH_ROW_SPLIT, K * 64 + vecs + (pipe ? 32 : 0), smem,
+        [&](int *v) {
+            return pipe ? ce::split_pipe_max_clusters(dtype, K, smem, v)
+                        : ce::split_max_clusters(dtype, K, vecs, smem, v);
+        },
+        &clusters);
     if (rc != CE_OK) return rc;
     if (clusters < 1) return CE_ERR_PATH;
     if ((long long)clusters > B) clusters = (int)B;
@@ -230,6 +247,7 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     pl->ctas = clusters * K;
     pl->threads = ce::kSplitThreads;
     pl->vecs = vecs;
+    pl->pipe = pipe;
     pl->smem = smem;
     pl->launches = 1;
     pl->nslots = nslots;
@@ -249,6 +267,14 @@ int plan_stream(long long B, long long C, Plan *pl) {
     pl->launches = 2;
     pl->chunks = chunks;
     return CE_OK;
+}
+
+cudaError_t launch_split_plan(const ce::Params &p, int dtype, const Plan &pl, cudaStream_t s) {
+    if (pl.pipe)
+        return ce::launch_split_pipe(p, dtype, pl.split, pl.ctas, pl.nslots, pl.slot_bytes,
+                                     pl.slice, pl.smem, s);
+    return ce::launch_split(p, dtype, pl.split, pl.vecs, pl.ctas, pl.nslots, pl.slot_bytes,
+                            pl.slice, pl.smem, s);
 }
 
 int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl) {
@@ -409,8 +435,7 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
                                      pl.slot_bytes, pl.smem, s);
             break;
         case CE_PATH_ROW_SPLIT:
-            e = ce::launch_split(p, dtype, pl.split, pl.vecs, pl.ctas, pl.nslots, pl.slot_bytes,
-                                 pl.slice, pl.smem, s);
+            e = launch_split_plan(p, dtype, pl, s);
             break;
         default:
             e = ce::launch_stream(p, dtype, pl.chunks, s);
@@ -522,8 +547,7 @@ int run_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C
         e = ce::launch_rows_warp(p, dtype, pl.per_sm, pl.ctas, pl.nslots, pl.rows_per_tile,
                                  pl.slot_bytes, pl.smem, s);
     else
-        e = ce::launch_split(p, dtype, pl.split, pl.vecs, pl.ctas, pl.nslots, pl.slot_bytes,
-                             pl.slice, pl.smem, s);
+        e = launch_split_plan(p, dtype, pl, s);
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);

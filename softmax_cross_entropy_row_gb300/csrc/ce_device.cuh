@@ -337,6 +337,49 @@ __device__ __forceinline__ float ld_dsmem_f32(const void *local, uint32_t rank) 
     return v;
 }
 
+// Shared::cluster address of `local`'s counterpart in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(const void *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)),
+                 "r"(rank));
+    return remote;
+}
+
+// Store 16 bytes into the shared memory of a CTA of the cluster (`dst`, a
+// shared::cluster address) and complete 16 bytes of the transaction count of
+// that CTA's mbarrier `bar` (also a shared::cluster address).  The completion
+// releases the data at cluster scope; nothing waits for it here.
+__device__ __forceinline__ void st_async_f4(uint32_t dst, float4 v, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(dst),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+        : "memory");
+}
+
+// try_wait with acquire at cluster scope: for phases completed by other CTAs'
+// st.async transactions.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (clock64() - t0 > kWaitLimitCycles) return false;
+    }
+    return true;
+}
+
 // ---------------------------------------------------------- batch-loss tail
 
 // Error-free sum of two floats (Knuth's TwoSum): a + b = s + e exactly.

@@ -33,6 +33,14 @@ cudaError_t launch_split(const Params &p, int dtype, int K, int vecs, int ctas, 
 // Largest number of co-resident clusters of K CTAs with `smem` dynamic bytes.
 cudaError_t split_max_clusters(int dtype, int K, int vecs, int smem, int *clusters);
 
+// The pipelined variant of the split-row path for K > 1 (ce_row_pipe.cu):
+// slices of at most kSplitThreads * kPipeVecs vectors, the cluster exchange of
+// one row overlapped with the next row's work.
+constexpr int kPipeVecs = 8;
+cudaError_t launch_split_pipe(const Params &p, int dtype, int K, int ctas, int nslots,
+                              int slot_bytes, long long slice_elems, int smem, cudaStream_t s);
+cudaError_t split_pipe_max_clusters(int dtype, int K, int smem, int *clusters);
+
 // Warp-per-row path: tiles of `rows_per_tile` consecutive rows, `slots` tiles
 // staged per warp; `per_sm` (1 or 2) selects the build made for that many
 // resident CTAs per SM.

@@ -101,8 +101,10 @@ def test_stream_path_shapes(B, C, dtype):
 
 def test_many_rows_per_cluster():
     """More rows than clusters: the shared-memory rings wrap several times."""
-    for dtype, C, K in [("f32", 3000, 1), ("bf16", 9000, 2), ("f32", 20000, 2), ("f32", 50257, 3)]:
-        inp = _case(1500, C, dtype, seed=C + K, sigma=2.0)
+    for B, dtype, C, K in [(1500, "f32", 3000, 1), (1500, "bf16", 9000, 2), (1500, "f32", 20000, 2),
+                           (1500, "f32", 50257, 3), (600, "f32", 50257, 4), (100, "f32", 20000, 4),
+                           (77, "bf16", 9000, 8), (300, "bf16", 128256, 4)]:
+        inp = _case(B, C, dtype, seed=C + K, sigma=2.0)
         z, t = device_inputs(inp)
         loss, grad = run(z, t, SPLIT, K)
         torch.cuda.synchronize()
