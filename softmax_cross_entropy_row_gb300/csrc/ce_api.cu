@@ -102,7 +102,7 @@ struct Plan {
     int rows_per_tile = 0;
     int per_sm = 1;       // warp path: the build for 1 or 2 resident CTAs per SM
     int vecs = 8;         // split path: 16-byte vectors per thread (8, 12 or 16)
-    bool pipe = false;    // split path, K > 1: the pipelined kernel
+    bool pipe = false;    // split path: the pipelined kernel (slices of at most 8 vectors)
     long long chunks = 0; // stream path
 };
 
@@ -122,8 +122,8 @@ int warp_per_sm_override() {
     return n;
 }
 
-// Tuning knob: CE_SPLIT_PIPE=0 keeps split rows of K > 1 on the
-// barrier-per-row kernel even where the pipelined one applies.  Read once.
+// Tuning knob: CE_SPLIT_PIPE=0 keeps split rows on the barrier-per-row
+// kernel even where the pipelined one applies.  Read once.
 bool split_pipe_enabled() {
     static const bool on = [] {
         const char *e = getenv("CE_SPLIT_PIPE");
@@ -186,7 +186,9 @@ int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, 
 // Split-row path: K CTAs per row (a cluster when K > 1), each holding a
 // slice of SE classes in registers (at most kSplitThreads x 16 vectors, i.e.
 // 128 KB) with a ring of at least two shared-memory slots.  The smallest such
-// K is chosen: fewer CTAs per row means fewer cluster barriers per byte.
+// K is chosen: fewer CTAs per row means fewer exchanges per byte.  For K > 1,
+// slices of at most 8 vectors per thread run on the pipelined kernel (no
+// CTA-wide barrier per row); the rest on the barrier-per-row kernel.
 int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype, int K_forced,
                Plan *pl) {
     const int budget = d.smem_optin - kStaticSmemReserve;
@@ -230,6 +232,7 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     const long long slot_bytes = slot_of(se);
     const int smem = nslots * (int)slot_bytes;
     // K > 1 with slices of at most 8 vectors per thread: the pipelined kernel
+    // (for K = 1 the barrier-per-row kernel measured faster)
     const bool pipe = K > 1 && vecs <= ce::kPipeVecs && split_pipe_enabled();
     int clusters = 0;
     int rc = cached_occupancy(

@@ -251,14 +251,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for phase `parity` of an mbarrier, for at most kWaitLimitCycles.
+// Polls between two reads of the clock in the bounded waits: a poll is one
+// try_wait and a branch, so a waiting warp takes few issue slots from the
+// warps that compute.
+constexpr int kPollsPerClockRead = 8;
+
+// Wait for phase `parity` of an mbarrier, for at most kWaitLimitCycles (plus
+// at most kPollsPerClockRead suspended polls).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    for (;;) {
+#pragma unroll
+        for (int i = 0; i < kPollsPerClockRead; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (clock64() - t0 > kWaitLimitCycles) return false;
     }
-    return true;
 }
 
 // One TMA bulk copy global -> this CTA's shared memory, completing on `bar`.
@@ -374,10 +382,12 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait_cluster(bar, parity)) {
+    for (;;) {
+#pragma unroll
+        for (int i = 0; i < kPollsPerClockRead; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
         if (clock64() - t0 > kWaitLimitCycles) return false;
     }
-    return true;
 }
 
 // ---------------------------------------------------------- batch-loss tail

@@ -33,9 +33,9 @@ cudaError_t launch_split(const Params &p, int dtype, int K, int vecs, int ctas, 
 // Largest number of co-resident clusters of K CTAs with `smem` dynamic bytes.
 cudaError_t split_max_clusters(int dtype, int K, int vecs, int smem, int *clusters);
 
-// The pipelined variant of the split-row path for K > 1 (ce_row_pipe.cu):
-// slices of at most kSplitThreads * kPipeVecs vectors, the cluster exchange of
-// one row overlapped with the next row's work.
+// The pipelined split-row kernel (ce_row_pipe.cu): K = 1..8 CTAs per row,
+// slices of at most kSplitThreads * kPipeVecs vectors, no CTA-wide barrier per
+// row; the partials of one row are exchanged while the next row is reduced.
 constexpr int kPipeVecs = 8;
 cudaError_t launch_split_pipe(const Params &p, int dtype, int K, int ctas, int nslots,
                               int slot_bytes, long long slice_elems, int smem, cudaStream_t s);
