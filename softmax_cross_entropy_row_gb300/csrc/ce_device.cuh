@@ -457,16 +457,22 @@ __device__ __forceinline__ float2 tail_virtual_warp(const Params &p, int vw, int
 }
 
 // Adds the 8 virtual-warp totals in order, writes L and re-arms the ticket.
+// (h + l) / B is formed in fp32 with one correction step (no fp64: its
+// division is a long dependent sequence on this part):
+//   q0 = h * fp32(1/B),  r = (h - q0 B) + l  (the fma is exact up to one
+//   rounding),  L = q0 + r * fp32(1/B).
 __device__ __forceinline__ void tail_write(const Params &p, const float2 *vw_totals) {
     float h = 0.f, l = 0.f;
+#pragma unroll
     for (int w = 0; w < kTailWarps; ++w) {
         float s, e;
         two_sum(h, vw_totals[w].x, s, e);
         h = s;
         l += vw_totals[w].y + e;
     }
-    const double total = static_cast<double>(h) + static_cast<double>(l);
-    *p.loss_out = static_cast<float>(total / static_cast<double>(p.B));
+    const float q0 = h * p.inv_b;
+    const float r = fmaf(-q0, static_cast<float>(p.B), h) + l;
+    *p.loss_out = fmaf(r, p.inv_b, q0);
     *p.ticket = 0u;  // ready for the next launch on this workspace
 }
 
@@ -476,14 +482,20 @@ __device__ __forceinline__ void tail_write(const Params &p, const float2 *vw_tot
 __device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *scratch) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
+        // acquire-release at GPU scope: publishes this CTA's row losses (the
+        // barrier above orders the other threads' stores before it) and, in
+        // the last CTA, makes every other CTA's visible to the loads below
+        // (the barrier after it extends that to the other threads)
         const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
-        const unsigned int prev = atomicAdd(p.ticket, 1u);
+        unsigned int prev;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(p.ticket)
+                     : "memory");
         *flag = (prev == total - 1u);
     }
     __syncthreads();
     if (*flag) {
-        __threadfence();
         const int warp = threadIdx.x >> 5;
         const int lane = threadIdx.x & 31;
         for (int vw = warp; vw < kTailWarps; vw += blockDim.x >> 5) {

@@ -33,7 +33,7 @@ cudaError_t launch_split(const Params &p, int dtype, int K, int vecs, int ctas, 
 // Largest number of co-resident clusters of K CTAs with `smem` dynamic bytes.
 cudaError_t split_max_clusters(int dtype, int K, int vecs, int smem, int *clusters);
 
-// The pipelined split-row kernel (ce_row_pipe.cu): K = 1..8 CTAs per row,
+// The pipelined split-row kernel (ce_row_pipe.cu): K = 2..8 CTAs per row,
 // slices of at most kSplitThreads * kPipeVecs vectors, no CTA-wide barrier per
 // row; the partials of one row are exchanged while the next row is reduced.
 constexpr int kPipeVecs = 8;

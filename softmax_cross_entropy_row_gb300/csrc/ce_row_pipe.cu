@@ -1,4 +1,4 @@
-// Pipelined split-row kernel: rows of K slices (K = 1, 2, 3, 4, 6 or 8), one
+// Pipelined split-row kernel: rows of K slices (K = 2, 3, 4, 6 or 8), one
 // slice per CTA of a cluster of K, each slice of at most kSplitThreads x 8
 // 16-byte vectors (64 KB), with no CTA-wide barrier per row.
 //
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(NT, 1)
     constexpr int kLossWarp = NW / 2;  // its lane 0 (in rank 0) writes the row losses
     constexpr int kNoTarget = -0x40000000;
     constexpr bool kKeepExp = sizeof(T) == 4;  // fp32: exponentials overwrite the logits
-    static_assert(K >= 1 && K <= 32 && NW >= 2, "shape");
+    static_assert(K >= 2 && K <= 32 && NW >= 2, "shape");
 
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[kMaxSplitSlots];
@@ -497,7 +497,7 @@ cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;  // K = 1: clusters of one CTA
+    attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = K;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
@@ -529,7 +529,6 @@ template <typename T>
 cudaError_t launch_t(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
                      int smem, cudaStream_t s) {
     switch (K) {
-        case 1: return launch_k<T, 1>(p, ctas, nslots, slot_bytes, se, smem, s);
         case 2: return launch_k<T, 2>(p, ctas, nslots, slot_bytes, se, smem, s);
         case 3: return launch_k<T, 3>(p, ctas, nslots, slot_bytes, se, smem, s);
         case 4: return launch_k<T, 4>(p, ctas, nslots, slot_bytes, se, smem, s);
@@ -542,7 +541,6 @@ cudaError_t launch_t(const Params &p, int K, int ctas, int nslots, int slot_byte
 template <typename T>
 cudaError_t max_clusters_t(int K, int smem, int *clusters) {
     switch (K) {
-        case 1: return max_clusters_k<T, 1>(smem, clusters);
         case 2: return max_clusters_k<T, 2>(smem, clusters);
         case 3: return max_clusters_k<T, 3>(smem, clusters);
         case 4: return max_clusters_k<T, 4>(smem, clusters);
