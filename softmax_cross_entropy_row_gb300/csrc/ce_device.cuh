@@ -190,6 +190,31 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Warp-wide max in one instruction (NaN inputs are ignored, as fmaxf does);
 // every lane gets the same value.
+// 1/x by the hardware approximation (rcp.approx.ftz, within 1 ulp); used for
+// 1/S, where S >= 1 (the row maximum's own term is 1).
+__device__ __forceinline__ float fast_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2(x) by the hardware approximation (lg2.approx.ftz).
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The row loss l = log(S / e_t) (Step 3), from S_rest = S - e_t, e_t > 0, S
+// and the target logit z_t, with e_t = 2^(z_t*log2e - M):
+//   log1p(S_rest / e_t)          when the target dominates (S_rest < e_t, so
+//                                l < ln 2 and only this form keeps l's
+//                                relative precision);
+//   ln2 * (log2(S) - (z_t*log2e - M))   otherwise (l >= ln 2).
+__device__ __forceinline__ float row_loss(float s_rest, float e_t, float S, float zt, float M) {
+    return s_rest < e_t ? log1pf(s_rest / e_t) : kLn2 * (fast_log2(S) - fmaf(zt, kLog2e, -M));
+}
+
 __device__ __forceinline__ float warp_max(float v) {
     float r;
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));

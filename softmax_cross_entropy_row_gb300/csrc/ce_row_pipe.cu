@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(NT, 1)
         S = s_rest + e_t;
 
         // Step 4: gradient of the slice
-        const float scale = (1.0f / S) * p.inv_b;
+        const float scale = fast_rcp(S) * p.inv_b;
         // a thread without elements has nothing to scale (and M_t = 0 is not
         // an upper bound of anything)
         const float escale = hv ? scale * ex2(off - M) : 0.f;
@@ -436,10 +436,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (rank == 0 && warp == kLossWarp && lane == 0 && !skip) {
             float l;
             if (has_t) {
-                // l = log(S / e_t) = log1p(S_rest / e_t): the second form keeps
-                // its precision when the target dominates (then e_t > S / 2).
-                l = s_rest < e_t ? log1pf(s_rest / e_t)
-                                 : kLn2 * (log2f(S) - fmaf(zt, kLog2e, -M));
+                l = row_loss(s_rest, e_t, S, zt, M);
             } else {
                 l = NAN;
                 atomicAdd(&p.err[kErrBadTarget], 1);

@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(NT, 1)
         S = s_rest + e_t;
 
         // ---- Step 4: gradient of the slice
-        const float scale = (1.0f / S) * p.inv_b;
+        const float scale = fast_rcp(S) * p.inv_b;
         const float escale = K > 1 ? scale * ex2(M_off - M) : scale;
         const unsigned long long esc2 = f2_pack(escale, escale);
         // (p_t - 1) / B = -S_rest / (S B): no cancellation when p_t is near 1
@@ -391,10 +391,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (rank == 0 && tid == 0 && !failed) {
             float l;
             if (has_t) {
-                // l = log(S / e_t) = log1p(S_rest / e_t): the second form keeps
-                // its precision when the target dominates (then e_t > S / 2).
-                l = s_rest < e_t ? log1pf(s_rest / e_t)
-                                 : kLn2 * (log2f(S) - fmaf(zt, kLog2e, -M));
+                l = row_loss(s_rest, e_t, S, zt, M);
             } else {
                 l = NAN;
                 atomicAdd(&p.err[kErrBadTarget], 1);

@@ -157,8 +157,14 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
                 x[k] = kNeg;
                 if (v < nvec) x[k] = lds128(vrow + 16 * v);
             }
-            const float hz = lane < nh ? E::load(row + lane * ES) : -INFINITY;
-            const float tz = lane < nt ? E::load(vrow + (nvec * W + lane) * ES) : -INFINITY;
+            // head and tail elements exist only for rows that do not start and
+            // end on a 16-byte boundary (the same in every lane)
+            const bool ragged = (nh | nt) != 0;
+            float hz = -INFINITY, tz = -INFINITY;
+            if (ragged) {
+                if (lane < nh) hz = E::load(row + lane * ES);
+                if (lane < nt) tz = E::load(vrow + (nvec * W + lane) * ES);
+            }
             const float zt = has_t ? E::load(row + t * ES) : 0.f;
             // lane 0 also takes the target's vector
             const uint4 xt = lane == 0 && v_t >= 0 ? lds128(vrow + 16 * v_t) : kNeg;
@@ -201,16 +207,19 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
                 for (int j = 0; j < W; ++j)
                     if (j != d) sa += ex2(fmaf(z[j], kLog2e, -M));
             }
-            const float eh = lane < nh ? ex2(fmaf(hz, kLog2e, -M)) : 0.f;
-            const float et = lane < nt ? ex2(fmaf(tz, kLog2e, -M)) : 0.f;
-            if (lane != t) sa += eh;
-            if (nh + nvec * W + lane != t) sb += et;
+            float eh = 0.f, et = 0.f;
+            if (ragged) {
+                if (lane < nh) eh = ex2(fmaf(hz, kLog2e, -M));
+                if (lane < nt) et = ex2(fmaf(tz, kLog2e, -M));
+                if (lane != t) sa += eh;
+                if (nh + nvec * W + lane != t) sb += et;
+            }
             const float s_rest = warp_sum(sa + sb);
             const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
             const float S = s_rest + e_t;
 
             // Step 4: gradient; (p_t - 1) / B = -S_rest / (S B)
-            const float scale = (1.0f / S) * inv_b;
+            const float scale = fast_rcp(S) * inv_b;
             const unsigned long long sc2 = f2_pack(scale, scale);
             const float g_t = -s_rest * scale;
             unsigned char *grow = p.grad + (size_t)r * C * ES;
@@ -245,18 +254,19 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
                     if (v == v_t) E::store(grow + (size_t)t * ES, g_t);
                 }
             }
-            if (lane < nh) E::store(grow + lane * ES, lane == t ? g_t : eh * scale);
-            if (lane < nt) {
-                const int c = nh + nvec * W + lane;
-                E::store(grow + c * ES, c == t ? g_t : et * scale);
+            if (ragged) {
+                if (lane < nh) E::store(grow + lane * ES, lane == t ? g_t : eh * scale);
+                if (lane < nt) {
+                    const int c = nh + nvec * W + lane;
+                    E::store(grow + c * ES, c == t ? g_t : et * scale);
+                }
             }
 
             // Step 3: loss of the row, log(S / e_t)
             if (lane == 0) {
                 float l;
                 if (has_t) {
-                    l = s_rest < e_t ? log1pf(s_rest / e_t)
-                                     : kLn2 * (log2f(S) - fmaf(zt, kLog2e, -M));
+                    l = row_loss(s_rest, e_t, S, zt, M);
                 } else {
                     l = NAN;
                     atomicAdd(&p.err[kErrBadTarget], 1);

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(NT) stream_grad_kernel(Params p, long long chu
     const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
     const float S = s_rest + e_t;
     const float inv_b = p.inv_b;
-    const float scale = (1.0f / S) * inv_b;
+    const float scale = fast_rcp(S) * inv_b;
     const float g_t = -s_rest * scale;  // (p_t - 1) / B without cancellation
     const unsigned char *row = p.logits + (size_t)(b * C) * E::kBytes;
     unsigned char *grow = p.grad + (size_t)(b * C) * E::kBytes;
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(NT) stream_grad_kernel(Params p, long long chu
     if (k == 0 && threadIdx.x == 0) {
         float l;
         if (has_t) {
-            l = s_rest < e_t ? log1pf(s_rest / e_t) : kLn2 * (log2f(S) - fmaf(zt, kLog2e, -M));
+            l = row_loss(s_rest, e_t, S, zt, M);
         } else {
             l = NAN;
             atomicAdd(&p.err[kErrBadTarget], 1);
