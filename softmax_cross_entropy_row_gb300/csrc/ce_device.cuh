@@ -111,11 +111,14 @@ struct Elem<float> {
     __device__ __forceinline__ static void store(unsigned char *p, float v) {
         *reinterpret_cast<float *>(p) = v;
     }
-    // Max over one 16-byte vector (exact).
-    __device__ __forceinline__ static float vmax(const uint4 &w) {
-        return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
-                     fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+    // Running max over 16-byte vectors (exact): accumulator, step, value.
+    using MaxAcc = float;
+    __device__ __forceinline__ static MaxAcc max_init() { return -INFINITY; }
+    __device__ __forceinline__ static void max_step(MaxAcc &m, const uint4 &w) {
+        m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                           fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
     }
+    __device__ __forceinline__ static float max_value(MaxAcc m) { return m; }
 };
 
 template <>
@@ -168,15 +171,20 @@ struct Elem<__nv_bfloat16> {
     __device__ __forceinline__ static void store(unsigned char *p, float v) {
         *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
     }
-    // Max over one 16-byte vector, taken on the packed bf16 pairs (exact: the
-    // widening to fp32 is monotonic).
-    __device__ __forceinline__ static float vmax(const uint4 &w) {
-        __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&w.x);
-        __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w.y);
-        __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162 *>(&w.z);
-        __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162 *>(&w.w);
-        __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
-        return fmaxf(__low2float(m), __high2float(m));
+    // Running max over 16-byte vectors, kept as a packed bf16 pair (exact:
+    // the widening to fp32 is monotonic); one max.bf16x2 per 4 elements.
+    using MaxAcc = uint32_t;
+    __device__ __forceinline__ static uint32_t max2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ __forceinline__ static MaxAcc max_init() { return kNegInfWord; }
+    __device__ __forceinline__ static void max_step(MaxAcc &m, const uint4 &w) {
+        m = max2(m, max2(max2(w.x, w.y), max2(w.z, w.w)));
+    }
+    __device__ __forceinline__ static float max_value(MaxAcc m) {
+        return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
     }
 };
 

@@ -120,13 +120,15 @@ __global__ void __launch_bounds__(NT, 1)
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const uint32_t rank = cluster_rank();
-    const long long cid = (long long)cluster_id_x();
-    const long long ncl = (long long)cluster_count_x();
+    // rows, classes and targets fit in int (B, C < 2^31); only element
+    // offsets (row * C) need 64 bits
+    const int cid = (int)cluster_id_x();
+    const int ncl = (int)cluster_count_x();
     const long long C = p.C;
-    const long long c0 = min((long long)rank * SE, C);
-    const long long c1 = min(c0 + SE, C);
-    const int slice_n = (int)(c1 - c0);
-    const long long nrows = cid < p.B ? (p.B - cid + ncl - 1) / ncl : 0;
+    const int c0 = (int)min((long long)rank * SE, C);
+    const int c1 = (int)min((long long)c0 + SE, C);
+    const int slice_n = c1 - c0;
+    const int nrows = cid < p.B ? (int)((p.B - cid + ncl - 1) / ncl) : 0;
     const uint64_t lbase = reinterpret_cast<uint64_t>(p.logits);
     const bool vec_store = p.grad_vec_ok != 0;
     const unsigned long long kL2E2 = f2_pack(kLog2e, kLog2e);
@@ -142,9 +144,9 @@ __global__ void __launch_bounds__(NT, 1)
         int head, nv, vf0, vf1;
         bool head_partial, tail_partial;
     };
-    auto geom = [&](long long row) {
+    auto geom = [&](int row) {
         Geom g;
-        g.e0 = row * C + c0;
+        g.e0 = (long long)row * C + c0;
         const uint32_t b0 = ((uint32_t)lbase + (uint32_t)g.e0 * ES) & 15u;  // gs mod 16
         g.head = (int)(b0 / ES);
         const uint32_t end = b0 + (uint32_t)slice_n * ES;  // ge - g0
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(NT, 1)
         g.tail_partial = g.vf1 == g.nv - 1 && g.nv - 1 >= g.vf0;
         return g;
     };
-    auto issue = [&](long long j, int s) {  // row j of this cluster into slot s
+    auto issue = [&](int j, int s) {  // row j of this cluster into slot s
         const Geom g = geom(cid + j * ncl);
         const uint64_t g0 = lbase + (uint64_t)g.e0 * ES - (uint64_t)g.head * ES;
         const uint64_t lo = g0 > p.lo_clip ? g0 : p.lo_clip;
@@ -183,17 +185,17 @@ __global__ void __launch_bounds__(NT, 1)
     cluster_sync();
 
     const bool issuer = warp == kPub && lane == 0;
-    long long issued = 0;  // issuer: rows whose copy was issued
+    int issued = 0;        // issuer: rows whose copy was issued
     int s_issue = 0;       // issuer: slot of the next copy
     if (issuer) {
         for (int b = 0; b < NB && b < nrows; ++b)
             mbar_arrive_expect_tx(&xbar[b], (uint32_t)(K * sizeof(float4)));
         for (; issued < nrows && issued < nslots; ++issued) issue(issued, (int)issued);
-        s_issue = (int)(issued % nslots);
+        s_issue = issued % nslots;
     }
 
     bool failed = false;   // this thread saw a wait give up
-    long long consumed = 0;
+    int consumed = 0;
     int s_cur = 0;         // slot and phase parity of the next row to consume
     uint32_t ph_cur = 0;
     int t_next = nrows > 0 ? __ldg(p.targets + cid) : 0;
@@ -205,15 +207,15 @@ __global__ void __launch_bounds__(NT, 1)
     };
 
     // ---------------------------------------------------------------- A(j)
-    auto stage_a = [&](long long j, uint4 (&x)[VPT], float &off, bool &hv, long long &t_out) {
-        const long long row = cid + j * ncl;
-        const int par = (int)(j & 1);
-        const long long t = t_next;
+    auto stage_a = [&](int j, uint4 (&x)[VPT], float &off, bool &hv, int &t_out) {
+        const int row = cid + j * ncl;
+        const int par = j & 1;
+        const int t = t_next;
         t_out = t;
         if (j + 1 < nrows) t_next = __ldg(p.targets + row + ncl);
         const Geom g = geom(row);
         const bool has_t = t >= c0 && t < c1;
-        const int tl = has_t ? (int)(t - c0) + g.head : kNoTarget;  // target, vector-0 based
+        const int tl = has_t ? t - c0 + g.head : kNoTarget;  // target, vector-0 based
         const int v_t = has_t ? tl / W : -1;
         unsigned char *slot = smem + (size_t)s_cur * slot_bytes;
 
@@ -260,9 +262,10 @@ __global__ void __launch_bounds__(NT, 1)
         }
 
         // Step 1 (per thread): m_t
-        float mx = -INFINITY;
+        typename E::MaxAcc macc = E::max_init();
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) mx = fmaxf(mx, E::vmax(x[k]));
+        for (int k = 0; k < VPT; ++k) E::max_step(macc, x[k]);
+        const float mx = E::max_value(macc);
         const float Mx = mx * kLog2e;  // -inf when the thread holds no element
         hv = mx != -INFINITY;
         off = hv ? Mx : 0.f;
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(NT, 1)
                 mbar_arrive_expect_tx(&xbar[(j - 2) & (NB - 1)], (uint32_t)(K * sizeof(float4)));
             __syncwarp();
             if (lane < K) {
-                const int b = (int)(j & (NB - 1));
+                const int b = j & (NB - 1);
                 st_async_f4(mapa(&xbuf[b][rank], (uint32_t)lane),
                             make_float4(Mc, sc, zt, has_t ? 1.f : 0.f),
                             mapa(&xbar[b], (uint32_t)lane));
@@ -343,13 +346,13 @@ __global__ void __launch_bounds__(NT, 1)
     };
 
     // -------------------------------------------------------------- B(j-1)
-    auto stage_b = [&](long long jp, const uint4 (&x)[VPT], float off, bool hv, long long t) {
-        const long long row = cid + jp * ncl;
+    auto stage_b = [&](int jp, const uint4 (&x)[VPT], float off, bool hv, int t) {
+        const int row = cid + jp * ncl;
         const Geom g = geom(row);
         const bool has_loc = t >= c0 && t < c1;
-        const int tl = has_loc ? (int)(t - c0) + g.head : kNoTarget;
+        const int tl = has_loc ? t - c0 + g.head : kNoTarget;
         const int v_t = has_loc ? tl / W : -1;
-        const int b = (int)(jp & (NB - 1));
+        const int b = jp & (NB - 1);
         if (!failed && !mbar_wait_cluster(&xbar[b], (uint32_t)((jp >> 2) & 1))) fail();
         // combine the K partials in rank order (the same bits in every warp
         // of every CTA of the cluster)
@@ -450,16 +453,16 @@ __global__ void __launch_bounds__(NT, 1)
     uint4 xp[VPT];
     float offp = 0.f;
     bool hvp = false;
-    long long tp = 0;
+    int tp = 0;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) xp[k] = kNeg;
-    for (long long j = 0; j <= nrows; ++j) {
+    for (int j = 0; j <= nrows; ++j) {
         uint4 xc[VPT];
 #pragma unroll
         for (int k = 0; k < VPT; ++k) xc[k] = kNeg;
         float offc = 0.f;
         bool hvc = false;
-        long long tc = 0;
+        int tc = 0;
         if (j < nrows) stage_a(j, xc, offc, hvc, tc);
         if (j > 0) stage_b(j - 1, xp, offp, hvp, tp);
 #pragma unroll
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(NT, 1)
     // A CTA that gave up still owns copies in flight: wait for them (bounded)
     // before its shared memory is released.
     if (issuer && (failed || cta_failed)) {
-        for (long long j = consumed; j < issued; ++j) {
+        for (int j = consumed; j < issued; ++j) {
             if (!mbar_wait(&full[j % nslots], (uint32_t)((j / nslots) & 1))) break;
         }
     }

@@ -201,9 +201,10 @@ __global__ void __launch_bounds__(NT, 1)
         }
 
         // ---- Step 1: slice max
-        float mx = -INFINITY;
+        typename E::MaxAcc macc = E::max_init();
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) mx = fmaxf(mx, E::vmax(x[k]));
+        for (int k = 0; k < VPT; ++k) E::max_step(macc, x[k]);
+        float mx = E::max_value(macc);
         mx = warp_max(mx);
         if (lane == 0) red_max[par][warp] = mx;
         failed = __syncthreads_or(failed);  // the slot is no longer read: back to the copy engine

@@ -171,8 +171,10 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
 
             // Step 1: max
             float m = fmaxf(hz, tz);
+            typename E::MaxAcc macc = E::max_init();
 #pragma unroll
-            for (int k = 0; k < MAXV; ++k) m = fmaxf(m, E::vmax(x[k]));
+            for (int k = 0; k < MAXV; ++k) E::max_step(macc, x[k]);
+            m = fmaxf(m, E::max_value(macc));
             m = warp_max(m);
             const float M = m * kLog2e;
             const unsigned long long nM2 = f2_pack(-M, -M);
