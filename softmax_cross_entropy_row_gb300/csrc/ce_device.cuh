@@ -317,6 +317,15 @@ __device__ __forceinline__ uint4 lds128(const unsigned char *p) {
     return *reinterpret_cast<const uint4 *>(p);
 }
 
+// Named barriers (ids 1..15; id 0 is __syncthreads): a non-blocking arrival
+// and a waiting arrival, `threads` counting both.
+__device__ __forceinline__ void named_arrive(int id, int threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ------------------------------------------------------------------ clusters
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -509,16 +518,16 @@ __device__ __forceinline__ void tail_write(const Params &p, const float2 *vw_tot
     *p.ticket = 0u;  // ready for the next launch on this workspace
 }
 
-// CTA-wide completion: called by every thread once the CTA's row losses are
-// stored.  The CTA that finishes last evaluates the batch loss, one virtual
-// warp per real warp.  `flag` and `scratch` ([8]) live in shared memory.
-__device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *scratch) {
+// CTA-wide publication of the row losses: called by every thread once the
+// CTA's row losses are stored; returns true (in every thread) in the CTA that
+// finishes last.  `flag` lives in shared memory.
+__device__ __forceinline__ bool publish_rows(const Params &p, int *flag) {
     __syncthreads();
     if (threadIdx.x == 0) {
         // acquire-release at GPU scope: publishes this CTA's row losses (the
         // barrier above orders the other threads' stores before it) and, in
-        // the last CTA, makes every other CTA's visible to the loads below
-        // (the barrier after it extends that to the other threads)
+        // the last CTA, makes every other CTA's visible to the loads of the
+        // batch tail (the barrier after it extends that to the other threads)
         const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
         unsigned int prev;
         asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
@@ -528,16 +537,25 @@ __device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *s
         *flag = (prev == total - 1u);
     }
     __syncthreads();
-    if (*flag) {
-        const int warp = threadIdx.x >> 5;
-        const int lane = threadIdx.x & 31;
-        for (int vw = warp; vw < kTailWarps; vw += blockDim.x >> 5) {
-            const float2 v = tail_virtual_warp(p, vw, lane);
-            if (lane == 0) scratch[vw] = v;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) tail_write(p, scratch);
+    return *flag != 0;
+}
+
+// The batch loss, evaluated by every thread of the last CTA (one virtual warp
+// per real warp).  `scratch` ([8]) lives in shared memory.
+__device__ __forceinline__ void batch_tail(const Params &p, float2 *scratch) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int vw = warp; vw < kTailWarps; vw += blockDim.x >> 5) {
+        const float2 v = tail_virtual_warp(p, vw, lane);
+        if (lane == 0) scratch[vw] = v;
     }
+    __syncthreads();
+    if (threadIdx.x == 0) tail_write(p, scratch);
+}
+
+// publish_rows, then the batch tail in the last CTA.
+__device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *scratch) {
+    if (publish_rows(p, flag)) batch_tail(p, scratch);
 }
 
 }  // namespace ce

@@ -57,13 +57,6 @@ namespace {
 
 constexpr int kExchangeSlots = 4;
 
-__device__ __forceinline__ void named_arrive(int id, int threads) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-__device__ __forceinline__ void named_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 // A vector's exponentials as fp32 pairs: the vector itself when it already
 // holds them (fp32 rows), else 2^(z*log2e - M_t) from its logits.
 template <typename E, bool kHeld, int W2>
