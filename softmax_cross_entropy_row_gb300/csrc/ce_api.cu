@@ -132,6 +132,16 @@ bool split_pipe_enabled() {
     return on;
 }
 
+// Tuning knob: CE_SPLIT_STAGE=0 makes the barrier-per-row split kernel store
+// its gradient directly instead of through the row's slot.  Read once.
+bool split_stage_enabled() {
+    static const bool on = [] {
+        const char *e = getenv("CE_SPLIT_STAGE");
+        return !(e && atoi(e) == 0);
+    }();
+    return on;
+}
+
 int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, Plan *pl) {
     const long long row_bytes = C * es;
     if (row_bytes > kWarpRowMax) return CE_ERR_PATH;
@@ -279,7 +289,7 @@ cudaError_t launch_split_plan(const ce::Params &p, int dtype, const Plan &pl, cu
         return ce::launch_split_pipe(p, dtype, pl.split, pl.ctas, pl.nslots, pl.slot_bytes,
                                      pl.slice, pl.smem, s);
     return ce::launch_split(p, dtype, pl.split, pl.vecs, pl.ctas, pl.nslots, pl.slot_bytes,
-                            pl.slice, pl.smem, s);
+                            pl.slice, pl.smem, split_stage_enabled() ? 1 : 0, s);
 }
 
 int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl) {

@@ -33,7 +33,7 @@ namespace {
 
 template <typename T, int K, int NT, int VPT>
 __global__ void __launch_bounds__(NT, 1)
-    row_split_kernel(Params p, int nslots, int slot_bytes, long long SE) {
+    row_split_kernel(Params p, int nslots, int slot_bytes, long long SE, int staged) {
     using E = Elem<T>;
     constexpr int NW = NT / 32;
     constexpr int W = E::kVec;
@@ -65,6 +65,10 @@ __global__ void __launch_bounds__(NT, 1)
     const long long nrows = cid < p.B ? (p.B - cid + ncl - 1) / ncl : 0;
     const uint64_t lbase = reinterpret_cast<uint64_t>(p.logits);
     const bool vec_store = p.grad_vec_ok != 0;
+    // Staged gradient: each thread writes its whole vectors' gradient over
+    // their logits in the slot, and the row leaves in one TMA bulk store; the
+    // slot is handed back to the copy engine one row later, once read out.
+    const bool stage = staged != 0 && vec_store;
     const unsigned long long kL2E2 = f2_pack(kLog2e, kLog2e);
 
     // Byte range [gs, ge) of this CTA's slice of row `row`, and the aligned
@@ -207,11 +211,23 @@ __global__ void __launch_bounds__(NT, 1)
         float mx = E::max_value(macc);
         mx = warp_max(mx);
         if (lane == 0) red_max[par][warp] = mx;
-        failed = __syncthreads_or(failed);  // the slot is no longer read: back to the copy engine
+        failed = __syncthreads_or(failed);
         if (tid == 0 && !failed && issued < nrows) {
-            fence_proxy_async();
-            issue(issued);
-            ++issued;
+            if (stage) {
+                // the slot of row j-1 comes back once its gradient has been
+                // read out by the copy engine
+                if (j > 0) {
+                    bulk_wait_read_all();
+                    fence_proxy_async();
+                    issue(issued);
+                    ++issued;
+                }
+            } else {
+                // the slot is no longer read: back to the copy engine
+                fence_proxy_async();
+                issue(issued);
+                ++issued;
+            }
         }
         float m = lane < NW ? red_max[par][lane] : -INFINITY;
         m = warp_max(m);
@@ -348,7 +364,11 @@ __global__ void __launch_bounds__(NT, 1)
                     exps(x[k], g2);
 #pragma unroll
                     for (int i = 0; i < W2; ++i) g2[i] = f2_mul(g2[i], esc2);
-                    if (vec_store) {
+                    if (stage) {
+                        // in place of the vector's logits, which this thread alone read
+                        *reinterpret_cast<uint4 *>(slot + 16 * v) = E::pack2(g2);
+                        if (v == v_t) E::store(slot + (size_t)tl * ES, g_t);
+                    } else if (vec_store) {
                         *reinterpret_cast<uint4 *>(gbase + 16 * v) = E::pack2(g2);
                     } else {
 #pragma unroll
@@ -360,7 +380,7 @@ __global__ void __launch_bounds__(NT, 1)
                         }
                     }
                     // the owner of the target's vector overwrites the target
-                    if (v == v_t) E::store(gbase + (size_t)tl * ES, g_t);
+                    if (!stage && v == v_t) E::store(gbase + (size_t)tl * ES, g_t);
                 }
             }
             // the partial vectors: element by element, by their owners
@@ -388,6 +408,17 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
 
+        if (stage) {
+            // the whole vectors leave in one bulk store once every thread's
+            // writes are visible to the copy engine
+            fence_proxy_async();
+            failed = __syncthreads_or(failed);
+            if (tid == 0 && !failed && vf1 > vf0) {
+                bulk_s2g(gbase + 16 * vf0, slot + 16 * vf0, (uint32_t)(16 * (vf1 - vf0)));
+                bulk_commit();
+            }
+        }
+
         // ---- Step 3: the row's loss (one writer per row)
         if (rank == 0 && tid == 0 && !failed) {
             float l;
@@ -401,6 +432,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
     }
 
+    if (stage && tid == 0) bulk_wait_all();  // the last gradient stores have landed
     // A CTA that gave up still owns copies in flight: wait for them (bounded)
     // before its shared memory is released.
     if (tid == 0 && failed) {
@@ -414,7 +446,7 @@ __global__ void __launch_bounds__(NT, 1)
 
 template <typename T, int K, int NT, int VPT>
 cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long long se,
-                     int smem, cudaStream_t s) {
+                     int smem, int staged, cudaStream_t s) {
     auto kern = row_split_kernel<T, K, NT, VPT>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
@@ -435,7 +467,7 @@ cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, kern, p, nslots, slot_bytes, se);
+    return cudaLaunchKernelEx(&cfg, kern, p, nslots, slot_bytes, se, staged);
 }
 
 template <typename T, int K, int NT, int VPT>
@@ -469,15 +501,15 @@ cudaError_t max_clusters_k(int smem, int *clusters) {
 
 template <typename T, int V>
 cudaError_t launch_v(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
-                     int smem, cudaStream_t s) {
+                     int smem, int staged, cudaStream_t s) {
     constexpr int NT = kSplitThreads;
     switch (K) {
-        case 1: return launch_k<T, 1, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 2: return launch_k<T, 2, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 3: return launch_k<T, 3, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 4: return launch_k<T, 4, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 6: return launch_k<T, 6, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
-        case 8: return launch_k<T, 8, NT, V>(p, ctas, nslots, slot_bytes, se, smem, s);
+        case 1: return launch_k<T, 1, NT, V>(p, ctas, nslots, slot_bytes, se, smem, staged, s);
+        case 2: return launch_k<T, 2, NT, V>(p, ctas, nslots, slot_bytes, se, smem, staged, s);
+        case 3: return launch_k<T, 3, NT, V>(p, ctas, nslots, slot_bytes, se, smem, staged, s);
+        case 4: return launch_k<T, 4, NT, V>(p, ctas, nslots, slot_bytes, se, smem, staged, s);
+        case 6: return launch_k<T, 6, NT, V>(p, ctas, nslots, slot_bytes, se, smem, staged, s);
+        case 8: return launch_k<T, 8, NT, V>(p, ctas, nslots, slot_bytes, se, smem, staged, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -498,10 +530,10 @@ cudaError_t max_clusters_v(int K, int smem, int *clusters) {
 
 template <typename T>
 cudaError_t launch_t(const Params &p, int K, int vecs, int ctas, int nslots, int slot_bytes,
-                     long long se, int smem, cudaStream_t s) {
-    if (vecs == 16) return launch_v<T, 16>(p, K, ctas, nslots, slot_bytes, se, smem, s);
-    if (vecs == 12) return launch_v<T, 12>(p, K, ctas, nslots, slot_bytes, se, smem, s);
-    if (vecs == 8) return launch_v<T, 8>(p, K, ctas, nslots, slot_bytes, se, smem, s);
+                     long long se, int smem, int staged, cudaStream_t s) {
+    if (vecs == 16) return launch_v<T, 16>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
+    if (vecs == 12) return launch_v<T, 12>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
+    if (vecs == 8) return launch_v<T, 8>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
     return cudaErrorInvalidValue;
 }
 
@@ -516,10 +548,12 @@ cudaError_t max_clusters_t(int K, int vecs, int smem, int *clusters) {
 }  // namespace
 
 cudaError_t launch_split(const Params &p, int dtype, int K, int vecs, int ctas, int nslots,
-                         int slot_bytes, long long slice_elems, int smem, cudaStream_t s) {
+                         int slot_bytes, long long slice_elems, int smem, int staged,
+                         cudaStream_t s) {
     if (dtype == 0)
-        return launch_t<float>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem, s);
-    return launch_t<__nv_bfloat16>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem, s);
+        return launch_t<float>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem, staged, s);
+    return launch_t<__nv_bfloat16>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem,
+                                   staged, s);
 }
 
 cudaError_t split_max_clusters(int dtype, int K, int vecs, int smem, int *clusters) {
