@@ -37,14 +37,23 @@ typedef enum {
     CE_ERR_DTYPE = 3,    /* dtype is not a ce_dtype                             */
     CE_ERR_ALIGN = 4,    /* a pointer is not aligned to its element size        */
     CE_ERR_CUDA = 5,     /* a CUDA runtime call failed (see ce_last_cuda_error) */
-    CE_ERR_OVERLAP = 6,  /* grad_out overlaps logits, targets or loss_out       */
+    CE_ERR_OVERLAP = 6,  /* an output (grad_out, loss_out) overlaps an input or
+                            the other output                                    */
     CE_ERR_POINTER = 7,  /* a pointer is not accessible from the current device */
     CE_ERR_CAPTURE = 8,  /* the call needs to grow its workspace while the
                             stream is being captured; call once uncaptured first */
     CE_ERR_PATH = 9,     /* a forced path/split cannot run this shape           */
-    CE_ERR_SCRATCH = 10  /* ce_fwd_bwd_noalloc: the shape needs more scratch than
+    CE_ERR_SCRATCH = 10, /* ce_fwd_bwd_noalloc: the shape needs more scratch than
                             its static array holds                               */
+    CE_ERR_REDUCTION = 11 /* reduction is not a ce_reduction                    */
 } ce_status;
+
+/* How the row losses l_b are reduced (ce_fwd_bwd_ex, ce_forward). */
+typedef enum {
+    CE_REDUCE_MEAN = 0, /* loss_out[0] = (1/B) sum_b l_b; grad = (softmax - onehot) / B  */
+    CE_REDUCE_SUM = 1,  /* loss_out[0] = sum_b l_b;       grad = softmax - onehot        */
+    CE_REDUCE_NONE = 2  /* loss_out[b] = l_b ([B] fp32);  grad row b = d l_b / d z_b      */
+} ce_reduction;
 
 /* Kernel paths (for ce_fwd_bwd_path and ce_query_plan). */
 typedef enum {
@@ -100,6 +109,46 @@ int ce_fwd_bwd(const void *logits, const int32_t *targets, int64_t B, int64_t C,
 int ce_fwd_bwd_path(const void *logits, const int32_t *targets, int64_t B, int64_t C,
                     int dtype, float *loss_out, void *grad_out, void *stream, int path,
                     int split);
+
+/*
+ * ce_fwd_bwd_ex -- ce_fwd_bwd with a reduction, an upstream gradient, and an
+ * optional gradient.  The rumus project page's backward for this loss (M7a)
+ * scales the gradient precomputed in the forward pass by the upstream
+ * gradient, a device scalar; this entry point fuses that scale into the
+ * gradient's single write.
+ *
+ *   reduction   a ce_reduction (see above): the loss written to loss_out and
+ *               the row factor of the gradient (1/B for the mean, else 1).
+ *   grad_scale  device pointer or NULL (= 1): for CE_REDUCE_MEAN and
+ *               CE_REDUCE_SUM one fp32 multiplying the whole gradient (the
+ *               upstream gradient of the reduced loss); for CE_REDUCE_NONE
+ *               [B] fp32, row b's gradient multiplied by grad_scale[b].
+ *               Read on the device; 4-byte aligned.
+ *   loss_out    device: one fp32 (mean, sum) or [B] fp32 (none).
+ *   grad_out    device [B][C] in the logits' dtype, or NULL: loss only (the
+ *               gradient is neither computed nor written; the logits are the
+ *               only large read and nothing large is written).
+ * The sum is formed in the same fixed order as the mean (bitwise
+ * reproducible); per-row losses are written directly.  Outputs must not
+ * overlap inputs or each other.  Returns a ce_status (CE_ERR_REDUCTION for an
+ * unknown reduction).
+ */
+int ce_fwd_bwd_ex(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
+                  int reduction, const float *grad_scale, float *loss_out, void *grad_out,
+                  void *stream);
+
+/* ce_fwd_bwd_ex with the kernel path forced, as in ce_fwd_bwd_path. */
+int ce_fwd_bwd_ex_path(const void *logits, const int32_t *targets, int64_t B, int64_t C,
+                       int dtype, int reduction, const float *grad_scale, float *loss_out,
+                       void *grad_out, void *stream, int path, int split);
+
+/*
+ * ce_forward -- the loss alone (inference): ce_fwd_bwd_ex with grad_scale and
+ * grad_out NULL.  The rumus project page's loss forward (M7a) without the
+ * precomputed gradient.
+ */
+int ce_forward(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
+               int reduction, float *loss_out, void *stream);
 
 /*
  * ce_query_plan -- the launch that ce_fwd_bwd would make for this shape on

@@ -57,6 +57,11 @@ def _load():
             lib.ce_oracle_rows.argtypes = [vp, ctypes.c_int, vp, i64, i64, vp, i64, vp, vp]
             lib.ce_oracle_rows.restype = ctypes.c_int
             lib.ce_oracle_batch_loss.argtypes = [vp, i64]
+            lib.ce_oracle_rows_ex.argtypes = [vp, ctypes.c_int, vp, i64, i64, ctypes.c_int, vp,
+                                              vp, i64, vp, vp]
+            lib.ce_oracle_rows_ex.restype = ctypes.c_int
+            lib.ce_oracle_reduce.argtypes = [vp, i64, ctypes.c_int]
+            lib.ce_oracle_reduce.restype = ctypes.c_double
             lib.ce_oracle_batch_loss.restype = ctypes.c_double
             lib.ce_oracle_fwd_bwd.argtypes = [vp, ctypes.c_int, vp, i64, i64, vp, vp, vp]
             lib.ce_oracle_fwd_bwd.restype = ctypes.c_int
@@ -102,6 +107,46 @@ def rows(logits: np.ndarray, targets: np.ndarray, row_ids=None, grad: bool = Tru
     if rc != 0:
         raise ValueError("ce_oracle_rows rejected its arguments")
     return (loss, g) if grad else loss
+
+
+MEAN, SUM, NONE = 0, 1, 2
+
+
+def rows_ex(logits: np.ndarray, targets: np.ndarray, reduction: int, upstream=None,
+            row_ids=None, grad: bool = True):
+    """Per-row losses and fp64 gradient rows for a reduction (MEAN, SUM, NONE)
+    and an upstream gradient ``upstream`` (None = 1; one value for MEAN and
+    SUM, [B] values for NONE): the gradient is upstream * dL/dz."""
+    lib = _load()
+    logits = np.ascontiguousarray(logits)
+    targets = np.ascontiguousarray(targets, dtype=np.int32)
+    B, C = logits.shape
+    if targets.shape != (B,):
+        raise ValueError("targets must have shape [B]")
+    up = None
+    if upstream is not None:
+        up = np.ascontiguousarray(np.atleast_1d(np.asarray(upstream, dtype=np.float64)))
+        if up.size != (B if reduction == NONE else 1):
+            raise ValueError("upstream must hold one value (mean, sum) or B values (none)")
+    if row_ids is None:
+        ids_ptr, n = None, B
+    else:
+        ids = np.ascontiguousarray(row_ids, dtype=np.int64)
+        ids_ptr, n = ids.ctypes.data, ids.size
+    loss = np.empty(n, dtype=np.float64)
+    g = np.empty((n, C), dtype=np.float64) if grad else None
+    rc = lib.ce_oracle_rows_ex(logits.ctypes.data, _dtype_code(logits), targets.ctypes.data,
+                               B, C, int(reduction), None if up is None else up.ctypes.data,
+                               ids_ptr, n, loss.ctypes.data, None if g is None else g.ctypes.data)
+    if rc != 0:
+        raise ValueError("ce_oracle_rows_ex rejected its arguments")
+    return (loss, g) if grad else loss
+
+
+def reduce(loss_rows: np.ndarray, reduction: int) -> float:
+    """Pass 2 for MEAN ((sum l_b) / B) or SUM (sum l_b), in row order, fp64."""
+    lr = np.ascontiguousarray(loss_rows, dtype=np.float64)
+    return float(_load().ce_oracle_reduce(lr.ctypes.data, lr.size, int(reduction)))
 
 
 def batch_loss(loss_rows: np.ndarray) -> float:

@@ -51,9 +51,10 @@ static double oracle_z(const void *logits, int dtype, int64_t i) {
     return (double)f;
 }
 
-/* One row: the four steps of Pass 1.  grad_row may be NULL (loss only). */
+/* One row: the four steps of Pass 1.  grad_row may be NULL (loss only);
+ * factor multiplies the gradient (1/B for the batch mean). */
 static double oracle_row(const void *logits, int dtype, int64_t b, int64_t C,
-                         int32_t t, double inv_b, double *grad_row) {
+                         int32_t t, double factor, double *grad_row) {
     const int64_t row_start = b * C;
     int target_ok = (t >= 0 && (int64_t)t < C);
 
@@ -73,7 +74,7 @@ static double oracle_row(const void *logits, int dtype, int64_t b, int64_t C,
         for (int64_t c = 0; c < C; ++c) {
             double p = exp(oracle_z(logits, dtype, row_start + c) - m) / s;
             double one_hot = (target_ok && c == (int64_t)t) ? 1.0 : 0.0;
-            grad_row[c] = (p - one_hot) * inv_b;
+            grad_row[c] = (p - one_hot) * factor;
         }
     }
     return loss;
@@ -128,6 +129,48 @@ double ce_oracle_batch_loss(const double *loss_rows, int64_t B) {
     double s = 0.0;
     for (int64_t b = 0; b < B; ++b) s += loss_rows[b];
     return s / (double)B;
+}
+
+/*
+ * The reductions and the upstream gradient.  The rumus project page's backward
+ * for this loss (milestone M7a) multiplies the gradient precomputed in the
+ * forward pass by the upstream gradient; written out for each reduction of
+ * the row losses l_b:
+ *   mean (0):  L = (1/B) sum_b l_b   dL/dz[b][c]     = (p[b][c] - [c == t_b]) / B
+ *   sum  (1):  L = sum_b l_b         dL/dz[b][c]     = p[b][c] - [c == t_b]
+ *   none (2):  L_b = l_b             dL_b/dz[b][c]   = p[b][c] - [c == t_b]
+ * and with an upstream gradient u (one value for mean and sum, u_b per row
+ * for none; NULL means 1) the gradient returned is u * dL/dz.
+ *   upstream  NULL, [1] (mean, sum) or [B] (none), in fp64
+ * Otherwise as ce_oracle_rows.  Returns 0, or -1 on a bad argument.
+ */
+int ce_oracle_rows_ex(const void *logits, int dtype, const int32_t *targets, int64_t B,
+                      int64_t C, int reduction, const double *upstream, const int64_t *rows,
+                      int64_t nrows, double *loss, double *grad) {
+    if (!logits || !targets || !loss || B <= 0 || C <= 0 || nrows < 0) return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+    if (reduction < 0 || reduction > 2) return -1;
+    if (!rows && nrows != B) return -1;
+    for (int64_t i = 0; i < nrows; ++i)
+        if (rows && (rows[i] < 0 || rows[i] >= B)) return -1;
+    const double base = reduction == 0 ? 1.0 / (double)B : 1.0;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t b = rows ? rows[i] : i;
+        double u = 1.0;
+        if (upstream) u = reduction == 2 ? upstream[b] : upstream[0];
+        loss[i] = oracle_row(logits, dtype, b, C, targets[b], base * u,
+                             grad ? grad + i * C : (double *)0);
+    }
+    return 0;
+}
+
+/* Pass 2 for a reduction: (sum_b l_b) / B for the mean, sum_b l_b for the sum,
+ * summed in row order. */
+double ce_oracle_reduce(const double *loss_rows, int64_t B, int reduction) {
+    double s = 0.0;
+    for (int64_t b = 0; b < B; ++b) s += loss_rows[b];
+    return reduction == 0 ? s / (double)B : s;
 }
 
 /* Narrow a double to fp32 and then to bf16 (round to nearest even each time). */

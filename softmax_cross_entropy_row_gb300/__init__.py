@@ -12,6 +12,9 @@ Pass 1 and the reduction of Pass 2 of rumus 0.1.1's cross_entropy.wgsl):
 
     loss = (1/B) * sum_b (logsumexp(z_b) - z_b[t_b])
     grad = (softmax(z_b) - onehot(t_b)) / B
+
+and, through ce_fwd_bwd_ex / ce_forward, the sum and per-row reductions, an
+upstream gradient fused into the gradient's write, and the loss alone.
 """
 
 from __future__ import annotations
@@ -29,17 +32,21 @@ CE_PATH_ROWS_WARP = 1
 CE_PATH_ROW_SPLIT = 2
 CE_PATH_STREAM = 3
 
+CE_REDUCE_MEAN = 0
+CE_REDUCE_SUM = 1
+CE_REDUCE_NONE = 2
+
 PATH_NAMES = {CE_PATH_ROWS_WARP: "rows_warp", CE_PATH_ROW_SPLIT: "row_split",
               CE_PATH_STREAM: "stream"}
 
 STATUS = {0: "CE_OK", 1: "CE_ERR_NULL", 2: "CE_ERR_SHAPE", 3: "CE_ERR_DTYPE",
           4: "CE_ERR_ALIGN", 5: "CE_ERR_CUDA", 6: "CE_ERR_OVERLAP", 7: "CE_ERR_POINTER",
-          8: "CE_ERR_CAPTURE", 9: "CE_ERR_PATH", 10: "CE_ERR_SCRATCH"}
+          8: "CE_ERR_CAPTURE", 9: "CE_ERR_PATH", 10: "CE_ERR_SCRATCH", 11: "CE_ERR_REDUCTION"}
 
 # Symbols declared in include/ce.h.
 EXPORTS = ("ce_fwd_bwd", "ce_fwd_bwd_path", "ce_query_plan", "ce_get_device_errors",
            "ce_release_workspaces", "ce_status_string", "ce_last_cuda_error",
-           "ce_fwd_bwd_noalloc")
+           "ce_fwd_bwd_noalloc", "ce_fwd_bwd_ex", "ce_fwd_bwd_ex_path", "ce_forward")
 
 
 class CEError(RuntimeError):
@@ -81,6 +88,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.ce_last_cuda_error.restype = ctypes.c_char_p
     lib.ce_fwd_bwd_noalloc.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp]
     lib.ce_fwd_bwd_noalloc.restype = ci
+    lib.ce_fwd_bwd_ex.argtypes = [vp, vp, i64, i64, ci, ci, vp, vp, vp, vp]
+    lib.ce_fwd_bwd_ex.restype = ci
+    lib.ce_fwd_bwd_ex_path.argtypes = [vp, vp, i64, i64, ci, ci, vp, vp, vp, vp, ci, ci]
+    lib.ce_fwd_bwd_ex_path.restype = ci
+    lib.ce_forward.argtypes = [vp, vp, i64, i64, ci, ci, vp, vp]
+    lib.ce_forward.restype = ci
     if path is None:
         _lib = lib
     return lib
@@ -143,6 +156,34 @@ def ce_fwd_bwd_path(logits, targets, loss_out, grad_out, stream=None, path=CE_PA
     _check(lib.ce_fwd_bwd_path(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
                                _ptr(loss_out), _ptr(grad_out), _stream_handle(stream),
                                int(path), int(split)))
+
+
+def ce_fwd_bwd_ex(logits, targets, loss_out, grad_out=None, reduction=CE_REDUCE_MEAN,
+                  grad_scale=None, stream=None, path=CE_PATH_AUTO, split=0) -> None:
+    """ce_fwd_bwd with a reduction (CE_REDUCE_MEAN / SUM / NONE), an optional
+    upstream gradient ``grad_scale`` (a one-element fp32 CUDA tensor for the
+    mean and sum, a [B] one for NONE) and an optional ``grad_out`` (None: the
+    loss alone).  ``loss_out`` holds one fp32 (mean, sum) or B (none)."""
+    lib = load_library()
+    if logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous [B, C] tensor")
+    if grad_out is not None and (grad_out.shape != logits.shape or grad_out.dtype != logits.dtype
+                                 or not grad_out.is_contiguous()):
+        raise ValueError("grad_out must be a contiguous tensor of the logits' shape and dtype")
+    B, C = logits.shape
+    _check(lib.ce_fwd_bwd_ex_path(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
+                                  int(reduction), _ptr(grad_scale), _ptr(loss_out),
+                                  _ptr(grad_out), _stream_handle(stream), int(path), int(split)))
+
+
+def ce_forward(logits, targets, loss_out, reduction=CE_REDUCE_MEAN, stream=None) -> None:
+    """The loss alone (no gradient): one fp32 (mean, sum) or [B] (none)."""
+    lib = load_library()
+    if logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous [B, C] tensor")
+    B, C = logits.shape
+    _check(lib.ce_forward(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
+                          int(reduction), _ptr(loss_out), _stream_handle(stream)))
 
 
 def ce_fwd_bwd_raw(logits_ptr: int, targets_ptr: int, B: int, C: int, dtype: int,

@@ -381,10 +381,15 @@ int check_pointer(const void *p, const DeviceInfo &d) {
     return CE_ERR_POINTER;
 }
 
+// grad_out == nullptr: loss only.  grad_scale: nullptr, one fp32 (mean,
+// sum) or [B] fp32 (none).  loss_out: one fp32 (mean, sum) or [B] (none).
 int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
-        float *loss_out, void *grad_out, void *stream, int path, int split) {
+        int reduction, const float *grad_scale, float *loss_out, void *grad_out, void *stream,
+        int path, int split) {
     if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_DTYPE;
-    if (!logits || !targets || !loss_out || !grad_out) return CE_ERR_NULL;
+    if (reduction != CE_REDUCE_MEAN && reduction != CE_REDUCE_SUM && reduction != CE_REDUCE_NONE)
+        return CE_ERR_REDUCTION;
+    if (!logits || !targets || !loss_out) return CE_ERR_NULL;
     if (B < 1 || C < 1 || B > 0x7fffffffLL || C > 0x7fffffffLL) return CE_ERR_SHAPE;
     const int es = dtype == CE_F32 ? 4 : 2;
     if ((unsigned long long)B * (unsigned long long)C > (1ull << 61) / (unsigned)es)
@@ -393,10 +398,16 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     const uintptr_t gz = reinterpret_cast<uintptr_t>(grad_out);
     const uintptr_t tz = reinterpret_cast<uintptr_t>(targets);
     const uintptr_t oz = reinterpret_cast<uintptr_t>(loss_out);
-    if (lz % es || gz % es || tz % 4 || oz % 4) return CE_ERR_ALIGN;
+    const uintptr_t sz = reinterpret_cast<uintptr_t>(grad_scale);
+    if (lz % es || gz % es || tz % 4 || oz % 4 || sz % 4) return CE_ERR_ALIGN;
     const size_t nbytes = (size_t)B * (size_t)C * es;
-    if (ranges_overlap(gz, nbytes, lz, nbytes) || ranges_overlap(gz, nbytes, tz, (size_t)B * 4) ||
-        ranges_overlap(gz, nbytes, oz, 4))
+    const size_t per_row = reduction == CE_REDUCE_NONE ? (size_t)B * 4 : 4;  // loss_out, grad_scale
+    if (grad_out &&
+        (ranges_overlap(gz, nbytes, lz, nbytes) || ranges_overlap(gz, nbytes, tz, (size_t)B * 4) ||
+         ranges_overlap(gz, nbytes, oz, per_row) || (grad_scale && ranges_overlap(gz, nbytes, sz, per_row))))
+        return CE_ERR_OVERLAP;
+    if (ranges_overlap(oz, per_row, lz, nbytes) || ranges_overlap(oz, per_row, tz, (size_t)B * 4) ||
+        (grad_scale && ranges_overlap(oz, per_row, sz, per_row)))
         return CE_ERR_OVERLAP;
 
     int dev = 0;
@@ -406,8 +417,8 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     int rc = device_info(dev, &d);
     if (rc != CE_OK) return rc;
     for (const void *ptr : {logits, (const void *)targets, (const void *)loss_out,
-                            (const void *)grad_out}) {
-        if ((rc = check_pointer(ptr, d)) != CE_OK) return rc;
+                            (const void *)grad_out, (const void *)grad_scale}) {
+        if (ptr && (rc = check_pointer(ptr, d)) != CE_OK) return rc;
     }
 
     Plan pl;
@@ -433,7 +444,9 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     p.loss_out = loss_out;
     p.ticket = reinterpret_cast<unsigned int *>(ws.base);
     p.err = reinterpret_cast<int *>(ws.base + 4);
-    p.loss_rows = reinterpret_cast<float *>(ws.base + kHeaderBytes);
+    // per-row losses as the output: written where the caller wants them
+    p.loss_rows = reduction == CE_REDUCE_NONE ? loss_out
+                                              : reinterpret_cast<float *>(ws.base + kHeaderBytes);
     p.parts = pl.path == CE_PATH_STREAM ? reinterpret_cast<float2 *>(ws.base + parts_off) : nullptr;
     p.zt = pl.path == CE_PATH_STREAM ? reinterpret_cast<float *>(ws.base + zt_off) : nullptr;
     p.B = B;
@@ -442,7 +455,11 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     p.lo_clip = (uint64_t)((lz + 15) & ~(uintptr_t)15);
     p.hi_clip = (uint64_t)((lz + nbytes) & ~(uintptr_t)15);
     if (p.hi_clip < p.lo_clip) p.hi_clip = p.lo_clip;
-    p.grad_vec_ok = ((gz - lz) % 16) == 0;
+    p.grad_vec_ok = grad_out != nullptr && ((gz - lz) % 16) == 0;
+    p.reduction = reduction;
+    p.grad_base = reduction == CE_REDUCE_MEAN ? p.inv_b : 1.f;
+    p.grad_scale = grad_scale;
+    p.scale_per_row = grad_scale != nullptr && reduction == CE_REDUCE_NONE;
 
     switch (pl.path) {
         case CE_PATH_ROWS_WARP:
@@ -557,6 +574,10 @@ int run_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C
     p.hi_clip = (uint64_t)((lz + nbytes) & ~(uintptr_t)15);
     if (p.hi_clip < p.lo_clip) p.hi_clip = p.lo_clip;
     p.grad_vec_ok = ((gz - lz) % 16) == 0;
+    p.reduction = CE_REDUCE_MEAN;
+    p.grad_base = p.inv_b;
+    p.grad_scale = nullptr;
+    p.scale_per_row = 0;
 
     if (pl.path == CE_PATH_ROWS_WARP)
         e = ce::launch_rows_warp(p, dtype, pl.per_sm, pl.ctas, pl.nslots, pl.rows_per_tile,
@@ -593,12 +614,36 @@ extern "C" {
 
 int ce_fwd_bwd(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
                float *loss_out, void *grad_out, void *stream) {
-    return run(logits, targets, B, C, dtype, loss_out, grad_out, stream, CE_PATH_AUTO, 0);
+    if (!grad_out) return CE_ERR_NULL;
+    return run(logits, targets, B, C, dtype, CE_REDUCE_MEAN, nullptr, loss_out, grad_out, stream,
+               CE_PATH_AUTO, 0);
 }
 
 int ce_fwd_bwd_path(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
                     float *loss_out, void *grad_out, void *stream, int path, int split) {
-    return run(logits, targets, B, C, dtype, loss_out, grad_out, stream, path, split);
+    if (!grad_out) return CE_ERR_NULL;
+    return run(logits, targets, B, C, dtype, CE_REDUCE_MEAN, nullptr, loss_out, grad_out, stream,
+               path, split);
+}
+
+int ce_fwd_bwd_ex(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
+                  int reduction, const float *grad_scale, float *loss_out, void *grad_out,
+                  void *stream) {
+    return run(logits, targets, B, C, dtype, reduction, grad_scale, loss_out, grad_out, stream,
+               CE_PATH_AUTO, 0);
+}
+
+int ce_fwd_bwd_ex_path(const void *logits, const int32_t *targets, int64_t B, int64_t C,
+                       int dtype, int reduction, const float *grad_scale, float *loss_out,
+                       void *grad_out, void *stream, int path, int split) {
+    return run(logits, targets, B, C, dtype, reduction, grad_scale, loss_out, grad_out, stream,
+               path, split);
+}
+
+int ce_forward(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
+               int reduction, float *loss_out, void *stream) {
+    return run(logits, targets, B, C, dtype, reduction, nullptr, loss_out, nullptr, stream,
+               CE_PATH_AUTO, 0);
 }
 
 int ce_query_plan(int64_t B, int64_t C, int dtype, int *path, int *split, int *ctas,
@@ -664,13 +709,14 @@ const char *ce_status_string(int status) {
         case CE_ERR_DTYPE: return "unknown dtype";
         case CE_ERR_ALIGN: return "pointer not aligned to its element size";
         case CE_ERR_CUDA: return "CUDA runtime error";
-        case CE_ERR_OVERLAP: return "grad_out overlaps an input or loss_out";
+        case CE_ERR_OVERLAP: return "an output overlaps an input or the other output";
         case CE_ERR_POINTER: return "pointer not accessible from the current device";
         case CE_ERR_CAPTURE: return "workspace must grow while the stream is being captured";
         case CE_ERR_PATH: return "the forced path cannot run this shape";
         case CE_ERR_SCRATCH:
             return "shape exceeds the static scratch of ce_fwd_bwd_noalloc (B <= 262144, "
                    "rows held in shared memory)";
+        case CE_ERR_REDUCTION: return "reduction is not a ce_reduction";
         default: return "unknown status";
     }
 }

@@ -44,7 +44,27 @@ struct Params {
     uint64_t lo_clip;             // TMA-safe byte range of the logits:
     uint64_t hi_clip;             //   [round_up16(begin), round_down16(end))
     int grad_vec_ok;              // grad and logits share their address mod 16
+    // Reductions and the upstream gradient.  grad == nullptr: loss only.
+    int reduction;                // kReduceMean, kReduceSum or kReduceNone
+    float grad_base;              // 1/B (mean) or 1 (sum, none)
+    const float *grad_scale;      // nullptr (1), one fp32, or [B] fp32 (scale_per_row)
+    int scale_per_row;
 };
+
+constexpr int kReduceMean = 0;
+constexpr int kReduceSum = 1;
+constexpr int kReduceNone = 2;  // the row losses are the output (loss_rows = loss_out)
+
+// The upstream gradient when it is one scalar (1 when absent or per row).
+__device__ __forceinline__ float scalar_grad_scale(const Params &p) {
+    return (p.grad_scale != nullptr && !p.scale_per_row) ? __ldg(p.grad_scale) : 1.f;
+}
+
+// The gradient's factor for row `row`: 1/B (mean) or 1, times the upstream
+// gradient (the scalar `scalar` from scalar_grad_scale, or row's own).
+__device__ __forceinline__ float row_grad_factor(const Params &p, float scalar, long long row) {
+    return p.grad_base * (p.scale_per_row ? __ldg(p.grad_scale + row) : scalar);
+}
 
 // Packed fp32 pairs (Blackwell f32x2 arithmetic: each half is rounded exactly
 // as the scalar instruction would round it).
@@ -519,8 +539,9 @@ __device__ __forceinline__ float2 tail_virtual_warp(const Params &p, int vw, int
 }
 
 // Adds the 8 virtual-warp totals in order, writes L and re-arms the ticket.
-// (h + l) / B is formed in fp32 with one correction step (no fp64: its
-// division is a long dependent sequence on this part):
+// The sum h + l is the loss of the sum reduction; for the mean, (h + l) / B
+// is formed in fp32 with one correction step (no fp64: its division is a long
+// dependent sequence on this part):
 //   q0 = h * fp32(1/B),  r = (h - q0 B) + l  (the fma is exact up to one
 //   rounding),  L = q0 + r * fp32(1/B).
 __device__ __forceinline__ void tail_write(const Params &p, const float2 *vw_totals) {
@@ -532,9 +553,13 @@ __device__ __forceinline__ void tail_write(const Params &p, const float2 *vw_tot
         h = s;
         l += vw_totals[w].y + e;
     }
-    const float q0 = h * p.inv_b;
-    const float r = fmaf(-q0, static_cast<float>(p.B), h) + l;
-    *p.loss_out = fmaf(r, p.inv_b, q0);
+    if (p.reduction == kReduceSum) {
+        *p.loss_out = h + l;
+    } else {
+        const float q0 = h * p.inv_b;
+        const float r = fmaf(-q0, static_cast<float>(p.B), h) + l;
+        *p.loss_out = fmaf(r, p.inv_b, q0);
+    }
     *p.ticket = 0u;  // ready for the next launch on this workspace
 }
 
@@ -573,8 +598,10 @@ __device__ __forceinline__ void batch_tail(const Params &p, float2 *scratch) {
     if (threadIdx.x == 0) tail_write(p, scratch);
 }
 
-// publish_rows, then the batch tail in the last CTA.
+// publish_rows, then the batch tail in the last CTA (nothing to do when the
+// row losses are themselves the output).
 __device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *scratch) {
+    if (p.reduction == kReduceNone) return;
     if (publish_rows(p, flag)) batch_tail(p, scratch);
 }
 

@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     pdl_trigger();
     pdl_wait();  // nothing above touched global memory
+    const float gsc = scalar_grad_scale(p);
     // every CTA's exchange mbarriers exist before any peer pushes into them
     cluster_sync();
 
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(NT, 1)
         S = s_rest + e_t;
 
         // Step 4: gradient of the slice
-        const float scale = fast_rcp(S) * p.inv_b;
+        const float scale = fast_rcp(S) * row_grad_factor(p, gsc, row);
         // a thread without elements has nothing to scale (and M_t = 0 is not
         // an upper bound of anything)
         const float escale = hv ? scale * ex2(off - M) : 0.f;
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(NT, 1)
         const float g_t = -s_rest * scale;
         unsigned char *gbase = p.grad + ((uint64_t)g.e0 - (uint64_t)g.head) * ES;
         const bool skip = failed || *reinterpret_cast<volatile int *>(&cta_failed) != 0;
-        if (!skip) {
+        if (!skip && p.grad != nullptr) {  // else loss only
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = tid + k * NT;

@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(NT, 1)
     // Staged gradient: each thread writes its whole vectors' gradient over
     // their logits in the slot, and the row leaves in one TMA bulk store; the
     // slot is handed back to the copy engine one row later, once read out.
-    const bool stage = staged != 0 && vec_store;
+    const bool write_grad = p.grad != nullptr;  // false: loss only
+    const bool stage = staged != 0 && vec_store && write_grad;
     const unsigned long long kL2E2 = f2_pack(kLog2e, kLog2e);
 
     // Byte range [gs, ge) of this CTA's slice of row `row`, and the aligned
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     pdl_trigger();
     pdl_wait();  // nothing above touched global memory
+    const float gsc = scalar_grad_scale(p);
     __syncthreads();
     long long issued = 0;
     if (tid == 0) {
@@ -336,14 +338,15 @@ __global__ void __launch_bounds__(NT, 1)
         S = s_rest + e_t;
 
         // ---- Step 4: gradient of the slice
-        const float scale = fast_rcp(S) * p.inv_b;
+        const float scale = fast_rcp(S) * row_grad_factor(p, gsc, row);
         const float escale = K > 1 ? scale * ex2(M_off - M) : scale;
         const unsigned long long esc2 = f2_pack(escale, escale);
         // (p_t - 1) / B = -S_rest / (S B): no cancellation when p_t is near 1
         const float g_t = -s_rest * scale;
         unsigned char *gbase = p.grad + (g0 - lbase);  // grad byte of vector 0
         // The slice's exponentials as fp32 pairs: held in x for fp32 rows,
-        // evaluated again from the raw bf16 logits otherwise.
+        // evaluated again from the raw bf16 logits otherwise.  Nothing is
+        // written when only the loss is wanted.
         auto exps = [&](const uint4 &xv, unsigned long long (&e2)[W2]) {
             E::unpack2(xv, e2);
             if (!kKeepExp) {
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
         };
-        if (!failed) {
+        if (!failed && write_grad) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = tid + k * NT;

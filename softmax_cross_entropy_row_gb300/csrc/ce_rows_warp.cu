@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     unsigned char *my_slots = smem + (size_t)warp * slots * slot_bytes;
     uint64_t *my_full = full + warp * kMaxWarpSlots;
     const bool vec_store = p.grad_vec_ok != 0;
-    const float inv_b = p.inv_b;
+    const bool write_grad = p.grad != nullptr;  // false: loss only
     const unsigned long long kL2E2 = f2_pack(kLog2e, kLog2e);
 
     auto span = [&](long long tile, long long &r0, long long &r1, uint64_t &gs, uint64_t &ge,
@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     }
     pdl_trigger();
     pdl_wait();  // nothing above touched global memory
+    const float gsc = scalar_grad_scale(p);
     __syncwarp();
     long long issued = 0;
     if (lane == 0) {
@@ -220,47 +221,50 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
             const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
             const float S = s_rest + e_t;
 
-            // Step 4: gradient; (p_t - 1) / B = -S_rest / (S B)
-            const float scale = fast_rcp(S) * inv_b;
+            // Step 4: gradient; (p_t - 1) / B = -S_rest / (S B), times the
+            // upstream gradient (1/B becomes 1 for the sum and per-row losses)
+            const float scale = fast_rcp(S) * row_grad_factor(p, gsc, r);
             const unsigned long long sc2 = f2_pack(scale, scale);
             const float g_t = -s_rest * scale;
-            unsigned char *grow = p.grad + (size_t)r * C * ES;
-            unsigned char *gvec = grow + nh * ES;
+            if (write_grad) {
+                unsigned char *grow = p.grad + (size_t)r * C * ES;
+                unsigned char *gvec = grow + nh * ES;
 #pragma unroll
-            for (int k = 0; k < MAXV; ++k) {
-                const int v = lane + 32 * k;
-                if (v < nvec) {
-                    unsigned long long g2[W2];
-                    E::unpack2(x[k], g2);
-#pragma unroll
-                    for (int j = 0; j < W2; ++j) {
-                        if (!kKeepExp) {
-                            float a, b;
-                            f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
-                            g2[j] = f2_pack(ex2(a), ex2(b));
-                        }
-                        g2[j] = f2_mul(g2[j], sc2);
-                    }
-                    if (vec_store) {
-                        *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack2(g2);
-                    } else {
+                for (int k = 0; k < MAXV; ++k) {
+                    const int v = lane + 32 * k;
+                    if (v < nvec) {
+                        unsigned long long g2[W2];
+                        E::unpack2(x[k], g2);
 #pragma unroll
                         for (int j = 0; j < W2; ++j) {
-                            float a, b;
-                            f2_unpack(g2[j], a, b);
-                            E::store(gvec + (v * W + 2 * j) * ES, a);
-                            E::store(gvec + (v * W + 2 * j + 1) * ES, b);
+                            if (!kKeepExp) {
+                                float a, b;
+                                f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
+                                g2[j] = f2_pack(ex2(a), ex2(b));
+                            }
+                            g2[j] = f2_mul(g2[j], sc2);
                         }
+                        if (vec_store) {
+                            *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack2(g2);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < W2; ++j) {
+                                float a, b;
+                                f2_unpack(g2[j], a, b);
+                                E::store(gvec + (v * W + 2 * j) * ES, a);
+                                E::store(gvec + (v * W + 2 * j + 1) * ES, b);
+                            }
+                        }
+                        // the owner of the target's vector overwrites the target
+                        if (v == v_t) E::store(grow + (size_t)t * ES, g_t);
                     }
-                    // the owner of the target's vector overwrites the target
-                    if (v == v_t) E::store(grow + (size_t)t * ES, g_t);
                 }
-            }
-            if (ragged) {
-                if (lane < nh) E::store(grow + lane * ES, lane == t ? g_t : eh * scale);
-                if (lane < nt) {
-                    const int c = nh + nvec * W + lane;
-                    E::store(grow + c * ES, c == t ? g_t : et * scale);
+                if (ragged) {
+                    if (lane < nh) E::store(grow + lane * ES, lane == t ? g_t : eh * scale);
+                    if (lane < nt) {
+                        const int c = nh + nvec * W + lane;
+                        E::store(grow + c * ES, c == t ? g_t : et * scale);
+                    }
                 }
             }
 

@@ -101,17 +101,19 @@ __global__ void __launch_bounds__(NT) stream_grad_kernel(Params p, long long chu
     const float zt = has_t ? __ldcg(p.zt + b) : 0.f;
     const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
     const float S = s_rest + e_t;
-    const float inv_b = p.inv_b;
-    const float scale = fast_rcp(S) * inv_b;
-    const float g_t = -s_rest * scale;  // (p_t - 1) / B without cancellation
-    const unsigned char *row = p.logits + (size_t)(b * C) * E::kBytes;
-    unsigned char *grow = p.grad + (size_t)(b * C) * E::kBytes;
+    // (p_t - 1) / B without cancellation, times the upstream gradient
+    const float scale = fast_rcp(S) * row_grad_factor(p, scalar_grad_scale(p), b);
+    const float g_t = -s_rest * scale;
+    if (p.grad != nullptr) {  // else loss only
+        const unsigned char *row = p.logits + (size_t)(b * C) * E::kBytes;
+        unsigned char *grow = p.grad + (size_t)(b * C) * E::kBytes;
 #pragma unroll
-    for (int i = 0; i < PT; ++i) {
-        const long long c = cbeg + i * NT + threadIdx.x;
-        if (c < C) {
-            const float ev = ex2(fmaf(E::load_global(row + c * E::kBytes), kLog2e, -M));
-            E::store(grow + c * E::kBytes, c == t ? g_t : ev * scale);
+        for (int i = 0; i < PT; ++i) {
+            const long long c = cbeg + i * NT + threadIdx.x;
+            if (c < C) {
+                const float ev = ex2(fmaf(E::load_global(row + c * E::kBytes), kLog2e, -M));
+                E::store(grow + c * E::kBytes, c == t ? g_t : ev * scale);
+            }
         }
     }
     if (k == 0 && threadIdx.x == 0) {

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_need_no_gpu(lib):
-    for code in range(11):
+    for code in range(12):
         s = lib.ce_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.ce_status_string(99).decode() == "unknown status"
@@ -55,6 +55,27 @@ def test_host_side_argument_errors_need_no_gpu(lib):
     assert f(256, 514, 4, 4, 1, 1024, 4096) == 4            # int32 targets at 2 mod 4
     assert f(1 << 20, 512, 4, 4, 0, 1024, (1 << 20) + 32) == 6  # grad overlaps logits
     assert f(1 << 20, 1 << 24, 4, 4, 0, 1 << 25, (1 << 24) - 32) == 6  # grad covers targets
+
+
+def test_host_side_errors_of_the_extended_entry_points(lib):
+    """Reductions, the upstream gradient and the loss-only forward check their
+    arguments before any CUDA call too."""
+    ex = lib.ce_fwd_bwd_ex
+    fw = lib.ce_forward
+    # reduction out of range
+    assert ex(256, 512, 4, 4, 0, 3, None, 1024, 4096, None) == 11
+    assert fw(256, 512, 4, 4, 0, -1, 1024, None) == 11
+    # loss only: the gradient may be NULL, the loss may not
+    assert fw(256, 512, 4, 4, 0, 0, None, None) == 1
+    assert ex(256, 512, 4, 4, 0, 2, None, None, None, None) == 1
+    # misaligned upstream gradient
+    assert ex(256, 512, 4, 4, 0, 0, 2050, 1024, 4096, None) == 4
+    # per-row losses (4 B bytes) overlapping the logits
+    assert ex(1 << 20, 1 << 24, 4, 4, 0, 2, None, (1 << 20) + 16, 1 << 26, None) == 6
+    # a per-row upstream gradient overlapping the per-row losses
+    assert ex(1 << 20, 1 << 24, 4, 4, 0, 2, 1 << 25, (1 << 25) + 8, 1 << 26, None) == 6
+    # the gradient overlapping the scalar upstream gradient
+    assert ex(1 << 20, 1 << 24, 4, 4, 0, 0, (1 << 26) + 32, 1 << 25, 1 << 26, None) == 6
 
 
 def test_no_cpu_fallback_without_library(tmp_path):

@@ -270,3 +270,71 @@ def test_rejects_bad_arguments(oracle_mod):
         oracle_mod.rows(np.zeros((2, 3), np.float32), np.zeros(2, np.int32), row_ids=[2])
     with pytest.raises(TypeError):
         oracle_mod.rows(np.zeros((2, 3), np.float64), np.zeros(2, np.int32))
+
+
+# ------------------------------------- reductions and the upstream gradient
+
+def test_reductions_against_torch(oracle_mod):
+    """sum and none against torch CPU fp64 F.cross_entropy with autograd, with
+    an upstream gradient (a scalar for the sum, one value per row for none)."""
+    torch = pytest.importorskip("torch")
+    B, C = 48, 257
+    inp = wl.random_case(B, C, "f32", seed=5, sigma=4.0)
+    zt = torch.tensor(inp.logits, dtype=torch.float64, requires_grad=True)
+    tt = torch.tensor(inp.targets, dtype=torch.int64)
+    # sum, upstream 0.375
+    l_sum, g_sum = oracle_mod.rows_ex(inp.logits, inp.targets, oracle_mod.SUM, upstream=0.375)
+    loss = torch.nn.functional.cross_entropy(zt, tt, reduction="sum")
+    (0.375 * loss).backward()
+    assert oracle_mod.reduce(l_sum, oracle_mod.SUM) == pytest.approx(loss.item(), rel=1e-13)
+    assert np.allclose(g_sum, zt.grad.numpy(), rtol=1e-12, atol=1e-18)
+    # none, per-row upstream u_b
+    u = np.linspace(-2.0, 3.0, B)
+    zt.grad = None
+    l_none, g_none = oracle_mod.rows_ex(inp.logits, inp.targets, oracle_mod.NONE, upstream=u)
+    per_row = torch.nn.functional.cross_entropy(zt, tt, reduction="none")
+    (per_row * torch.tensor(u)).sum().backward()
+    assert np.allclose(l_none, per_row.detach().numpy(), rtol=1e-13, atol=1e-14)
+    assert np.allclose(g_none, zt.grad.numpy(), rtol=1e-12, atol=1e-18)
+
+
+def test_per_row_gradient_matches_finite_differences(oracle_mod):
+    """For none, row b's gradient is d l_b / d z_b: central differences of the
+    row loss with exact fp32 steps; other rows' losses do not move."""
+    rng = np.random.default_rng(11)
+    B, C = 3, 4
+    h = 2.0 ** -10
+    z = (rng.integers(-512, 512, size=(B, C)) * h).astype(np.float32)
+    t = rng.integers(0, C, B).astype(np.int32)
+    l0, g = oracle_mod.rows_ex(z, t, oracle_mod.NONE)
+    for b in range(B):
+        for c in range(C):
+            zp, zm = z.copy(), z.copy()
+            zp[b, c] += np.float32(h)
+            zm[b, c] -= np.float32(h)
+            lp = oracle_mod.rows_ex(zp, t, oracle_mod.NONE, grad=False)
+            lm = oracle_mod.rows_ex(zm, t, oracle_mod.NONE, grad=False)
+            assert (lp[b] - lm[b]) / (2 * h) == pytest.approx(g[b, c], abs=2e-7)
+            others = [r for r in range(B) if r != b]
+            assert np.array_equal(lp[others], l0[others])
+
+
+def test_reduction_relations(oracle_mod):
+    """The mean is the sum over B, with the gradient over B; the per-row losses
+    are the same in every reduction; the upstream gradient scales linearly."""
+    inp = wl.random_case(16, 300, "bf16", seed=8, sigma=3.0)
+    B = 16
+    l_m, g_m = oracle_mod.rows_ex(inp.logits, inp.targets, oracle_mod.MEAN)
+    l_s, g_s = oracle_mod.rows_ex(inp.logits, inp.targets, oracle_mod.SUM)
+    l_n, g_n = oracle_mod.rows_ex(inp.logits, inp.targets, oracle_mod.NONE)
+    assert np.array_equal(l_m, l_s) and np.array_equal(l_m, l_n)
+    assert oracle_mod.reduce(l_m, oracle_mod.MEAN) * B == pytest.approx(
+        oracle_mod.reduce(l_s, oracle_mod.SUM), rel=1e-14)
+    assert np.allclose(g_m * B, g_s, rtol=1e-14, atol=0)
+    assert np.array_equal(g_s, g_n)
+    _, g_u = oracle_mod.rows_ex(inp.logits, inp.targets, oracle_mod.MEAN, upstream=-2.5)
+    assert np.allclose(g_u, -2.5 * g_m, rtol=1e-15, atol=0)
+    with pytest.raises(ValueError):
+        oracle_mod.rows_ex(inp.logits, inp.targets, 3)
+    with pytest.raises(ValueError):
+        oracle_mod.rows_ex(inp.logits, inp.targets, oracle_mod.NONE, upstream=1.0)
