@@ -17,6 +17,7 @@
 namespace {
 
 using ce::Params;
+using ce::ParamsEx;
 
 thread_local char g_cuda_error[256] = "";
 
@@ -284,7 +285,7 @@ int plan_stream(long long B, long long C, Plan *pl) {
     return CE_OK;
 }
 
-cudaError_t launch_split_plan(const ce::Params &p, int dtype, const Plan &pl, cudaStream_t s) {
+cudaError_t launch_split_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, cudaStream_t s) {
     if (pl.pipe)
         return ce::launch_split_pipe(p, dtype, pl.split, pl.ctas, pl.nslots, pl.slot_bytes,
                                      pl.slice, pl.smem, s);
@@ -437,7 +438,7 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     Workspace ws;
     if ((rc = get_workspace(dev, s, need, &ws)) != CE_OK) return rc;
 
-    Params p;
+    ParamsEx p;
     p.logits = static_cast<const unsigned char *>(logits);
     p.targets = targets;
     p.grad = static_cast<unsigned char *>(grad_out);
@@ -557,7 +558,7 @@ int run_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C
     // counters must start at zero, the row losses are all rewritten.
     if ((e = cudaMemsetAsync(base, 0, kHeaderBytes, s)) != cudaSuccess) return cuda_fail(e);
 
-    Params p;
+    ParamsEx p;
     p.logits = static_cast<const unsigned char *>(logits);
     p.targets = targets;
     p.grad = static_cast<unsigned char *>(grad_out);

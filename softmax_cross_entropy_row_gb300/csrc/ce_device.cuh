@@ -44,9 +44,15 @@ struct Params {
     uint64_t lo_clip;             // TMA-safe byte range of the logits:
     uint64_t hi_clip;             //   [round_up16(begin), round_down16(end))
     int grad_vec_ok;              // grad and logits share their address mod 16
-    // Reductions and the upstream gradient.  grad == nullptr: loss only.
+};
+
+// The general call's parameters: a reduction, an upstream gradient, or the
+// loss alone.  The kernels are built for Params (the plain call: the mean,
+// no upstream gradient, a gradient to write) and for ParamsEx; the plain
+// build carries none of the general case's work.
+struct ParamsEx : Params {
     int reduction;                // kReduceMean, kReduceSum or kReduceNone
-    float grad_base;              // 1/B (mean) or 1 (sum, none)
+    float grad_base;              // the gradient's row factor: 1/B (mean) or 1 (sum, none)
     const float *grad_scale;      // nullptr (1), one fp32, or [B] fp32 (scale_per_row)
     int scale_per_row;
 };
@@ -55,15 +61,35 @@ constexpr int kReduceMean = 0;
 constexpr int kReduceSum = 1;
 constexpr int kReduceNone = 2;  // the row losses are the output (loss_rows = loss_out)
 
+__host__ __device__ __forceinline__ constexpr int reduction_of(const Params &) {
+    return kReduceMean;
+}
+__host__ __device__ __forceinline__ int reduction_of(const ParamsEx &p) { return p.reduction; }
+
+// false: the loss alone (no gradient computed or written)
+__host__ __device__ __forceinline__ constexpr bool writes_grad(const Params &) { return true; }
+__host__ __device__ __forceinline__ bool writes_grad(const ParamsEx &p) {
+    return p.grad != nullptr;
+}
+
 // The upstream gradient when it is one scalar (1 when absent or per row).
-__device__ __forceinline__ float scalar_grad_scale(const Params &p) {
+__device__ __forceinline__ float scalar_grad_scale(const Params &) { return 1.f; }
+__device__ __forceinline__ float scalar_grad_scale(const ParamsEx &p) {
     return (p.grad_scale != nullptr && !p.scale_per_row) ? __ldg(p.grad_scale) : 1.f;
 }
 
 // The gradient's factor for row `row`: 1/B (mean) or 1, times the upstream
 // gradient (the scalar `scalar` from scalar_grad_scale, or row's own).
-__device__ __forceinline__ float row_grad_factor(const Params &p, float scalar, long long row) {
+__device__ __forceinline__ float row_grad_factor(const Params &p, float, long long) {
+    return p.inv_b;
+}
+__device__ __forceinline__ float row_grad_factor(const ParamsEx &p, float scalar, long long row) {
     return p.grad_base * (p.scale_per_row ? __ldg(p.grad_scale + row) : scalar);
+}
+
+// The plain call, which runs the Params build of the kernels.
+inline bool is_plain(const ParamsEx &p) {
+    return p.reduction == kReduceMean && p.grad_scale == nullptr && p.grad != nullptr;
 }
 
 // Packed fp32 pairs (Blackwell f32x2 arithmetic: each half is rounded exactly
@@ -544,7 +570,8 @@ __device__ __forceinline__ float2 tail_virtual_warp(const Params &p, int vw, int
 // dependent sequence on this part):
 //   q0 = h * fp32(1/B),  r = (h - q0 B) + l  (the fma is exact up to one
 //   rounding),  L = q0 + r * fp32(1/B).
-__device__ __forceinline__ void tail_write(const Params &p, const float2 *vw_totals) {
+template <typename P>
+__device__ __forceinline__ void tail_write(const P &p, const float2 *vw_totals) {
     float h = 0.f, l = 0.f;
 #pragma unroll
     for (int w = 0; w < kTailWarps; ++w) {
@@ -553,7 +580,7 @@ __device__ __forceinline__ void tail_write(const Params &p, const float2 *vw_tot
         h = s;
         l += vw_totals[w].y + e;
     }
-    if (p.reduction == kReduceSum) {
+    if (reduction_of(p) == kReduceSum) {
         *p.loss_out = h + l;
     } else {
         const float q0 = h * p.inv_b;
@@ -587,7 +614,8 @@ __device__ __forceinline__ bool publish_rows(const Params &p, int *flag) {
 
 // The batch loss, evaluated by every thread of the last CTA (one virtual warp
 // per real warp).  `scratch` ([8]) lives in shared memory.
-__device__ __forceinline__ void batch_tail(const Params &p, float2 *scratch) {
+template <typename P>
+__device__ __forceinline__ void batch_tail(const P &p, float2 *scratch) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     for (int vw = warp; vw < kTailWarps; vw += blockDim.x >> 5) {
@@ -600,8 +628,9 @@ __device__ __forceinline__ void batch_tail(const Params &p, float2 *scratch) {
 
 // publish_rows, then the batch tail in the last CTA (nothing to do when the
 // row losses are themselves the output).
-__device__ __forceinline__ void finish_cta(const Params &p, int *flag, float2 *scratch) {
-    if (p.reduction == kReduceNone) return;
+template <typename P>
+__device__ __forceinline__ void finish_cta(const P &p, int *flag, float2 *scratch) {
+    if (reduction_of(p) == kReduceNone) return;
     if (publish_rows(p, flag)) batch_tail(p, scratch);
 }
 

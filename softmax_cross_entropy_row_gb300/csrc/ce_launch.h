@@ -30,7 +30,7 @@ constexpr int kMaxWarpSlots = 4;  // per warp
 // kSplitThreads * vecs 16-byte vectors (vecs = 8, 12 or 16) in registers.
 // `staged` = 1: gradients of whole vectors go out through the row's own slot
 // by one TMA bulk store (needs grad and logits equally aligned mod 16).
-cudaError_t launch_split(const Params &p, int dtype, int K, int vecs, int ctas, int nslots,
+cudaError_t launch_split(const ParamsEx &p, int dtype, int K, int vecs, int ctas, int nslots,
                          int slot_bytes, long long slice_elems, int smem, int staged,
                          cudaStream_t s);
 // Largest number of co-resident clusters of K CTAs with `smem` dynamic bytes.
@@ -40,18 +40,18 @@ cudaError_t split_max_clusters(int dtype, int K, int vecs, int smem, int *cluste
 // slices of at most kSplitThreads * kPipeVecs vectors, no CTA-wide barrier per
 // row; the partials of one row are exchanged while the next row is reduced.
 constexpr int kPipeVecs = 8;
-cudaError_t launch_split_pipe(const Params &p, int dtype, int K, int ctas, int nslots,
+cudaError_t launch_split_pipe(const ParamsEx &p, int dtype, int K, int ctas, int nslots,
                               int slot_bytes, long long slice_elems, int smem, cudaStream_t s);
 cudaError_t split_pipe_max_clusters(int dtype, int K, int smem, int *clusters);
 
 // Warp-per-row path: tiles of `rows_per_tile` consecutive rows, `slots` tiles
 // staged per warp; `per_sm` (1 or 2) selects the build made for that many
 // resident CTAs per SM.
-cudaError_t launch_rows_warp(const Params &p, int dtype, int per_sm, int ctas, int slots,
+cudaError_t launch_rows_warp(const ParamsEx &p, int dtype, int per_sm, int ctas, int slots,
                              int rows_per_tile, int slot_bytes, int smem, cudaStream_t s);
 cudaError_t rows_warp_max_ctas_per_sm(int dtype, int per_sm, long long C, int smem, int *ctas);
 
 // Streaming path: pass A (chunk partials) and pass B (combine, gradient, loss).
-cudaError_t launch_stream(const Params &p, int dtype, long long chunks, cudaStream_t s);
+cudaError_t launch_stream(const ParamsEx &p, int dtype, long long chunks, cudaStream_t s);
 
 }  // namespace ce

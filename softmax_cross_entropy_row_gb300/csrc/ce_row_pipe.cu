@@ -84,9 +84,9 @@ __device__ __forceinline__ float element_of(const uint4 &w, int d) {
     return __uint_as_float((d & 1) ? (q & 0xffff0000u) : (q << 16));
 }
 
-template <typename T, int K, int NT, int VPT>
+template <typename T, int K, int NT, int VPT, typename P>
 __global__ void __launch_bounds__(NT, 1)
-    row_pipe_kernel(Params p, int nslots, int slot_bytes, long long SE) {
+    row_pipe_kernel(P p, int nslots, int slot_bytes, long long SE) {
     using E = Elem<T>;
     constexpr int NW = NT / 32;
     constexpr int W = E::kVec;
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(NT, 1)
         const float g_t = -s_rest * scale;
         unsigned char *gbase = p.grad + ((uint64_t)g.e0 - (uint64_t)g.head) * ES;
         const bool skip = failed || *reinterpret_cast<volatile int *>(&cta_failed) != 0;
-        if (!skip && p.grad != nullptr) {  // else loss only
+        if (!skip && writes_grad(p)) {  // else loss only
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = tid + k * NT;
@@ -477,10 +477,10 @@ __global__ void __launch_bounds__(NT, 1)
     finish_cta(p, &tail_flag, tail_scratch);
 }
 
-template <typename T, int K>
-cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long long se,
-                     int smem, cudaStream_t s) {
-    auto kern = row_pipe_kernel<T, K, kSplitThreads, kPipeVecs>;
+template <typename T, int K, typename P>
+cudaError_t launch_kp(const P &p, int ctas, int nslots, int slot_bytes, long long se,
+                      int smem, cudaStream_t s) {
+    auto kern = row_pipe_kernel<T, K, kSplitThreads, kPipeVecs, P>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -500,9 +500,19 @@ cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long
     return cudaLaunchKernelEx(&cfg, kern, p, nslots, slot_bytes, se);
 }
 
+// The plain call runs the Params build, any other the ParamsEx build.
+template <typename T, int K>
+cudaError_t launch_k(const ParamsEx &p, int ctas, int nslots, int slot_bytes, long long se,
+                     int smem, cudaStream_t s) {
+    if (is_plain(p))
+        return launch_kp<T, K, Params>(static_cast<const Params &>(p), ctas, nslots, slot_bytes,
+                                       se, smem, s);
+    return launch_kp<T, K, ParamsEx>(p, ctas, nslots, slot_bytes, se, smem, s);
+}
+
 template <typename T, int K>
 cudaError_t max_clusters_k(int smem, int *clusters) {
-    auto kern = row_pipe_kernel<T, K, kSplitThreads, kPipeVecs>;
+    auto kern = row_pipe_kernel<T, K, kSplitThreads, kPipeVecs, Params>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -520,7 +530,7 @@ cudaError_t max_clusters_k(int smem, int *clusters) {
 }
 
 template <typename T>
-cudaError_t launch_t(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
+cudaError_t launch_t(const ParamsEx &p, int K, int ctas, int nslots, int slot_bytes, long long se,
                      int smem, cudaStream_t s) {
     switch (K) {
         case 2: return launch_k<T, 2>(p, ctas, nslots, slot_bytes, se, smem, s);
@@ -546,7 +556,7 @@ cudaError_t max_clusters_t(int K, int smem, int *clusters) {
 
 }  // namespace
 
-cudaError_t launch_split_pipe(const Params &p, int dtype, int K, int ctas, int nslots,
+cudaError_t launch_split_pipe(const ParamsEx &p, int dtype, int K, int ctas, int nslots,
                               int slot_bytes, long long slice_elems, int smem, cudaStream_t s) {
     if (dtype == 0) return launch_t<float>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);
     return launch_t<__nv_bfloat16>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);

@@ -31,9 +31,9 @@
 namespace ce {
 namespace {
 
-template <typename T, int K, int NT, int VPT>
+template <typename T, int K, int NT, int VPT, typename P>
 __global__ void __launch_bounds__(NT, 1)
-    row_split_kernel(Params p, int nslots, int slot_bytes, long long SE, int staged) {
+    row_split_kernel(P p, int nslots, int slot_bytes, long long SE, int staged) {
     using E = Elem<T>;
     constexpr int NW = NT / 32;
     constexpr int W = E::kVec;
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(NT, 1)
     // Staged gradient: each thread writes its whole vectors' gradient over
     // their logits in the slot, and the row leaves in one TMA bulk store; the
     // slot is handed back to the copy engine one row later, once read out.
-    const bool write_grad = p.grad != nullptr;  // false: loss only
+    const bool write_grad = writes_grad(p);  // false: loss only
     const bool stage = staged != 0 && vec_store && write_grad;
     const unsigned long long kL2E2 = f2_pack(kLog2e, kLog2e);
 
@@ -447,10 +447,10 @@ __global__ void __launch_bounds__(NT, 1)
     finish_cta(p, &tail_flag, tail_scratch);
 }
 
-template <typename T, int K, int NT, int VPT>
-cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long long se,
-                     int smem, int staged, cudaStream_t s) {
-    auto kern = row_split_kernel<T, K, NT, VPT>;
+template <typename T, int K, int NT, int VPT, typename P>
+cudaError_t launch_kp(const P &p, int ctas, int nslots, int slot_bytes, long long se,
+                      int smem, int staged, cudaStream_t s) {
+    auto kern = row_split_kernel<T, K, NT, VPT, P>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -473,9 +473,19 @@ cudaError_t launch_k(const Params &p, int ctas, int nslots, int slot_bytes, long
     return cudaLaunchKernelEx(&cfg, kern, p, nslots, slot_bytes, se, staged);
 }
 
+// The plain call runs the Params build, any other the ParamsEx build.
+template <typename T, int K, int NT, int VPT>
+cudaError_t launch_k(const ParamsEx &p, int ctas, int nslots, int slot_bytes, long long se,
+                     int smem, int staged, cudaStream_t s) {
+    if (is_plain(p))
+        return launch_kp<T, K, NT, VPT, Params>(static_cast<const Params &>(p), ctas, nslots,
+                                                slot_bytes, se, smem, staged, s);
+    return launch_kp<T, K, NT, VPT, ParamsEx>(p, ctas, nslots, slot_bytes, se, smem, staged, s);
+}
+
 template <typename T, int K, int NT, int VPT>
 cudaError_t max_clusters_k(int smem, int *clusters) {
-    auto kern = row_split_kernel<T, K, NT, VPT>;
+    auto kern = row_split_kernel<T, K, NT, VPT, Params>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     if (K == 1) {
@@ -503,7 +513,7 @@ cudaError_t max_clusters_k(int smem, int *clusters) {
 }
 
 template <typename T, int V>
-cudaError_t launch_v(const Params &p, int K, int ctas, int nslots, int slot_bytes, long long se,
+cudaError_t launch_v(const ParamsEx &p, int K, int ctas, int nslots, int slot_bytes, long long se,
                      int smem, int staged, cudaStream_t s) {
     constexpr int NT = kSplitThreads;
     switch (K) {
@@ -532,7 +542,7 @@ cudaError_t max_clusters_v(int K, int smem, int *clusters) {
 }
 
 template <typename T>
-cudaError_t launch_t(const Params &p, int K, int vecs, int ctas, int nslots, int slot_bytes,
+cudaError_t launch_t(const ParamsEx &p, int K, int vecs, int ctas, int nslots, int slot_bytes,
                      long long se, int smem, int staged, cudaStream_t s) {
     if (vecs == 16) return launch_v<T, 16>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
     if (vecs == 12) return launch_v<T, 12>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
@@ -550,7 +560,7 @@ cudaError_t max_clusters_t(int K, int vecs, int smem, int *clusters) {
 
 }  // namespace
 
-cudaError_t launch_split(const Params &p, int dtype, int K, int vecs, int ctas, int nslots,
+cudaError_t launch_split(const ParamsEx &p, int dtype, int K, int vecs, int ctas, int nslots,
                          int slot_bytes, long long slice_elems, int smem, int staged,
                          cudaStream_t s) {
     if (dtype == 0)

@@ -18,9 +18,9 @@
 namespace ce {
 namespace {
 
-template <typename T, int MAXV, int MINB>
+template <typename T, int MAXV, int MINB, typename P>
 __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
-    rows_warp_kernel(Params p, int slots, int rows_per_tile, int slot_bytes) {
+    rows_warp_kernel(P p, int slots, int rows_per_tile, int slot_bytes) {
     using E = Elem<T>;
     constexpr int NW = kWarpKernelWarps;
     constexpr int ES = E::kBytes;
@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     unsigned char *my_slots = smem + (size_t)warp * slots * slot_bytes;
     uint64_t *my_full = full + warp * kMaxWarpSlots;
     const bool vec_store = p.grad_vec_ok != 0;
-    const bool write_grad = p.grad != nullptr;  // false: loss only
+    const bool write_grad = writes_grad(p);  // false: loss only
     const unsigned long long kL2E2 = f2_pack(kLog2e, kLog2e);
 
     auto span = [&](long long tile, long long &r0, long long &r1, uint64_t &gs, uint64_t &ge,
@@ -296,10 +296,10 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
     finish_cta(p, &tail_flag, tail_scratch);
 }
 
-template <typename T, int MAXV, int MINB>
-cudaError_t launch_v(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
+template <typename T, int MAXV, int MINB, typename P>
+cudaError_t launch_p(const P &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
                      int smem, cudaStream_t s) {
-    auto kern = rows_warp_kernel<T, MAXV, MINB>;
+    auto kern = rows_warp_kernel<T, MAXV, MINB, P>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -315,9 +315,19 @@ cudaError_t launch_v(const Params &p, int ctas, int slots, int rows_per_tile, in
     return cudaLaunchKernelEx(&cfg, kern, p, slots, rows_per_tile, slot_bytes);
 }
 
+// The plain call runs the Params build, any other the ParamsEx build.
+template <typename T, int MAXV, int MINB>
+cudaError_t launch_v(const ParamsEx &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
+                     int smem, cudaStream_t s) {
+    if (is_plain(p))
+        return launch_p<T, MAXV, MINB, Params>(static_cast<const Params &>(p), ctas, slots,
+                                               rows_per_tile, slot_bytes, smem, s);
+    return launch_p<T, MAXV, MINB, ParamsEx>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+}
+
 template <typename T, int MAXV, int MINB>
 cudaError_t occ_v(int smem, int *ctas) {
-    auto kern = rows_warp_kernel<T, MAXV, MINB>;
+    auto kern = rows_warp_kernel<T, MAXV, MINB, Params>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, kWarpKernelWarps * 32, smem);
@@ -331,7 +341,7 @@ int vectors_per_lane(long long C, int es) {
 }
 
 template <typename T, int MINB>
-cudaError_t launch_m(const Params &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
+cudaError_t launch_m(const ParamsEx &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
                      int smem, cudaStream_t s) {
     switch (vectors_per_lane(p.C, sizeof(T))) {
         case 2: return launch_v<T, 2, MINB>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
@@ -352,7 +362,7 @@ cudaError_t occ_m(long long C, int smem, int *ctas) {
 }
 
 template <typename T>
-cudaError_t launch_t(const Params &p, int per_sm, int ctas, int slots, int rows_per_tile,
+cudaError_t launch_t(const ParamsEx &p, int per_sm, int ctas, int slots, int rows_per_tile,
                      int slot_bytes, int smem, cudaStream_t s) {
     if (per_sm >= 2) return launch_m<T, 2>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
     return launch_m<T, 1>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
@@ -366,7 +376,7 @@ cudaError_t occ_t(int per_sm, long long C, int smem, int *ctas) {
 
 }  // namespace
 
-cudaError_t launch_rows_warp(const Params &p, int dtype, int per_sm, int ctas, int slots,
+cudaError_t launch_rows_warp(const ParamsEx &p, int dtype, int per_sm, int ctas, int slots,
                              int rows_per_tile, int slot_bytes, int smem, cudaStream_t s) {
     if (dtype == 0)
         return launch_t<float>(p, per_sm, ctas, slots, rows_per_tile, slot_bytes, smem, s);

@@ -72,8 +72,8 @@ __global__ void __launch_bounds__(NT) stream_partials_kernel(Params p, long long
         p.zt[b] = E::load_global(row + t * E::kBytes);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(NT) stream_grad_kernel(Params p, long long chunks) {
+template <typename T, typename P>
+__global__ void __launch_bounds__(NT) stream_grad_kernel(P p, long long chunks) {
     using E = Elem<T>;
     __shared__ float red[NT / 32];
     __shared__ float2 tail_scratch[kTailThreads / 32];
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(NT) stream_grad_kernel(Params p, long long chu
     // (p_t - 1) / B without cancellation, times the upstream gradient
     const float scale = fast_rcp(S) * row_grad_factor(p, scalar_grad_scale(p), b);
     const float g_t = -s_rest * scale;
-    if (p.grad != nullptr) {  // else loss only
+    if (writes_grad(p)) {  // else loss only
         const unsigned char *row = p.logits + (size_t)(b * C) * E::kBytes;
         unsigned char *grow = p.grad + (size_t)(b * C) * E::kBytes;
 #pragma unroll
@@ -130,19 +130,23 @@ __global__ void __launch_bounds__(NT) stream_grad_kernel(Params p, long long chu
 }
 
 template <typename T>
-cudaError_t launch_t(const Params &p, long long chunks, cudaStream_t s) {
+cudaError_t launch_t(const ParamsEx &p, long long chunks, cudaStream_t s) {
     const long long blocks = p.B * chunks;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    stream_partials_kernel<T><<<(unsigned)blocks, NT, 0, s>>>(p, chunks);
+    const Params &pp = p;
+    stream_partials_kernel<T><<<(unsigned)blocks, NT, 0, s>>>(pp, chunks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    stream_grad_kernel<T><<<(unsigned)blocks, NT, 0, s>>>(p, chunks);
+    if (is_plain(p))
+        stream_grad_kernel<T, Params><<<(unsigned)blocks, NT, 0, s>>>(pp, chunks);
+    else
+        stream_grad_kernel<T, ParamsEx><<<(unsigned)blocks, NT, 0, s>>>(p, chunks);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_stream(const Params &p, int dtype, long long chunks, cudaStream_t s) {
+cudaError_t launch_stream(const ParamsEx &p, int dtype, long long chunks, cudaStream_t s) {
     if (dtype == 0) return launch_t<float>(p, chunks, s);
     return launch_t<__nv_bfloat16>(p, chunks, s);
 }
