@@ -346,6 +346,81 @@ def bench_e2e(w, inp, device, steps):
             "d2h_bytes_per_step": 4, "steps": steps, "ms_per_step": per_step * 1e3}
 
 
+# The rows beyond the plain fused step, measured the same way: (label, workload,
+# call kind).  Bytes per step are those each call must move.
+NEXT_ROWS = [("loss_only_mean", "classifier_4096x1000_f32", "forward"),
+             ("loss_only_mean", "lm_head_8192x32000_bf16", "forward"),
+             ("sum_scalar_upstream", "classifier_4096x1000_f32", "sum"),
+             ("none_per_row_upstream", "classifier_4096x1000_f32", "none")]
+
+
+def next_row_bytes(w, kind):
+    read = w.B * w.C * w.elem_bytes + 4 * w.B
+    if kind == "forward":
+        return read + 4
+    if kind == "sum":
+        return read + w.B * w.C * w.elem_bytes + 4 + 4
+    return read + w.B * w.C * w.elem_bytes + 4 * w.B + 4 * w.B  # per-row scale and losses
+
+
+def bench_next_row(label, w, inp, kind, device, l2_bytes, hbm_peak):
+    """Device time per step of one extended call (graph replay over buffer
+    sets larger than twice L2, CUDA events on the launching stream)."""
+    import torch
+
+    import softmax_cross_entropy_row_gb300 as ce
+
+    nbytes = next_row_bytes(w, kind)
+    nsets = 1 if nbytes > 2 * l2_bytes else min(MAX_SETS, int(np.ceil(2 * l2_bytes / nbytes)) + 1)
+    z0, t0 = device_set(inp, device)
+    sets = []
+    for i in range(nsets):
+        z = z0 if i == 0 else z0.clone()
+        grad = None if kind == "forward" else torch.empty_like(z)
+        loss = torch.empty(w.B if kind == "none" else 1, dtype=torch.float32, device=device)
+        up = (torch.linspace(0.5, 1.5, w.B, device=device) if kind == "none"
+              else torch.full((1,), 0.5, device=device) if kind == "sum" else None)
+        sets.append((z, t0, loss, grad, up))
+    red = {"forward": ce.CE_REDUCE_MEAN, "sum": ce.CE_REDUCE_SUM, "none": ce.CE_REDUCE_NONE}[kind]
+    s = torch.cuda.Stream(device)
+
+    def call(i):
+        z, t, loss, grad, up = sets[i % nsets]
+        if kind == "forward":
+            ce.ce_forward(z, t, loss, red, s)
+        else:
+            ce.ce_fwd_bwd_ex(z, t, loss, grad, red, up, s)
+
+    with torch.cuda.stream(s):
+        for i in range(3):
+            call(i)
+        s.synchronize()
+        per_graph = nsets * max(1, int(np.ceil(32 / nsets)))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(per_graph):
+                call(i)
+        g.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+        e1.synchronize()
+        reps = max(2, min(200, int(0.3 / max(e0.elapsed_time(e1) / 1e3, 1e-6))))
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
+        e1.synchronize()
+    per_step = e0.elapsed_time(e1) / 1e3 / (reps * per_graph)
+    del g
+    gbs = nbytes / per_step / 1e9
+    return {"row": label, "workload": w.name, "call": kind, "us_per_step": per_step * 1e6,
+            "bytes_per_step": nbytes, "achieved_gbs": gbs, "frac_of_peak": gbs / hbm_peak,
+            "rows_per_s": w.B / per_step}
+
+
 def l2_note(res, w, l2_bytes):
     n = res["buffer_sets"]
     total = n * (2 * w.B * w.C * w.elem_bytes + 4 * w.B)
@@ -430,6 +505,13 @@ def main():
             head_inp = inp
         del inp
 
+    next_rows = []
+    if not args.headline_only and world == 1:
+        for label, name, kind in NEXT_ROWS:
+            ww = wl.WORKLOADS_BY_NAME[name]
+            next_rows.append(bench_next_row(label, ww, wl.make_inputs(ww), kind, device,
+                                            l2_bytes, hbm_peak))
+
     head = results[w.name]
     cpu = None
     if rank == 0 and world == 1 and args.cpu_sample_s > 0:
@@ -460,6 +542,7 @@ def main():
         "clocks": head["clocks"],
         "workloads": [dict(results[n], l2=l2_note(results[n], wl.WORKLOADS_BY_NAME[n], l2_bytes))
                       for n in names],
+        "next_rows": next_rows,
     }
     print(json.dumps(out))
     if world > 1:
