@@ -348,7 +348,13 @@ def bench_e2e(w, inp, device, steps):
 
 # The rows beyond the plain fused step, measured the same way: (label, workload,
 # call kind).  Bytes per step are those each call must move.
-NEXT_ROWS = [("loss_only_mean", "classifier_4096x1000_f32", "forward"),
+# f16 logits: the 32k-class LM head recipe drawn the same way, narrowed to f16
+F16_HEAD = wl.Workload("lm_head_8192x32000_f16", 8192, 32000, "f16", seed=2, sigma=3.0,
+                       description="LM head, f16 logits ~ N(0, 3^2)")
+wl.WORKLOADS_BY_NAME.setdefault(F16_HEAD.name, F16_HEAD)
+
+NEXT_ROWS = [("f16_logits", "lm_head_8192x32000_f16", "plain"),
+             ("loss_only_mean", "classifier_4096x1000_f32", "forward"),
              ("loss_only_mean", "lm_head_8192x32000_bf16", "forward"),
              ("sum_scalar_upstream", "classifier_4096x1000_f32", "sum"),
              ("none_per_row_upstream", "classifier_4096x1000_f32", "none")]
@@ -356,6 +362,8 @@ NEXT_ROWS = [("loss_only_mean", "classifier_4096x1000_f32", "forward"),
 
 def next_row_bytes(w, kind):
     read = w.B * w.C * w.elem_bytes + 4 * w.B
+    if kind == "plain":
+        return w.min_bytes
     if kind == "forward":
         return read + 4
     if kind == "sum":
@@ -381,13 +389,16 @@ def bench_next_row(label, w, inp, kind, device, l2_bytes, hbm_peak):
         up = (torch.linspace(0.5, 1.5, w.B, device=device) if kind == "none"
               else torch.full((1,), 0.5, device=device) if kind == "sum" else None)
         sets.append((z, t0, loss, grad, up))
-    red = {"forward": ce.CE_REDUCE_MEAN, "sum": ce.CE_REDUCE_SUM, "none": ce.CE_REDUCE_NONE}[kind]
+    red = {"forward": ce.CE_REDUCE_MEAN, "sum": ce.CE_REDUCE_SUM, "none": ce.CE_REDUCE_NONE,
+           "plain": ce.CE_REDUCE_MEAN}[kind]
     s = torch.cuda.Stream(device)
 
     def call(i):
         z, t, loss, grad, up = sets[i % nsets]
         if kind == "forward":
             ce.ce_forward(z, t, loss, red, s)
+        elif kind == "plain":
+            ce.ce_fwd_bwd(z, t, loss, grad, s)
         else:
             ce.ce_fwd_bwd_ex(z, t, loss, grad, red, up, s)
 

@@ -26,7 +26,9 @@ extern "C" {
 /* Element type of the logits and of the gradient (always the same type). */
 typedef enum {
     CE_F32 = 0,  /* IEEE fp32                                           */
-    CE_BF16 = 1  /* bfloat16; computed in fp32, gradient rounded to nearest even */
+    CE_BF16 = 1, /* bfloat16; computed in fp32, gradient rounded to nearest even */
+    CE_F16 = 2   /* IEEE fp16 (binary16); computed in fp32, gradient rounded to
+                    nearest even (subnormal results kept)                */
 } ce_dtype;
 
 /* Return codes.  Host-detectable errors return before anything is launched. */
@@ -76,7 +78,9 @@ typedef enum {
  *             term, and the per-stream device error count is incremented
  *             (read it with ce_get_device_errors).  Nothing traps.
  *   B, C      rows and classes, 1 <= B, C <= 2^31-1.
- *   dtype     a ce_dtype.
+ *   dtype     a ce_dtype.  (f16 is the half-precision type of the rumus
+ *             project page's milestone M11, FP16 mixed precision, whose shaders
+ *             run with their scalar type aliased to f16.)
  *   loss_out  device, one fp32: (1/B) * sum_b l_b.  The row losses are summed
  *             in a fixed order, so the value is bitwise reproducible for the
  *             same inputs on the same GPU model, whichever path runs.
@@ -99,7 +103,8 @@ int ce_fwd_bwd(const void *logits, const int32_t *targets, int64_t B, int64_t C,
 /*
  * ce_fwd_bwd_path -- ce_fwd_bwd with the kernel path forced (tests, tuning).
  *   path   a ce_path; CE_PATH_AUTO behaves exactly as ce_fwd_bwd.
- *   split  CE_PATH_ROW_SPLIT: CTAs per row (1, 2, 3, 4, 6 or 8; 0 = choose);
+ *   split  CE_PATH_ROW_SPLIT: CTAs per row (1, 2, 3, 4, 6 or 8; 0 = choose;
+ *          f16 rows need slices of at most 64 KB per CTA);
  *          CE_PATH_STREAM: classes per chunk (multiple of 8; 0 = choose);
  *          ignored otherwise.
  * Returns CE_ERR_PATH when the forced path cannot hold the row in shared

@@ -31,6 +31,7 @@ _lib = None
 
 F32 = 0
 BF16 = 1
+F16 = 2
 
 
 def build(force: bool = False) -> str:
@@ -78,7 +79,9 @@ def _dtype_code(logits: np.ndarray) -> int:
         return F32
     if logits.dtype == np.uint16:  # bf16 bit patterns
         return BF16
-    raise TypeError(f"oracle logits must be float32 or uint16 (bf16 bits), got {logits.dtype}")
+    if logits.dtype == np.float16:
+        return F16
+    raise TypeError(f"oracle logits must be float32, uint16 (bf16 bits) or float16, got {logits.dtype}")
 
 
 def rows(logits: np.ndarray, targets: np.ndarray, row_ids=None, grad: bool = True):

@@ -25,7 +25,7 @@
  *     NaN) and its gradient is softmax/B with no one-hot term;
  *   - 1/B is applied once to the sum of the row losses (the shader divides each
  *     row's loss by B before summing; identical in exact arithmetic);
- *   - bf16 logits are widened exactly to fp64 before any arithmetic.
+ *   - bf16 and f16 logits are widened exactly to fp64 before any arithmetic.
  *
  * Accumulation is in double, in class order within a row and row order for L.
  * Rows are independent and may run on several OpenMP threads; each row's
@@ -41,10 +41,25 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+#define ORACLE_F16 2
 
-/* Widen one element of the logits to double (bf16 -> fp32 is exact). */
+/* IEEE binary16 bits to double, from the format's definition: sign bit,
+ * 5 exponent bits with bias 15, 10 fraction bits; exponent 0 is subnormal
+ * (2^-14 * f/1024), exponent 31 is infinity (f = 0) or NaN. */
+static double oracle_half(uint16_t h) {
+    const int sign = (h >> 15) & 1, e = (h >> 10) & 31, f = h & 1023;
+    double v;
+    if (e == 0) v = ldexp((double)f, -24);
+    else if (e == 31) v = f ? NAN : INFINITY;
+    else v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* Widen one element of the logits to double (bf16 -> fp32 and f16 -> double
+ * are exact). */
 static double oracle_z(const void *logits, int dtype, int64_t i) {
     if (dtype == ORACLE_F32) return (double)((const float *)logits)[i];
+    if (dtype == ORACLE_F16) return oracle_half(((const uint16_t *)logits)[i]);
     uint32_t bits = ((uint32_t)((const uint16_t *)logits)[i]) << 16;
     float f;
     memcpy(&f, &bits, sizeof f);
@@ -99,7 +114,8 @@ void ce_oracle_set_threads(int n) {
 
 /*
  * Per-row losses and (optionally) gradients for a list of rows.
- *   logits   [B][C] row-major, fp32 (dtype 0) or bf16 bit patterns (dtype 1)
+ *   logits   [B][C] row-major, fp32 (dtype 0), bf16 bit patterns (dtype 1) or
+ *            IEEE binary16 bit patterns (dtype 2)
  *   targets  [B] int32
  *   rows     row indices to evaluate (NULL: all rows 0..B-1, nrows must be B)
  *   loss     [nrows] out, l_b of each listed row
@@ -110,7 +126,7 @@ int ce_oracle_rows(const void *logits, int dtype, const int32_t *targets, int64_
                    int64_t C, const int64_t *rows, int64_t nrows, double *loss,
                    double *grad) {
     if (!logits || !targets || !loss || B <= 0 || C <= 0 || nrows < 0) return -1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
     if (!rows && nrows != B) return -1;
     for (int64_t i = 0; i < nrows; ++i)
         if (rows && (rows[i] < 0 || rows[i] >= B)) return -1;
@@ -148,7 +164,7 @@ int ce_oracle_rows_ex(const void *logits, int dtype, const int32_t *targets, int
                       int64_t C, int reduction, const double *upstream, const int64_t *rows,
                       int64_t nrows, double *loss, double *grad) {
     if (!logits || !targets || !loss || B <= 0 || C <= 0 || nrows < 0) return -1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
     if (reduction < 0 || reduction > 2) return -1;
     if (!rows && nrows != B) return -1;
     for (int64_t i = 0; i < nrows; ++i)

@@ -26,6 +26,7 @@ from .build import LIB, build  # noqa: F401
 
 CE_F32 = 0
 CE_BF16 = 1
+CE_F16 = 2
 
 CE_PATH_AUTO = 0
 CE_PATH_ROWS_WARP = 1
@@ -115,7 +116,9 @@ def _dtype_code(t) -> int:
         return CE_F32
     if t.dtype == torch.bfloat16:
         return CE_BF16
-    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+    if t.dtype == torch.float16:
+        return CE_F16
+    raise TypeError(f"logits must be float32, bfloat16 or float16, got {t.dtype}")
 
 
 def _stream_handle(stream) -> int:

@@ -221,9 +221,10 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
         long long n = budget / slot_of(se);
         return (int)(n > ce::kMaxSplitSlots ? ce::kMaxSplitSlots : n);
     };
-    // bf16 slices re-evaluate their exponentials for the gradient, so their
+    // 16-bit slices re-evaluate their exponentials for the gradient, so their
     // per-thread work grows twice as fast with the slice: on 128k-class bf16
-    // rows, 4 CTAs of 64 KB ran faster than 3 of 96 KB, so bf16 stops at 8.
+    // rows, 4 CTAs of 64 KB ran faster than 3 of 96 KB, so bf16 and f16 stop
+    // at 8.
     const int auto_max_vecs = es == 2 ? 8 : 16;
     int K = K_forced;
     if (K == 0) {
@@ -242,6 +243,7 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     const int vecs = vecs_of(se);
     const int nslots = nslots_of(se);
     if (vecs == 0 || nslots < 1) return CE_ERR_PATH;
+    if (dtype == CE_F16 && vecs > 8) return CE_ERR_PATH;  // f16 is built for 8 vectors only
     const long long slot_bytes = slot_of(se);
     const int smem = nslots * (int)slot_bytes;
     // K > 1 with slices of at most 8 vectors per thread: the pipelined kernel
@@ -387,7 +389,7 @@ int check_pointer(const void *p, const DeviceInfo &d) {
 int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
         int reduction, const float *grad_scale, float *loss_out, void *grad_out, void *stream,
         int path, int split) {
-    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_DTYPE;
+    if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_DTYPE;
     if (reduction != CE_REDUCE_MEAN && reduction != CE_REDUCE_SUM && reduction != CE_REDUCE_NONE)
         return CE_ERR_REDUCTION;
     if (!logits || !targets || !loss_out) return CE_ERR_NULL;
@@ -519,7 +521,7 @@ int noalloc_scratch(int dev, unsigned char **out) {
 
 int run_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
                 float *loss_out, void *grad_out, void *stream) {
-    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_DTYPE;
+    if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_DTYPE;
     if (!logits || !targets || !loss_out || !grad_out) return CE_ERR_NULL;
     if (B < 1 || C < 1 || B > 0x7fffffffLL || C > 0x7fffffffLL) return CE_ERR_SHAPE;
     if (B > kNoAllocMaxRows) return CE_ERR_SCRATCH;
@@ -649,7 +651,7 @@ int ce_forward(const void *logits, const int32_t *targets, int64_t B, int64_t C,
 
 int ce_query_plan(int64_t B, int64_t C, int dtype, int *path, int *split, int *ctas,
                   int *threads, int *smem_bytes, int *launches) {
-    if (dtype != CE_F32 && dtype != CE_BF16) return CE_ERR_DTYPE;
+    if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_DTYPE;
     if (B < 1 || C < 1 || B > 0x7fffffffLL || C > 0x7fffffffLL) return CE_ERR_SHAPE;
     Plan pl;
     int rc = make_plan(B, C, dtype, CE_PATH_AUTO, 0, &pl);

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace ce {
@@ -231,6 +232,80 @@ struct Elem<__nv_bfloat16> {
     }
     __device__ __forceinline__ static float max_value(MaxAcc m) {
         return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+    }
+};
+
+template <>
+struct Elem<__half> {
+    static constexpr int kBytes = 2;
+    static constexpr int kVec = 8;
+    static constexpr uint32_t kNegInfWord = 0xfc00fc00u;
+    __device__ __forceinline__ static float widen(uint16_t h) {
+        return __half2float(__ushort_as_half(h));
+    }
+    __device__ __forceinline__ static float load(const unsigned char *p) {
+        return widen(*reinterpret_cast<const uint16_t *>(p));
+    }
+    __device__ __forceinline__ static float load_global(const unsigned char *p) {
+        return widen(__ldg(reinterpret_cast<const unsigned short *>(p)));
+    }
+    __device__ __forceinline__ static float2 widen2(uint32_t w) {
+        __half2 h;
+        *reinterpret_cast<uint32_t *>(&h) = w;
+        return __half22float2(h);  // exact
+    }
+    __device__ __forceinline__ static void unpack(const uint4 &w, float (&v)[8]) {
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = widen2(q[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&v)[8]) {
+        return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]),
+                          pack2(v[6], v[7]));
+    }
+    // The vector as fp32 pairs (elements 2i, 2i+1 in pair i).
+    __device__ __forceinline__ static void unpack2(const uint4 &w, unsigned long long (&v)[4]) {
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = widen2(q[i]);
+            v[i] = f2_pack(f.x, f.y);
+        }
+    }
+    __device__ __forceinline__ static uint32_t pack_pair(unsigned long long v) {
+        float lo, hi;
+        f2_unpack(v, lo, hi);
+        return pack2(lo, hi);
+    }
+    __device__ __forceinline__ static uint4 pack2(const unsigned long long (&v)[4]) {
+        return make_uint4(pack_pair(v[0]), pack_pair(v[1]), pack_pair(v[2]), pack_pair(v[3]));
+    }
+    __device__ __forceinline__ static void store(unsigned char *p, float v) {
+        *reinterpret_cast<__half *>(p) = __float2half_rn(v);
+    }
+    // Running max over 16-byte vectors on packed f16 pairs (exact: the
+    // widening is monotonic); one max.f16x2 per 4 elements.
+    using MaxAcc = uint32_t;
+    __device__ __forceinline__ static uint32_t max2(uint32_t a, uint32_t b) {
+        uint32_t d;
+        asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    __device__ __forceinline__ static MaxAcc max_init() { return kNegInfWord; }
+    __device__ __forceinline__ static void max_step(MaxAcc &m, const uint4 &w) {
+        m = max2(m, max2(max2(w.x, w.y), max2(w.z, w.w)));
+    }
+    __device__ __forceinline__ static float max_value(MaxAcc m) {
+        const float2 f = widen2(m);
+        return fmaxf(f.x, f.y);
     }
 };
 

@@ -76,12 +76,13 @@ __device__ __forceinline__ void exps_of(const uint4 &xv, unsigned long long (&e2
 // Element d of a 16-byte vector, widened to fp32 (selects, no indexing).
 template <typename E>
 __device__ __forceinline__ float element_of(const uint4 &w, int d) {
-    if (E::kVec == 4) {
+    if constexpr (E::kVec == 4) {
         const uint32_t q = (d & 2) ? ((d & 1) ? w.w : w.z) : ((d & 1) ? w.y : w.x);
         return __uint_as_float(q);
+    } else {
+        const uint32_t q = (d & 4) ? ((d & 2) ? w.w : w.z) : ((d & 2) ? w.y : w.x);
+        return E::widen((uint16_t)((d & 1) ? (q >> 16) : (q & 0xffffu)));
     }
-    const uint32_t q = (d & 4) ? ((d & 2) ? w.w : w.z) : ((d & 2) ? w.y : w.x);
-    return __uint_as_float((d & 1) ? (q & 0xffff0000u) : (q << 16));
 }
 
 template <typename T, int K, int NT, int VPT, typename P>
@@ -559,11 +560,13 @@ cudaError_t max_clusters_t(int K, int smem, int *clusters) {
 cudaError_t launch_split_pipe(const ParamsEx &p, int dtype, int K, int ctas, int nslots,
                               int slot_bytes, long long slice_elems, int smem, cudaStream_t s) {
     if (dtype == 0) return launch_t<float>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);
+    if (dtype == 2) return launch_t<__half>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);
     return launch_t<__nv_bfloat16>(p, K, ctas, nslots, slot_bytes, slice_elems, smem, s);
 }
 
 cudaError_t split_pipe_max_clusters(int dtype, int K, int smem, int *clusters) {
     if (dtype == 0) return max_clusters_t<float>(K, smem, clusters);
+    if (dtype == 2) return max_clusters_t<__half>(K, smem, clusters);
     return max_clusters_t<__nv_bfloat16>(K, smem, clusters);
 }
 

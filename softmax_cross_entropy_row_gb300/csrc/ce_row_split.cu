@@ -26,6 +26,8 @@
 // fixed order (Pass 2, fused into the same launch).
 #include <math.h>
 
+#include <type_traits>
+
 #include "ce_launch.h"
 
 namespace ce {
@@ -541,21 +543,33 @@ cudaError_t max_clusters_v(int K, int smem, int *clusters) {
     }
 }
 
+// f16 rows are built for slices of 8 vectors per thread only (the planner
+// keeps 16-bit rows there, as for bf16).
 template <typename T>
 cudaError_t launch_t(const ParamsEx &p, int K, int vecs, int ctas, int nslots, int slot_bytes,
                      long long se, int smem, int staged, cudaStream_t s) {
-    if (vecs == 16) return launch_v<T, 16>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
-    if (vecs == 12) return launch_v<T, 12>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
-    if (vecs == 8) return launch_v<T, 8>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
-    return cudaErrorInvalidValue;
+    if constexpr (std::is_same<T, __half>::value) {
+        if (vecs != 8) return cudaErrorInvalidValue;
+        return launch_v<T, 8>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
+    } else {
+        if (vecs == 16) return launch_v<T, 16>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
+        if (vecs == 12) return launch_v<T, 12>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
+        if (vecs == 8) return launch_v<T, 8>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
+        return cudaErrorInvalidValue;
+    }
 }
 
 template <typename T>
 cudaError_t max_clusters_t(int K, int vecs, int smem, int *clusters) {
-    if (vecs == 16) return max_clusters_v<T, 16>(K, smem, clusters);
-    if (vecs == 12) return max_clusters_v<T, 12>(K, smem, clusters);
-    if (vecs == 8) return max_clusters_v<T, 8>(K, smem, clusters);
-    return cudaErrorInvalidValue;
+    if constexpr (std::is_same<T, __half>::value) {
+        if (vecs != 8) return cudaErrorInvalidValue;
+        return max_clusters_v<T, 8>(K, smem, clusters);
+    } else {
+        if (vecs == 16) return max_clusters_v<T, 16>(K, smem, clusters);
+        if (vecs == 12) return max_clusters_v<T, 12>(K, smem, clusters);
+        if (vecs == 8) return max_clusters_v<T, 8>(K, smem, clusters);
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -565,12 +579,15 @@ cudaError_t launch_split(const ParamsEx &p, int dtype, int K, int vecs, int ctas
                          cudaStream_t s) {
     if (dtype == 0)
         return launch_t<float>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem, staged, s);
+    if (dtype == 2)
+        return launch_t<__half>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem, staged, s);
     return launch_t<__nv_bfloat16>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem,
                                    staged, s);
 }
 
 cudaError_t split_max_clusters(int dtype, int K, int vecs, int smem, int *clusters) {
     if (dtype == 0) return max_clusters_t<float>(K, vecs, smem, clusters);
+    if (dtype == 2) return max_clusters_t<__half>(K, vecs, smem, clusters);
     return max_clusters_t<__nv_bfloat16>(K, vecs, smem, clusters);
 }
 

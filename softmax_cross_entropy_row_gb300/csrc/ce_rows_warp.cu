@@ -380,11 +380,14 @@ cudaError_t launch_rows_warp(const ParamsEx &p, int dtype, int per_sm, int ctas,
                              int rows_per_tile, int slot_bytes, int smem, cudaStream_t s) {
     if (dtype == 0)
         return launch_t<float>(p, per_sm, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+    if (dtype == 2)
+        return launch_t<__half>(p, per_sm, ctas, slots, rows_per_tile, slot_bytes, smem, s);
     return launch_t<__nv_bfloat16>(p, per_sm, ctas, slots, rows_per_tile, slot_bytes, smem, s);
 }
 
 cudaError_t rows_warp_max_ctas_per_sm(int dtype, int per_sm, long long C, int smem, int *ctas) {
     if (dtype == 0) return occ_t<float>(per_sm, C, smem, ctas);
+    if (dtype == 2) return occ_t<__half>(per_sm, C, smem, ctas);
     return occ_t<__nv_bfloat16>(per_sm, C, smem, ctas);
 }
 

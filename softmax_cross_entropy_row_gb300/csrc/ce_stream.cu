@@ -148,6 +148,7 @@ cudaError_t launch_t(const ParamsEx &p, long long chunks, cudaStream_t s) {
 
 cudaError_t launch_stream(const ParamsEx &p, int dtype, long long chunks, cudaStream_t s) {
     if (dtype == 0) return launch_t<float>(p, chunks, s);
+    if (dtype == 2) return launch_t<__half>(p, chunks, s);
     return launch_t<__nv_bfloat16>(p, chunks, s);
 }
 

@@ -5,9 +5,10 @@ at the tolerances the method's targets state:
   fp32 logits:  |L - L_ref| <= 1e-5 |L_ref| (+1e-7 for L near 0)
                 |g - g_ref| <= 1e-6 / B per element
                 |sum_c g|   <= 1e-6 / B per row
-  bf16 logits:  the same loss bound, against the oracle run on the bf16 values;
-                |g - g_ref| <= 1 bf16 ulp of g_ref (0 allowed for |g_ref| < 2^-126,
-                the kernels flush subnormal fp32 results)
+  bf16 / f16 logits:  the same loss bound, against the oracle run on the
+                16-bit values;
+                |g - g_ref| <= 1 ulp of g_ref in the logits' type (0 allowed for
+                |g_ref| < 2^-126, the kernels flush subnormal fp32 results)
                 |sum_c g|   <= 1e-6 / B + sum_c ulp(g_c) / 2 per row (the bf16
                 rounding of each element; checked on the fp32 path exactly)
 """
@@ -61,6 +62,13 @@ def ulp_bf16(x: np.ndarray) -> np.ndarray:
     return np.exp2(e - 7)
 
 
+def ulp_f16(x: np.ndarray) -> np.ndarray:
+    """Spacing of IEEE binary16 values in x's binade (2^-24 below 2^-14)."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -14)))
+    return np.exp2(e - 10)
+
+
 def check_loss(L: float, L_ref: float) -> None:
     if np.isnan(L_ref):
         assert np.isnan(L), f"loss {L}, expected NaN"
@@ -83,7 +91,8 @@ def check_grad(g: np.ndarray, g_ref: np.ndarray, B: int, dtype: str, what: str =
         rs = np.abs(g.sum(axis=1) - target_sum) * B
         assert float(rs.max()) <= ROWSUM_ATOL_TIMES_B, f"{what}: row sum {float(rs.max()):.3g}/B"
     else:
-        tol = ulp_bf16(g_ref)
+        ulp = ulp_f16 if dtype == "f16" else ulp_bf16
+        tol = ulp(g_ref)
         flushed = (g == 0) & (np.abs(g_ref) < 2.0 ** -126)
         bad = (np.abs(g - g_ref) > tol) & ~flushed
         if bad.any():
@@ -91,8 +100,8 @@ def check_grad(g: np.ndarray, g_ref: np.ndarray, B: int, dtype: str, what: str =
             raise AssertionError(f"{what}: {int(bad.sum())} bf16 grads beyond 1 ulp, first at "
                                  f"{tuple(i)}: {g[tuple(i)]!r} vs {g_ref[tuple(i)]!r}")
         rs = np.abs(g.sum(axis=1) - target_sum)
-        bound = ROWSUM_ATOL_TIMES_B / B + 0.5 * ulp_bf16(g).sum(axis=1)
-        assert np.all(rs <= bound), f"{what}: bf16 row sum beyond its rounding bound"
+        bound = ROWSUM_ATOL_TIMES_B / B + 0.5 * ulp(g).sum(axis=1)
+        assert np.all(rs <= bound), f"{what}: {dtype} row sum beyond its rounding bound"
 
 
 def check_full(inp, loss, grad, what: str = "") -> None:

@@ -116,6 +116,35 @@ def test_many_rows_per_cluster():
     check_full(inp, loss, grad, "warp ring wrap")
 
 
+# ------------------------------------------------------------ f16 logits
+
+F16_CASES = [(WARP, 0, 300, 1000), (WARP, 0, 7, 4095), (SPLIT, 1, 5, 20000), (SPLIT, 1, 3, 32000),
+             (SPLIT, 2, 4, 50257), (SPLIT, 4, 6, 128256), (SPLIT, 8, 2, 250000),
+             (STREAM, 0, 3, 10000), (AUTO, 0, 4, 600000)]
+
+
+@pytest.mark.parametrize("path,split,B,C", F16_CASES)
+def test_f16_logits(path, split, B, C):
+    """IEEE binary16 logits on every path: loss to the fp32 bound, gradient
+    within 1 f16 ulp of the oracle run on the f16 values."""
+    inp = _case(B, C, "f16", seed=B + C, sigma=3.0)
+    z, t = device_inputs(inp)
+    assert z.dtype == torch.float16
+    loss, grad = run(z, t, path, split)
+    torch.cuda.synchronize()
+    assert grad.dtype == torch.float16
+    check_full(inp, loss, grad, f"f16 path {path} K={split} {B}x{C}")
+
+
+def test_f16_refuses_slices_beyond_64kb():
+    """f16 rows are built for slices of at most 8 vectors per thread."""
+    inp = _case(2, 40000, "f16", seed=1)
+    z, t = device_inputs(inp)
+    with pytest.raises(ce.CEError) as ei:
+        run(z, t, SPLIT, 1)
+    assert ei.value.status == 9
+
+
 # ------------------------------------------------------ pointer alignment
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -334,5 +363,5 @@ def test_error_codes_on_device_pointers():
     assert raw(z.data_ptr(), t.data_ptr(), 4, 8, 0, loss.data_ptr(), grad.data_ptr()) == 0
     assert raw(z.data_ptr(), t.data_ptr(), 4, 8, 0, loss.data_ptr(), z.data_ptr()) == 6
     assert raw(z.data_ptr() + 2, t.data_ptr(), 4, 8, 0, loss.data_ptr(), grad.data_ptr()) == 4
-    assert raw(z.data_ptr(), t.data_ptr(), 4, 8, 2, loss.data_ptr(), grad.data_ptr()) == 3
+    assert raw(z.data_ptr(), t.data_ptr(), 4, 8, 7, loss.data_ptr(), grad.data_ptr()) == 3
     torch.cuda.synchronize()

@@ -75,10 +75,10 @@ def _check(inp, reduction, loss, grad, u, what):
         eff_b = B if reduction == MEAN else 1
         check_grad(g / scale[:, None], g_ref / scale[:, None], eff_b, "f32", what)
     else:
-        check_grad(g, g_ref, B, "bf16", what)
+        check_grad(g, g_ref, B, inp.workload.dtype, what)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("reduction", [MEAN, SUM, NONE])
 @pytest.mark.parametrize("path,split,B,C", PATHS)
 @pytest.mark.parametrize("with_grad", [True, False])

@@ -338,3 +338,18 @@ def test_reduction_relations(oracle_mod):
         oracle_mod.rows_ex(inp.logits, inp.targets, 3)
     with pytest.raises(ValueError):
         oracle_mod.rows_ex(inp.logits, inp.targets, oracle_mod.NONE, upstream=1.0)
+
+
+def test_f16_widening_is_exact(oracle_mod):
+    """IEEE binary16 bit patterns mean what numpy's float16 says they mean
+    (normal, subnormal, the largest finite value, signed zero)."""
+    bits = np.array([[0x3C00, 0x4000, 0xBC00, 0x3555, 0x7BFF, 0x0001, 0x0400, 0x8000]],
+                    dtype=np.uint16)
+    z16 = bits.view(np.float16)
+    t = np.array([0], dtype=np.int32)
+    l16, g16 = oracle_mod.rows(z16, t)
+    z64 = z16.astype(np.float64)
+    assert z64[0, 4] == 65504.0 and z64[0, 5] == 2.0 ** -24 and z64[0, 6] == 2.0 ** -14
+    # the same row as fp32 values (exactly representable) gives the same fp64 results
+    l32, g32 = oracle_mod.rows(z64.astype(np.float32), t)
+    assert np.array_equal(l16, l32) and np.array_equal(g16, g32)

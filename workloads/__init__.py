@@ -22,8 +22,9 @@ import numpy as np
 # Element-type codes shared with the C-ABI (``ce_dtype``) and the oracle.
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
-DTYPE_CODES = {"f32": DTYPE_F32, "bf16": DTYPE_BF16}
-ELEM_BYTES = {"f32": 4, "bf16": 2}
+DTYPE_F16 = 2
+DTYPE_CODES = {"f32": DTYPE_F32, "bf16": DTYPE_BF16, "f16": DTYPE_F16}
+ELEM_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
 
 _ROWS_PER_CHUNK = 256
 
@@ -157,6 +158,8 @@ class Inputs:
         z = self.logits if rows is None else self.logits[rows]
         if self.workload.dtype == "bf16":
             return bf16_bits_to_f32(z)
+        if self.workload.dtype == "f16":
+            return z.astype(np.float32)
         return z
 
 
@@ -181,7 +184,8 @@ def make_inputs(w: Workload) -> Inputs:
             z[spike_rows, spike_cols] = np.float32(w.spike)
         order = np.argsort(spike_rows)
         spike_rows, spike_cols = spike_rows[order], spike_cols[order]
-    logits = f32_to_bf16_bits(z) if w.dtype == "bf16" else z
+    logits = (f32_to_bf16_bits(z) if w.dtype == "bf16"
+              else z.astype(np.float16) if w.dtype == "f16" else z)
     return Inputs(w, logits, t, uniform_rows, spike_rows, spike_cols)
 
 
@@ -195,6 +199,7 @@ def random_case(B: int, C: int, dtype: str, seed: int, sigma: float = 1.0,
     else:
         g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0xBAD])))
         t = g.integers(target_range[0], target_range[1], size=B, dtype=np.int32)
-    logits = f32_to_bf16_bits(z) if dtype == "bf16" else z
+    logits = (f32_to_bf16_bits(z) if dtype == "bf16"
+              else z.astype(np.float16) if dtype == "f16" else z)  # f16: numpy's RNE narrowing
     empty = np.zeros(0, dtype=np.int64)
     return Inputs(w, logits, t, empty, empty, empty)
