@@ -46,6 +46,7 @@ METRIC = "fused CE fwd+grad rows/s and achieved HBM GB/s vs ~8 TB/s roofline (1Ã
 HEADLINE = "classifier_4096x1000_f32"
 FALLBACK_HBM_GBS = 6800.0
 TARGET_REGION_S = 1.5      # timed work per workload when --steps is not given
+HOLD_CYCLES = 400_000      # device-side wait (~0.2 ms) queued ahead of each timed region
 CPU_SAMPLE_S = 10.0
 MAX_SETS = 64              # a workload this small stays L2-resident (said in the output)
 
@@ -266,6 +267,9 @@ def bench_workload(w, inp, steps, warmup, device, l2_bytes, hbm_peak, peak_note,
         torch.cuda.synchronize(device)
         sampler = ClockSampler(sampler_gpu)
         with sampler:
+            # keep the stream busy while the host submits the timed graphs, so
+            # that the start event does not wait on host launch latency
+            torch.cuda._sleep(HOLD_CYCLES)
             e0.record(s)
             for _ in range(replays):
                 graph.replay()
@@ -357,11 +361,20 @@ NEXT_ROWS = [("f16_logits", "lm_head_8192x32000_f16", "plain"),
              ("loss_only_mean", "classifier_4096x1000_f32", "forward"),
              ("loss_only_mean", "lm_head_8192x32000_bf16", "forward"),
              ("sum_scalar_upstream", "classifier_4096x1000_f32", "sum"),
-             ("none_per_row_upstream", "classifier_4096x1000_f32", "none")]
+             ("none_per_row_upstream", "classifier_4096x1000_f32", "none"),
+             ("softmax_forward", "lm_head_8192x32000_bf16", "softmax_fwd"),
+             ("softmax_forward", "classifier_4096x1000_f32", "softmax_fwd"),
+             ("softmax_backward", "lm_head_8192x32000_bf16", "softmax_bwd"),
+             ("softmax_backward", "classifier_4096x1000_f32", "softmax_bwd")]
 
 
 def next_row_bytes(w, kind):
-    read = w.B * w.C * w.elem_bytes + 4 * w.B
+    n = w.B * w.C * w.elem_bytes
+    if kind == "softmax_fwd":  # z in, p out
+        return 2 * n
+    if kind == "softmax_bwd":  # p and dy in, dx out
+        return 3 * n
+    read = n + 4 * w.B
     if kind == "plain":
         return w.min_bytes
     if kind == "forward":
@@ -385,17 +398,27 @@ def bench_next_row(label, w, inp, kind, device, l2_bytes, hbm_peak):
     for i in range(nsets):
         z = z0 if i == 0 else z0.clone()
         grad = None if kind == "forward" else torch.empty_like(z)
+        if kind == "softmax_bwd":  # (p, dy, -, dx, -): probabilities, an upstream gradient
+            probs = torch.empty_like(z)
+            ce.ce_softmax_fwd(z, probs)
+            dy = torch.empty_like(z).normal_() if i == 0 else sets[0][1].clone()
+            sets.append((probs, dy, None, torch.empty_like(z), None))
+            continue
         loss = torch.empty(w.B if kind == "none" else 1, dtype=torch.float32, device=device)
         up = (torch.linspace(0.5, 1.5, w.B, device=device) if kind == "none"
               else torch.full((1,), 0.5, device=device) if kind == "sum" else None)
         sets.append((z, t0, loss, grad, up))
-    red = {"forward": ce.CE_REDUCE_MEAN, "sum": ce.CE_REDUCE_SUM, "none": ce.CE_REDUCE_NONE,
-           "plain": ce.CE_REDUCE_MEAN}[kind]
+    red = {"forward": ce.CE_REDUCE_MEAN, "sum": ce.CE_REDUCE_SUM, "none": ce.CE_REDUCE_NONE
+           }.get(kind, ce.CE_REDUCE_MEAN)
     s = torch.cuda.Stream(device)
 
     def call(i):
         z, t, loss, grad, up = sets[i % nsets]
-        if kind == "forward":
+        if kind == "softmax_fwd":
+            ce.ce_softmax_fwd(z, grad, s)
+        elif kind == "softmax_bwd":
+            ce.ce_softmax_bwd(z, t, grad, s)  # (p, dy, dx)
+        elif kind == "forward":
             ce.ce_forward(z, t, loss, red, s)
         elif kind == "plain":
             ce.ce_fwd_bwd(z, t, loss, grad, s)
@@ -544,6 +567,9 @@ def main():
         "config": {"workload": w.name, "B": w.B, "C": w.C, "logits_dtype": w.dtype,
                    "l2": l2_note(head, w, l2_bytes),
                    "launch": "CUDA graph replay, one ce_fwd_bwd per step",
+                   "timing": ("CUDA events on the launching stream; a device-side wait is "
+                              "queued before the start event so that host submission "
+                              "latency stays outside the timed region"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
         "cpu_baseline": cpu,

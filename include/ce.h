@@ -156,6 +156,36 @@ int ce_forward(const void *logits, const int32_t *targets, int64_t B, int64_t C,
                int reduction, float *loss_out, void *stream);
 
 /*
+ * ce_softmax_fwd -- the row-wise softmax forward of the rumus project page
+ * (milestone M8c: row-wise softmax with log-sum-exp stability, forward and
+ * backward kernels):
+ *   probs_out[b][c] = exp(z[b][c] - m_b) / sum_c' exp(z[b][c'] - m_b)
+ * computed by the same kernels as the loss (Steps 1, 2 and 4 of Pass 1 of the
+ * cross_entropy.wgsl source page, with no target and no 1/B), written once
+ * in the logits' dtype.  logits and probs_out: device, [B][C] row-major,
+ * `dtype`, not overlapping.  Asynchronous on `stream`; returns a ce_status.
+ */
+int ce_softmax_fwd(const void *logits, int64_t B, int64_t C, int dtype, void *probs_out,
+                   void *stream);
+
+/* ce_softmax_fwd on a forced path and split, as for ce_fwd_bwd_path. */
+int ce_softmax_fwd_path(const void *logits, int64_t B, int64_t C, int dtype, void *probs_out,
+                        void *stream, int path, int split);
+
+/*
+ * ce_softmax_bwd -- the row-wise softmax backward of the same milestone (M8c):
+ *   dx[b][c] = p[b][c] * (dy[b][c] - sum_c' p[b][c'] dy[b][c'])
+ * for probabilities p (the forward's output) and the upstream gradient dy,
+ * all device [B][C] row-major in `dtype`; the row's dot product is formed in
+ * fp32 in a fixed order.  dx may be p or dy itself (in place) but may not
+ * overlap them otherwise.  Rows whose bytes are a multiple of 16 and at most
+ * 64 KB, with 16-byte aligned tensors, read p and dy once; other rows read
+ * them twice.  Asynchronous on `stream`; returns a ce_status.
+ */
+int ce_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int dtype,
+                   void *dx_out, void *stream);
+
+/*
  * ce_query_plan -- the launch that ce_fwd_bwd would make for this shape on
  * the current device (path, split, total CTAs, threads per CTA, dynamic shared
  * memory per CTA, kernel launches per call).  Any output pointer may be NULL.

@@ -63,6 +63,10 @@ def _load():
             lib.ce_oracle_rows_ex.restype = ctypes.c_int
             lib.ce_oracle_reduce.argtypes = [vp, i64, ctypes.c_int]
             lib.ce_oracle_reduce.restype = ctypes.c_double
+            lib.ce_oracle_softmax.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, vp]
+            lib.ce_oracle_softmax.restype = ctypes.c_int
+            lib.ce_oracle_softmax_bwd.argtypes = [vp, vp, ctypes.c_int, i64, i64, vp, i64, vp]
+            lib.ce_oracle_softmax_bwd.restype = ctypes.c_int
             lib.ce_oracle_batch_loss.restype = ctypes.c_double
             lib.ce_oracle_fwd_bwd.argtypes = [vp, ctypes.c_int, vp, i64, i64, vp, vp, vp]
             lib.ce_oracle_fwd_bwd.restype = ctypes.c_int
@@ -150,6 +154,42 @@ def reduce(loss_rows: np.ndarray, reduction: int) -> float:
     """Pass 2 for MEAN ((sum l_b) / B) or SUM (sum l_b), in row order, fp64."""
     lr = np.ascontiguousarray(loss_rows, dtype=np.float64)
     return float(_load().ce_oracle_reduce(lr.ctypes.data, lr.size, int(reduction)))
+
+
+def _row_ids(B, row_ids):
+    if row_ids is None:
+        return None, B, None
+    ids = np.ascontiguousarray(row_ids, dtype=np.int64)
+    return ids.ctypes.data, ids.size, ids
+
+
+def softmax(logits: np.ndarray, row_ids=None) -> np.ndarray:
+    """Row-wise softmax in fp64 ([B, C] or the listed rows)."""
+    lib = _load()
+    logits = np.ascontiguousarray(logits)
+    B, C = logits.shape
+    ptr, n, keep = _row_ids(B, row_ids)
+    out = np.empty((n, C), dtype=np.float64)
+    if lib.ce_oracle_softmax(logits.ctypes.data, _dtype_code(logits), B, C, ptr, n,
+                             out.ctypes.data) != 0:
+        raise ValueError("ce_oracle_softmax rejected its arguments")
+    return out
+
+
+def softmax_bwd(probs: np.ndarray, dy: np.ndarray, row_ids=None) -> np.ndarray:
+    """dx = p * (dy - sum(p * dy)) per row in fp64; p and dy of one element type."""
+    lib = _load()
+    probs = np.ascontiguousarray(probs)
+    dy = np.ascontiguousarray(dy)
+    if probs.shape != dy.shape or probs.dtype != dy.dtype:
+        raise ValueError("probs and dy must have one shape and element type")
+    B, C = probs.shape
+    ptr, n, keep = _row_ids(B, row_ids)
+    out = np.empty((n, C), dtype=np.float64)
+    if lib.ce_oracle_softmax_bwd(probs.ctypes.data, dy.ctypes.data, _dtype_code(probs), B, C,
+                                 ptr, n, out.ctypes.data) != 0:
+        raise ValueError("ce_oracle_softmax_bwd rejected its arguments")
+    return out
 
 
 def batch_loss(loss_rows: np.ndarray) -> float:

@@ -189,6 +189,57 @@ double ce_oracle_reduce(const double *loss_rows, int64_t B, int reduction) {
     return reduction == 0 ? s / (double)B : s;
 }
 
+/*
+ * Row-wise softmax, forward and backward (rumus project page, milestone M8c:
+ * row-wise softmax with log-sum-exp stability, forward and backward kernels).
+ *   forward   p[b][c] = exp(z[b][c] - m_b) / sum_c' exp(z[b][c'] - m_b)
+ *   backward  dx[b][c] = p[b][c] * (dy[b][c] - sum_c' p[b][c'] dy[b][c'])
+ * in fp64, inputs widened exactly from `dtype`; `rows` as in ce_oracle_rows;
+ * out is [nrows][C].  Returns 0, or -1 on a bad argument.
+ */
+int ce_oracle_softmax(const void *logits, int dtype, int64_t B, int64_t C, const int64_t *rows,
+                      int64_t nrows, double *out) {
+    if (!logits || !out || B <= 0 || C <= 0 || nrows < 0) return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
+    if (!rows && nrows != B) return -1;
+    for (int64_t i = 0; i < nrows; ++i)
+        if (rows && (rows[i] < 0 || rows[i] >= B)) return -1;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t row_start = (rows ? rows[i] : i) * C;
+        double m = -INFINITY;
+        for (int64_t c = 0; c < C; ++c) {
+            double z = oracle_z(logits, dtype, row_start + c);
+            if (z > m) m = z;
+        }
+        double s = 0.0;
+        for (int64_t c = 0; c < C; ++c) s += exp(oracle_z(logits, dtype, row_start + c) - m);
+        for (int64_t c = 0; c < C; ++c)
+            out[i * C + c] = exp(oracle_z(logits, dtype, row_start + c) - m) / s;
+    }
+    return 0;
+}
+
+int ce_oracle_softmax_bwd(const void *probs, const void *dy, int dtype, int64_t B, int64_t C,
+                          const int64_t *rows, int64_t nrows, double *out) {
+    if (!probs || !dy || !out || B <= 0 || C <= 0 || nrows < 0) return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
+    if (!rows && nrows != B) return -1;
+    for (int64_t i = 0; i < nrows; ++i)
+        if (rows && (rows[i] < 0 || rows[i] >= B)) return -1;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int64_t row_start = (rows ? rows[i] : i) * C;
+        double dot = 0.0;
+        for (int64_t c = 0; c < C; ++c)
+            dot += oracle_z(probs, dtype, row_start + c) * oracle_z(dy, dtype, row_start + c);
+        for (int64_t c = 0; c < C; ++c)
+            out[i * C + c] = oracle_z(probs, dtype, row_start + c) *
+                             (oracle_z(dy, dtype, row_start + c) - dot);
+    }
+    return 0;
+}
+
 /* Narrow a double to fp32 and then to bf16 (round to nearest even each time). */
 static uint16_t oracle_to_bf16(double v) {
     float f = (float)v;

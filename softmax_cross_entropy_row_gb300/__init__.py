@@ -47,7 +47,8 @@ STATUS = {0: "CE_OK", 1: "CE_ERR_NULL", 2: "CE_ERR_SHAPE", 3: "CE_ERR_DTYPE",
 # Symbols declared in include/ce.h.
 EXPORTS = ("ce_fwd_bwd", "ce_fwd_bwd_path", "ce_query_plan", "ce_get_device_errors",
            "ce_release_workspaces", "ce_status_string", "ce_last_cuda_error",
-           "ce_fwd_bwd_noalloc", "ce_fwd_bwd_ex", "ce_fwd_bwd_ex_path", "ce_forward")
+           "ce_fwd_bwd_noalloc", "ce_fwd_bwd_ex", "ce_fwd_bwd_ex_path", "ce_forward",
+           "ce_softmax_fwd", "ce_softmax_fwd_path", "ce_softmax_bwd")
 
 
 class CEError(RuntimeError):
@@ -95,6 +96,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.ce_fwd_bwd_ex_path.restype = ci
     lib.ce_forward.argtypes = [vp, vp, i64, i64, ci, ci, vp, vp]
     lib.ce_forward.restype = ci
+    lib.ce_softmax_fwd.argtypes = [vp, i64, i64, ci, vp, vp]
+    lib.ce_softmax_fwd.restype = ci
+    lib.ce_softmax_fwd_path.argtypes = [vp, i64, i64, ci, vp, vp, ci, ci]
+    lib.ce_softmax_fwd_path.restype = ci
+    lib.ce_softmax_bwd.argtypes = [vp, vp, i64, i64, ci, vp, vp]
+    lib.ce_softmax_bwd.restype = ci
     if path is None:
         _lib = lib
     return lib
@@ -187,6 +194,30 @@ def ce_forward(logits, targets, loss_out, reduction=CE_REDUCE_MEAN, stream=None)
     B, C = logits.shape
     _check(lib.ce_forward(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
                           int(reduction), _ptr(loss_out), _stream_handle(stream)))
+
+
+def ce_softmax_fwd(logits, probs_out, stream=None, path=CE_PATH_AUTO, split=0) -> None:
+    """Row-wise softmax of a contiguous [B, C] tensor into ``probs_out`` (same
+    shape and dtype); ``path`` / ``split`` force a kernel as for ce_fwd_bwd_path."""
+    lib = load_library()
+    if logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous [B, C] tensor")
+    if probs_out.shape != logits.shape or probs_out.dtype != logits.dtype or not probs_out.is_contiguous():
+        raise ValueError("probs_out must be a contiguous tensor of the logits' shape and dtype")
+    B, C = logits.shape
+    _check(lib.ce_softmax_fwd_path(_ptr(logits), B, C, _dtype_code(logits), _ptr(probs_out),
+                                   _stream_handle(stream), int(path), int(split)))
+
+
+def ce_softmax_bwd(probs, dy, dx_out, stream=None) -> None:
+    """dx = p * (dy - sum(p * dy, row)) for contiguous [B, C] tensors of one dtype."""
+    lib = load_library()
+    for name, t in (("probs", probs), ("dy", dy), ("dx_out", dx_out)):
+        if t.dim() != 2 or not t.is_contiguous() or t.shape != probs.shape or t.dtype != probs.dtype:
+            raise ValueError(f"{name} must be a contiguous tensor of the probabilities' shape and dtype")
+    B, C = probs.shape
+    _check(lib.ce_softmax_bwd(_ptr(probs), _ptr(dy), B, C, _dtype_code(probs), _ptr(dx_out),
+                              _stream_handle(stream)))
 
 
 def ce_fwd_bwd_raw(logits_ptr: int, targets_ptr: int, B: int, C: int, dtype: int,

@@ -386,13 +386,22 @@ int check_pointer(const void *p, const DeviceInfo &d) {
 
 // grad_out == nullptr: loss only.  grad_scale: nullptr, one fp32 (mean,
 // sum) or [B] fp32 (none).  loss_out: one fp32 (mean, sum) or [B] (none).
+// softmax: the row softmax forward -- no targets and no loss; grad_out
+// receives softmax(z_b).
 int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
         int reduction, const float *grad_scale, float *loss_out, void *grad_out, void *stream,
-        int path, int split) {
+        int path, int split, bool softmax = false) {
     if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_DTYPE;
+    if (softmax) {
+        if (!logits || !grad_out) return CE_ERR_NULL;
+        targets = nullptr;
+        loss_out = nullptr;
+        grad_scale = nullptr;
+        reduction = CE_REDUCE_NONE;
+    }
     if (reduction != CE_REDUCE_MEAN && reduction != CE_REDUCE_SUM && reduction != CE_REDUCE_NONE)
         return CE_ERR_REDUCTION;
-    if (!logits || !targets || !loss_out) return CE_ERR_NULL;
+    if (!softmax && (!logits || !targets || !loss_out)) return CE_ERR_NULL;
     if (B < 1 || C < 1 || B > 0x7fffffffLL || C > 0x7fffffffLL) return CE_ERR_SHAPE;
     const int es = dtype == CE_F32 ? 4 : 2;
     if ((unsigned long long)B * (unsigned long long)C > (1ull << 61) / (unsigned)es)
@@ -405,13 +414,18 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     if (lz % es || gz % es || tz % 4 || oz % 4 || sz % 4) return CE_ERR_ALIGN;
     const size_t nbytes = (size_t)B * (size_t)C * es;
     const size_t per_row = reduction == CE_REDUCE_NONE ? (size_t)B * 4 : 4;  // loss_out, grad_scale
-    if (grad_out &&
-        (ranges_overlap(gz, nbytes, lz, nbytes) || ranges_overlap(gz, nbytes, tz, (size_t)B * 4) ||
-         ranges_overlap(gz, nbytes, oz, per_row) || (grad_scale && ranges_overlap(gz, nbytes, sz, per_row))))
-        return CE_ERR_OVERLAP;
-    if (ranges_overlap(oz, per_row, lz, nbytes) || ranges_overlap(oz, per_row, tz, (size_t)B * 4) ||
-        (grad_scale && ranges_overlap(oz, per_row, sz, per_row)))
-        return CE_ERR_OVERLAP;
+    if (softmax) {
+        if (ranges_overlap(gz, nbytes, lz, nbytes)) return CE_ERR_OVERLAP;
+    } else {
+        if (grad_out && (ranges_overlap(gz, nbytes, lz, nbytes) ||
+                         ranges_overlap(gz, nbytes, tz, (size_t)B * 4) ||
+                         ranges_overlap(gz, nbytes, oz, per_row) ||
+                         (grad_scale && ranges_overlap(gz, nbytes, sz, per_row))))
+            return CE_ERR_OVERLAP;
+        if (ranges_overlap(oz, per_row, lz, nbytes) || ranges_overlap(oz, per_row, tz, (size_t)B * 4) ||
+            (grad_scale && ranges_overlap(oz, per_row, sz, per_row)))
+            return CE_ERR_OVERLAP;
+    }
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -463,6 +477,7 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     p.grad_base = reduction == CE_REDUCE_MEAN ? p.inv_b : 1.f;
     p.grad_scale = grad_scale;
     p.scale_per_row = grad_scale != nullptr && reduction == CE_REDUCE_NONE;
+    p.softmax = softmax ? 1 : 0;
 
     switch (pl.path) {
         case CE_PATH_ROWS_WARP:
@@ -581,6 +596,7 @@ int run_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C
     p.grad_base = p.inv_b;
     p.grad_scale = nullptr;
     p.scale_per_row = 0;
+    p.softmax = 0;
 
     if (pl.path == CE_PATH_ROWS_WARP)
         e = ce::launch_rows_warp(p, dtype, pl.per_sm, pl.ctas, pl.nslots, pl.rows_per_tile,
@@ -613,7 +629,63 @@ cudaError_t ensure_smem_attr(const void *func, int smem) {
 
 }  // namespace ce
 
+namespace {
+
+int run_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int dtype,
+                    void *dx_out, void *stream) {
+    if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_DTYPE;
+    if (!probs || !dy || !dx_out) return CE_ERR_NULL;
+    if (B < 1 || C < 1 || B > 0x7fffffffLL || C > 0x7fffffffLL) return CE_ERR_SHAPE;
+    const int es = dtype == CE_F32 ? 4 : 2;
+    if ((unsigned long long)B * (unsigned long long)C > (1ull << 61) / (unsigned)es)
+        return CE_ERR_SHAPE;
+    const uintptr_t pz = reinterpret_cast<uintptr_t>(probs);
+    const uintptr_t dz = reinterpret_cast<uintptr_t>(dy);
+    const uintptr_t xz = reinterpret_cast<uintptr_t>(dx_out);
+    if (pz % es || dz % es || xz % es) return CE_ERR_ALIGN;
+    const size_t nbytes = (size_t)B * (size_t)C * es;
+    // dx may not overlap p or dy unless it is one of them exactly (each element
+    // is read by the thread that then writes it, after the row's dot product)
+    if ((xz != pz && ranges_overlap(xz, nbytes, pz, nbytes)) ||
+        (xz != dz && ranges_overlap(xz, nbytes, dz, nbytes)))
+        return CE_ERR_OVERLAP;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DeviceInfo d;
+    int rc = device_info(dev, &d);
+    if (rc != CE_OK) return rc;
+    for (const void *ptr : {probs, dy, (const void *)dx_out})
+        if ((rc = check_pointer(ptr, d)) != CE_OK) return rc;
+    const bool vec = ce::softmax_bwd_vec_ok(C, es, pz, dz, xz);
+    e = ce::launch_softmax_bwd(probs, dy, dx_out, B, C, dtype, vec, d.sms,
+                               static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return CE_OK;
+}
+
+}  // namespace
+
 extern "C" {
+
+int ce_softmax_fwd(const void *logits, int64_t B, int64_t C, int dtype, void *probs_out,
+                   void *stream) {
+    return run(logits, nullptr, B, C, dtype, CE_REDUCE_NONE, nullptr, nullptr, probs_out, stream,
+               CE_PATH_AUTO, 0, true);
+}
+
+int ce_softmax_fwd_path(const void *logits, int64_t B, int64_t C, int dtype, void *probs_out,
+                        void *stream, int path, int split) {
+    return run(logits, nullptr, B, C, dtype, CE_REDUCE_NONE, nullptr, nullptr, probs_out, stream,
+               path, split, true);
+}
+
+int ce_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int dtype,
+                   void *dx_out, void *stream) {
+    return run_softmax_bwd(probs, dy, B, C, dtype, dx_out, stream);
+}
 
 int ce_fwd_bwd(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
                float *loss_out, void *grad_out, void *stream) {

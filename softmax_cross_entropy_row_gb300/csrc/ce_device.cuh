@@ -56,6 +56,7 @@ struct ParamsEx : Params {
     float grad_base;              // the gradient's row factor: 1/B (mean) or 1 (sum, none)
     const float *grad_scale;      // nullptr (1), one fp32, or [B] fp32 (scale_per_row)
     int scale_per_row;
+    int softmax;                  // 1: row softmax forward (no targets, no loss; grad = probabilities)
 };
 
 constexpr int kReduceMean = 0;
@@ -66,6 +67,19 @@ __host__ __device__ __forceinline__ constexpr int reduction_of(const Params &) {
     return kReduceMean;
 }
 __host__ __device__ __forceinline__ int reduction_of(const ParamsEx &p) { return p.reduction; }
+
+// Row softmax forward: no target (no one-hot term, nothing left out of the
+// sum), no loss; the "gradient" written is softmax(z_b) itself.
+__host__ __device__ __forceinline__ constexpr bool is_softmax(const Params &) { return false; }
+__host__ __device__ __forceinline__ bool is_softmax(const ParamsEx &p) { return p.softmax != 0; }
+
+// The target of row b (-1, no target, for the softmax forward).
+__device__ __forceinline__ int target_at(const Params &p, long long b) {
+    return __ldg(p.targets + b);
+}
+__device__ __forceinline__ int target_at(const ParamsEx &p, long long b) {
+    return p.softmax ? -1 : __ldg(p.targets + b);
+}
 
 // false: the loss alone (no gradient computed or written)
 __host__ __device__ __forceinline__ constexpr bool writes_grad(const Params &) { return true; }
@@ -90,7 +104,8 @@ __device__ __forceinline__ float row_grad_factor(const ParamsEx &p, float scalar
 
 // The plain call, which runs the Params build of the kernels.
 inline bool is_plain(const ParamsEx &p) {
-    return p.reduction == kReduceMean && p.grad_scale == nullptr && p.grad != nullptr;
+    return p.reduction == kReduceMean && p.grad_scale == nullptr && p.grad != nullptr &&
+           !p.softmax;
 }
 
 // Packed fp32 pairs (Blackwell f32x2 arithmetic: each half is rounded exactly
@@ -705,7 +720,7 @@ __device__ __forceinline__ void batch_tail(const P &p, float2 *scratch) {
 // row losses are themselves the output).
 template <typename P>
 __device__ __forceinline__ void finish_cta(const P &p, int *flag, float2 *scratch) {
-    if (reduction_of(p) == kReduceNone) return;
+    if (reduction_of(p) == kReduceNone || is_softmax(p)) return;
     if (publish_rows(p, flag)) batch_tail(p, scratch);
 }
 

@@ -54,4 +54,12 @@ cudaError_t rows_warp_max_ctas_per_sm(int dtype, int per_sm, long long C, int sm
 // Streaming path: pass A (chunk partials) and pass B (combine, gradient, loss).
 cudaError_t launch_stream(const ParamsEx &p, int dtype, long long chunks, cudaStream_t s);
 
+// Row softmax backward (ce_softmax_bwd.cu): dx = p * (dy - sum p dy) per row.
+// The vector kernel needs rows of at most 64 KB whose starts are 16-byte
+// aligned in all three tensors (softmax_bwd_vec_ok); the other reads p and dy
+// twice.
+bool softmax_bwd_vec_ok(long long C, int es, uintptr_t p, uintptr_t dy, uintptr_t dx);
+cudaError_t launch_softmax_bwd(const void *p, const void *dy, void *dx, long long B, long long C,
+                               int dtype, bool vec, int sms, cudaStream_t s);
+
 }  // namespace ce

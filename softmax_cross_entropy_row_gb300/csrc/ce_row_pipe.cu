@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(NT, 1)
     int consumed = 0;
     int s_cur = 0;         // slot and phase parity of the next row to consume
     uint32_t ph_cur = 0;
-    int t_next = nrows > 0 ? __ldg(p.targets + cid) : 0;
+    int t_next = nrows > 0 ? target_at(p, cid) : 0;
 
     auto fail = [&]() {
         failed = true;
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(NT, 1)
         const int par = j & 1;
         const int t = t_next;
         t_out = t;
-        if (j + 1 < nrows) t_next = __ldg(p.targets + row + ncl);
+        if (j + 1 < nrows) t_next = target_at(p, row + ncl);
         const Geom g = geom(row);
         const bool has_t = t >= c0 && t < c1;
         const int tl = has_t ? t - c0 + g.head : kNoTarget;  // target, vector-0 based
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         // Step 3: the row's loss, by one thread of rank 0
-        if (rank == 0 && warp == kLossWarp && lane == 0 && !skip) {
+        if (rank == 0 && warp == kLossWarp && lane == 0 && !skip && !is_softmax(p)) {
             float l;
             if (has_t) {
                 l = row_loss(s_rest, e_t, S, zt, M);

@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     bool failed = false;
     long long consumed = 0;
-    int t_next = nrows > 0 ? __ldg(p.targets + cid) : 0;
+    int t_next = nrows > 0 ? target_at(p, cid) : 0;
 
     for (long long j = 0; j < nrows; ++j) {
         const long long row = cid + j * ncl;
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t parity = (uint32_t)((j / nslots) & 1);
         unsigned char *slot = smem + (size_t)s * slot_bytes;
         const long long t = t_next;
-        if (j + 1 < nrows) t_next = __ldg(p.targets + row + ncl);
+        if (j + 1 < nrows) t_next = target_at(p, row + ncl);
 
         uint64_t gs, ge, g0, lo, hi;
         span(row, gs, ge, g0, lo, hi);
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
 
         // ---- Step 3: the row's loss (one writer per row)
-        if (rank == 0 && tid == 0 && !failed) {
+        if (rank == 0 && tid == 0 && !failed && !is_softmax(p)) {
             float l;
             if (has_t) {
                 l = row_loss(s_rest, e_t, S, zt, M);

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
         uint64_t gs, ge, g0, lo, hi;
         span(gw + i * TW, r0, r1, gs, ge, g0, lo, hi);
         // the tile's first targets, in flight while the copy lands
-        int tchunk = r0 + lane < r1 ? __ldg(p.targets + r0 + lane) : 0;
+        int tchunk = r0 + lane < r1 ? target_at(p, r0 + lane) : 0;
 
         if (!failed) {
             if (mbar_wait(&my_full[s], parity)) {
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
 
         for (long long r = r0; r < r1; ++r) {
             const int q = (int)(r - r0);
-            if (q > 0 && (q & 31) == 0) tchunk = r + lane < r1 ? __ldg(p.targets + r + lane) : 0;
+            if (q > 0 && (q & 31) == 0) tchunk = r + lane < r1 ? target_at(p, r + lane) : 0;
             const int t = __shfl_sync(0xffffffffu, tchunk, q & 31);
             const bool has_t = t >= 0 && t < C;
 
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
             }
 
             // Step 3: loss of the row, log(S / e_t)
-            if (lane == 0) {
+            if (lane == 0 && !is_softmax(p)) {
                 float l;
                 if (has_t) {
                     l = row_loss(s_rest, e_t, S, zt, M);

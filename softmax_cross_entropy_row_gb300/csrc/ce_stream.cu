@@ -41,8 +41,8 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
     return s;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(NT) stream_partials_kernel(Params p, long long chunks) {
+template <typename T, typename P>
+__global__ void __launch_bounds__(NT) stream_partials_kernel(P p, long long chunks) {
     using E = Elem<T>;
     __shared__ float red[NT / 32];
     const long long b = blockIdx.x / chunks;
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(NT) stream_partials_kernel(Params p, long long
         mx = fmaxf(mx, z[i]);
     }
     const float M = block_max(mx, red) * kLog2e;
-    const long long t = __ldg(p.targets + b);
+    const long long t = target_at(p, b);
     float s = 0.f;  // without the target's term
 #pragma unroll
     for (int i = 0; i < PT; ++i) {
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(NT) stream_grad_kernel(P p, long long chunks) 
     }
     const float s_rest = block_sum(sloc, red);  // the row's sum without the target's term
 
-    const long long t = __ldg(p.targets + b);
+    const long long t = target_at(p, b);
     const bool has_t = t >= 0 && t < C;
     const float zt = has_t ? __ldcg(p.zt + b) : 0.f;
     const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(NT) stream_grad_kernel(P p, long long chunks) 
             }
         }
     }
-    if (k == 0 && threadIdx.x == 0) {
+    if (k == 0 && threadIdx.x == 0 && !is_softmax(p)) {
         float l;
         if (has_t) {
             l = row_loss(s_rest, e_t, S, zt, M);
@@ -134,7 +134,10 @@ cudaError_t launch_t(const ParamsEx &p, long long chunks, cudaStream_t s) {
     const long long blocks = p.B * chunks;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const Params &pp = p;
-    stream_partials_kernel<T><<<(unsigned)blocks, NT, 0, s>>>(pp, chunks);
+    if (is_plain(p))
+        stream_partials_kernel<T, Params><<<(unsigned)blocks, NT, 0, s>>>(pp, chunks);
+    else
+        stream_partials_kernel<T, ParamsEx><<<(unsigned)blocks, NT, 0, s>>>(p, chunks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (is_plain(p))

@@ -78,6 +78,24 @@ def test_host_side_errors_of_the_extended_entry_points(lib):
     assert ex(1 << 20, 1 << 24, 4, 4, 0, 0, (1 << 26) + 32, 1 << 25, 1 << 26, None) == 6
 
 
+def test_host_side_errors_of_the_softmax_entry_points(lib):
+    """Row softmax forward and backward: the same checks, before any CUDA call."""
+    fw, fp, bw = lib.ce_softmax_fwd, lib.ce_softmax_fwd_path, lib.ce_softmax_bwd
+    assert fw(None, 4, 4, 0, 4096, None) == 1                # NULL logits
+    assert fw(256, 4, 4, 0, None, None) == 1                 # NULL output
+    assert fw(256, 4, 4, 7, 4096, None) == 3                 # dtype
+    assert fw(256, 0, 4, 0, 4096, None) == 2                 # B = 0
+    assert fp(256, 4, 0, 1, 4096, None, 0, 0) == 2           # C = 0
+    assert fw(258, 4, 4, 0, 4096, None) == 4                 # fp32 logits at 2 mod 4
+    assert fw(1 << 20, 4, 4, 0, (1 << 20) + 32, None) == 6   # output overlaps logits
+    assert bw(None, 512, 4, 4, 0, 4096, None) == 1
+    assert bw(256, 512, 4, 4, 7, 4096, None) == 3
+    assert bw(256, 512, 4, 4, 1, 4097, None) == 4            # bf16 dx at an odd address
+    # dx may be p or dy exactly, but may not overlap them otherwise
+    assert bw(1 << 20, 1 << 24, 4, 4, 0, (1 << 20) + 16, None) == 6
+    assert bw(1 << 20, 1 << 24, 4, 4, 0, (1 << 24) - 16, None) == 6
+
+
 def test_no_cpu_fallback_without_library(tmp_path):
     """The binding refuses to run when the CUDA library is absent."""
     import importlib

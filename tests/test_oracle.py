@@ -353,3 +353,69 @@ def test_f16_widening_is_exact(oracle_mod):
     # the same row as fp32 values (exactly representable) gives the same fp64 results
     l32, g32 = oracle_mod.rows(z64.astype(np.float32), t)
     assert np.array_equal(l16, l32) and np.array_equal(g16, g32)
+
+
+# ------------------------------------------------ row softmax, fwd and bwd
+
+def test_softmax_forward_pins(oracle_mod):
+    """Rows sum to 1; a uniform row gives 1/C; shift invariance; the target's
+    probability is exp(-l) of the loss oracle; torch CPU fp64 softmax."""
+    torch = pytest.importorskip("torch")
+    inp = wl.random_case(12, 777, "f32", seed=21, sigma=6.0)
+    p = oracle_mod.softmax(inp.logits)
+    assert np.allclose(p.sum(axis=1), 1.0, rtol=0, atol=1e-13)
+    l = oracle_mod.rows(inp.logits, inp.targets, grad=False)
+    assert np.allclose(p[np.arange(12), inp.targets], np.exp(-l), rtol=1e-12, atol=0)
+    # shift invariance on a grid where adding 64 is exact in fp32
+    zg = (np.random.default_rng(5).integers(-3000, 3000, size=(4, 333)) * 2.0 ** -7).astype(np.float32)
+    assert np.allclose(oracle_mod.softmax(zg + np.float32(64.0)), oracle_mod.softmax(zg),
+                       rtol=1e-12, atol=0)
+    ref = torch.softmax(torch.tensor(inp.logits, dtype=torch.float64), dim=1).numpy()
+    assert np.allclose(p, ref, rtol=1e-12, atol=1e-18)
+    u = np.full((2, 300), 3.5, dtype=np.float32)
+    assert np.allclose(oracle_mod.softmax(u), 1.0 / 300, rtol=1e-15, atol=0)
+
+
+def test_softmax_backward_is_the_jacobian_product(oracle_mod):
+    """dx equals J^T dy with J the softmax Jacobian taken by central finite
+    differences of the forward oracle (exact fp32 steps); rows of dx sum to
+    0; a row-constant dy gives dx = 0."""
+    rng = np.random.default_rng(9)
+    B, C = 2, 5
+    h = 2.0 ** -12
+    z = (rng.integers(-400, 400, size=(B, C)) * 2.0 ** -7).astype(np.float32)
+    p = oracle_mod.softmax(z)
+    dy = rng.standard_normal((B, C)).astype(np.float32)
+    dx = oracle_mod.softmax_bwd(p.astype(np.float32), dy)
+    # the oracle takes p in the element type: compare against p widened from fp32
+    p32 = p.astype(np.float32).astype(np.float64)
+    for b in range(B):
+        J = np.empty((C, C))
+        for c in range(C):
+            zp, zm = z.copy(), z.copy()
+            zp[b, c] += np.float32(h)
+            zm[b, c] -= np.float32(h)
+            J[:, c] = (oracle_mod.softmax(zp)[b] - oracle_mod.softmax(zm)[b]) / (2 * h)
+        assert np.allclose(dx[b], J.T @ dy[b].astype(np.float64), rtol=0, atol=5e-6)
+    assert np.allclose(dx.sum(axis=1), 0.0, atol=1e-6 * np.abs(p32).sum())
+    const = np.full((B, C), 1.25, dtype=np.float32)
+    assert np.allclose(oracle_mod.softmax_bwd(p.astype(np.float32), const), 0.0,
+                       atol=2e-7)
+
+
+def test_softmax_backward_against_torch(oracle_mod):
+    """torch CPU fp64 autograd of softmax at z = log p (softmax(log p) = p for
+    rows summing to 1) with upstream dy."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(13)
+    q = rng.random((6, 40))
+    p = (q / q.sum(axis=1, keepdims=True))
+    dy = rng.standard_normal((6, 40))
+    # fp32 inputs to the oracle, the same fp32 values to torch in fp64
+    p32, dy32 = p.astype(np.float32), dy.astype(np.float32)
+    pt = torch.tensor(p32.astype(np.float64))
+    pt = pt / pt.sum(dim=1, keepdim=True)
+    z = torch.log(pt).requires_grad_(True)
+    torch.softmax(z, dim=1).backward(torch.tensor(dy32.astype(np.float64)))
+    dx = oracle_mod.softmax_bwd(p32, dy32)
+    assert np.allclose(dx, z.grad.numpy(), rtol=1e-5, atol=1e-7)
