@@ -256,10 +256,13 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
 
-        // Step 1 (per thread): m_t
+        // Step 1 (per thread): m_t.  Vectors past the slice hold -inf and
+        // are skipped here and below (they would only add zeros), so a short
+        // slice costs only its own vectors.
         typename E::MaxAcc macc = E::max_init();
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) E::max_step(macc, x[k]);
+        for (int k = 0; k < VPT; ++k)
+            if (tid + k * NT < g.nv) E::max_step(macc, x[k]);
         const float mx = E::max_value(macc);
         const float Mx = mx * kLog2e;  // -inf when the thread holds no element
         hv = mx != -INFINITY;
@@ -274,6 +277,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = tid + k * NT;
+            if (v >= g.nv) continue;
             unsigned long long e2[W2];
             E::unpack2(x[k], e2);
             if (v == v_t) zt_sh[par] = element_of<E>(x[k], tl - v * W);
