@@ -202,7 +202,16 @@ int ce_query_plan(int64_t B, int64_t C, int dtype, int *path, int *split, int *c
  */
 int ce_get_device_errors(void *stream, int32_t *bad_targets, int32_t *timeouts);
 
-/* Free every cached workspace of every device (after their streams are idle). */
+/*
+ * Free every workspace of every device: the current one of each stream and
+ * the ones outgrown before.  A workspace that grows (a larger B, or the
+ * streaming path, on the same stream) is replaced, not freed, because kernels
+ * in flight and CUDA graphs captured with earlier calls still use the old
+ * one; a graph keeps working, with its own workspace (whose device error
+ * counters ce_get_device_errors no longer reads), until this call.  Call it
+ * only when the streams are idle and no graph captured with a library call
+ * will be replayed.
+ */
 int ce_release_workspaces(void);
 
 /*

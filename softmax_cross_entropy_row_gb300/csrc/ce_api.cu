@@ -10,6 +10,7 @@
 #include <mutex>
 #include <tuple>
 #include <utility>
+#include <vector>
 
 #include "../../include/ce.h"
 #include "ce_launch.h"
@@ -331,6 +332,10 @@ struct Workspace {
 
 std::mutex g_ws_mu;
 std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+// Outgrown workspaces (device, base): a CUDA graph captured with a call that
+// used one still holds its address, so it stays allocated until
+// ce_release_workspaces.
+std::vector<std::pair<int, unsigned char *>> g_ws_retired;
 
 constexpr size_t kHeaderBytes = 256;
 
@@ -345,8 +350,9 @@ int get_workspace(int dev, cudaStream_t s, size_t need, Workspace *out) {
         if (e != cudaSuccess) return cuda_fail(e);
         if (cs != cudaStreamCaptureStatusNone) return CE_ERR_CAPTURE;
         if (w.base) {
-            if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
-            cudaFree(w.base);
+            // not freed: kernels in flight and graphs captured earlier on this
+            // stream may still use it
+            g_ws_retired.push_back({dev, w.base});
             w.base = nullptr;
             w.bytes = 0;
         }
@@ -771,7 +777,13 @@ int ce_release_workspaces(void) {
         cudaError_t e = cudaFree(kv.second.base);
         if (e != cudaSuccess) rc = cuda_fail(e);
     }
+    for (auto &r : g_ws_retired) {
+        cudaSetDevice(r.first);
+        cudaError_t e = cudaFree(r.second);
+        if (e != cudaSuccess) rc = cuda_fail(e);
+    }
     g_ws.clear();
+    g_ws_retired.clear();
     cudaSetDevice(cur);
     return rc;
 }

@@ -316,6 +316,40 @@ def test_graph_capture_and_replay():
     check_full(inp2, loss, grad, "graph replay")
 
 
+def test_graph_survives_workspace_growth():
+    """A graph captured before its stream's workspace grows (here: a larger
+    batch on the streaming path, which adds per-chunk partials) still replays
+    correctly afterwards: the outgrown workspace stays allocated."""
+    inp = _case(256, 3000, "f32", seed=21)
+    z, t = device_inputs(inp)
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    grad = torch.empty_like(z)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ce.ce_fwd_bwd(z, t, loss, grad, s)
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            ce.ce_fwd_bwd(z, t, loss, grad, s)
+        big = _case(4000, 5000, "f32", seed=22)
+        zb, tb = device_inputs(big)
+        lb, gb = run(zb, tb, STREAM, 0, s)
+    s.synchronize()
+    check_full(big, lb, gb, "the call that grew the workspace")
+    inp2 = _case(256, 3000, "f32", seed=23)
+    z2, t2 = device_inputs(inp2)
+    z.copy_(z2)
+    t.copy_(t2)
+    loss.fill_(float("nan"))
+    with torch.cuda.stream(s):
+        graph.replay()
+    s.synchronize()
+    check_full(inp2, loss, grad, "graph replayed after the growth")
+    l_now, g_now = run(z, t, AUTO, 0, s)
+    s.synchronize()
+    assert torch.equal(l_now, loss) and torch.equal(g_now, grad)
+
+
 def test_capture_needs_a_sized_workspace():
     z = torch.zeros(4, 8, device="cuda")
     t = torch.zeros(4, dtype=torch.int32, device="cuda")
