@@ -199,6 +199,24 @@ def time_oracle(inp, budget_s: float = CPU_SAMPLE_S):
 
 # ------------------------------------------------------------------ our arm
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's `value` (replicas are timed by their
+    slowest rank); the value itself when the job has one process."""
+    import torch
+
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    tt = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def replica_rows_per_s(rows_per_rank: int, world: int, seconds_per_step: float) -> float:
+    """Whole-job throughput of `world` replicas that each process
+    `rows_per_rank` rows per step, timed by the slowest rank."""
+    return world * rows_per_rank / seconds_per_step
+
+
 def device_set(inp, device):
     import torch
 
@@ -278,11 +296,8 @@ def bench_workload(w, inp, steps, warmup, device, l2_bytes, hbm_peak, peak_note,
             e1.record(s)
             e1.synchronize()
         torch.cuda.synchronize(device)
-        elapsed = e0.elapsed_time(e1) / 1e3
+        elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, device)
         if world > 1:
-            tt = torch.tensor([elapsed], dtype=torch.float64, device=device)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            elapsed = float(tt.item())
             torch.distributed.barrier()
         bad, tmo = ce.ce_get_device_errors(s)
     del graph, tail
@@ -294,7 +309,7 @@ def bench_workload(w, inp, steps, warmup, device, l2_bytes, hbm_peak, peak_note,
         "path": plan["path_name"], "split": plan["split"], "ctas": plan["ctas"],
         "threads": plan["threads"], "smem_bytes": plan["smem_bytes"],
         "launches_per_step": plan["launches"], "steps": n_steps, "buffer_sets": nsets,
-        "ms_per_step": per_step * 1e3, "rows_per_s": world * w.B / per_step,
+        "ms_per_step": per_step * 1e3, "rows_per_s": replica_rows_per_s(w.B, world, per_step),
         "achieved_gbs": achieved, "frac_of_peak": achieved / hbm_peak,
         "min_bytes_per_step": w.min_bytes, "device_errors": [bad, tmo],
         "clocks": sampler.summary(),
@@ -302,14 +317,15 @@ def bench_workload(w, inp, steps, warmup, device, l2_bytes, hbm_peak, peak_note,
     if per_launch is not None:
         res["kernel_ms_per_launch"] = per_launch * 1e3
     if with_e2e:
-        res["e2e"] = bench_e2e(w, inp, device, steps=min(50, max(5, int(0.5 / max(est, 1e-6)))))
+        res["e2e"] = bench_e2e(w, inp, device, steps=min(50, max(5, int(0.5 / max(est, 1e-6)))),
+                               world=world)
     for z, t, loss, grad in sets:
         del z, t, loss, grad
     torch.cuda.empty_cache()
     return res
 
 
-def bench_e2e(w, inp, device, steps):
+def bench_e2e(w, inp, device, steps, world=1):
     """The public call with host inputs: pinned H2D copies of logits and
     targets, ce_fwd_bwd, and the 4-byte loss copied back, every step."""
     import torch
@@ -338,16 +354,20 @@ def bench_e2e(w, inp, device, steps):
         for _ in range(3):
             step()
         s.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
         for _ in range(steps):
             step()
         e1.record(s)
         e1.synchronize()
-    per_step = e0.elapsed_time(e1) / 1e3 / steps
+    per_step = max_over_ranks(e0.elapsed_time(e1) / 1e3, device) / steps
     h2d = hz.numel() * hz.element_size() + ht.numel() * ht.element_size()
-    return {"value": w.B / per_step, "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": 4, "steps": steps, "ms_per_step": per_step * 1e3}
+    # whole-job figures: every replica copies its own inputs and loss
+    return {"value": replica_rows_per_s(w.B, world, per_step), "unit": "rows/s",
+            "h2d_bytes_per_step": int(world * h2d), "d2h_bytes_per_step": 4 * world,
+            "steps": steps, "ms_per_step": per_step * 1e3}
 
 
 # The rows beyond the plain fused step, measured the same way: (label, workload,
@@ -575,7 +595,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": ({k: head["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step",
                                              "d2h_bytes_per_step")} if "e2e" in head else None),
-        "gpu_launches": head["steps"] * head["launches_per_step"],
+        "gpu_launches": world * head["steps"] * head["launches_per_step"],
         "clocks": head["clocks"],
         "workloads": [dict(results[n], l2=l2_note(results[n], wl.WORKLOADS_BY_NAME[n], l2_bytes))
                       for n in names],
