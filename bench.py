@@ -12,8 +12,8 @@ loss and the full gradient of one batch.
 Timing: steps run from a CUDA graph (one library call per step, captured
 once), cycling through enough buffer sets that every step reads inputs that
 are not in L2; CUDA events on the launching stream bracket the timed steps.
-``e2e`` times the eager public call with the step's inputs copied from pinned
-host memory and the loss copied back, every step.  ``--impl reference`` times
+``e2e`` times the host-buffer call ce_fwd_bwd_host, eagerly: every step copies
+its inputs from pinned host memory and its loss back.  ``--impl reference`` times
 the fp64 CPU oracle (the only reference this path has) on the host cores.
 
 With torchrun (N > 1) every rank runs an independent replica of the workload
@@ -70,19 +70,30 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The host-side C-ABI layer: argument checks, workspaces and the planner.  Its
+# launch decisions are recorded with the traffic (PLAN_KEYS), so the hash
+# covers the device code only.
+HOST_ONLY_SOURCES = ("ce_api.cu",)
+PLAN_KEYS = ("path", "split", "ctas", "threads", "smem_bytes")
+
+
 def source_hash() -> str:
+    """Hash of the kernels' sources (every csrc file but the host-only ones)."""
     h = hashlib.sha256()
     files = sorted(glob.glob(os.path.join(ROOT, "softmax_cross_entropy_row_gb300", "csrc", "*")))
     for p in files:
+        if os.path.basename(p) in HOST_ONLY_SOURCES:
+            continue
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, plan=None):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None if the kernels changed since it was taken."""
+    summary, or None if the kernels or their launch (path, split, CTAs,
+    threads, shared memory) changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -91,6 +102,8 @@ def recorded_traffic(workload: str):
         return None
     e = d.get(workload)
     if not e or e.get("source_sha") != source_hash():
+        return None
+    if plan is not None and e.get("plan") != {k: plan.get(k) for k in PLAN_KEYS}:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -326,8 +339,9 @@ def bench_workload(w, inp, steps, warmup, device, l2_bytes, hbm_peak, peak_note,
 
 
 def bench_e2e(w, inp, device, steps, world=1):
-    """The public call with host inputs: pinned H2D copies of logits and
-    targets, ce_fwd_bwd, and the 4-byte loss copied back, every step."""
+    """The public call with host buffers, ce_fwd_bwd_host: every step copies
+    the pinned logits and targets to the device, runs the fused kernel and
+    copies the 4-byte loss back to the host."""
     import torch
 
     import softmax_cross_entropy_row_gb300 as ce
@@ -338,17 +352,11 @@ def bench_e2e(w, inp, device, steps, world=1):
         hz = torch.from_numpy(inp.logits).pin_memory()
     ht = torch.from_numpy(inp.targets).pin_memory()
     hl = torch.empty(1, dtype=torch.float32).pin_memory()
-    dz = torch.empty(hz.shape, dtype=hz.dtype, device=device)
-    dt = torch.empty(ht.shape, dtype=ht.dtype, device=device)
-    dl = torch.empty(1, dtype=torch.float32, device=device)
-    dg = torch.empty_like(dz)
+    dg = torch.empty(hz.shape, dtype=hz.dtype, device=device)
     s = torch.cuda.Stream(device)
 
     def step():
-        dz.copy_(hz, non_blocking=True)
-        dt.copy_(ht, non_blocking=True)
-        ce.ce_fwd_bwd(dz, dt, dl, dg, s)
-        hl.copy_(dl, non_blocking=True)
+        ce.ce_fwd_bwd_host(hz, ht, hl, dg, s)
 
     with torch.cuda.stream(s):
         for _ in range(3):
@@ -575,7 +583,10 @@ def main():
             torch.distributed.destroy_process_group()
         return
     roof = {"bound": "hbm", "achieved": head["achieved_gbs"], "peak": hbm_peak, "unit": "GB/s",
-            "frac": head["frac_of_peak"], "traffic": recorded_traffic(w.name),
+            "frac": head["frac_of_peak"],
+            "traffic": recorded_traffic(w.name, {"path": head["path"], "split": head["split"],
+                                                 "ctas": head["ctas"], "threads": head["threads"],
+                                                 "smem_bytes": head["smem_bytes"]}),
             "peak_source": peak_note,
             "algorithmic_bytes_per_launch": w.min_bytes,
             "kernel": head["path"]}

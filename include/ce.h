@@ -186,6 +186,24 @@ int ce_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int 
                    void *dx_out, void *stream);
 
 /*
+ * ce_fwd_bwd_host -- ce_fwd_bwd for logits and targets in host memory: the
+ * same L (the same bits) and gradient, with the copies to the device made by
+ * the library.  logits_host [B][C] in `dtype` and targets_host [B] int32:
+ * host memory (page-locked for asynchronous copies; pageable memory works,
+ * with copies the host waits for); loss_host: one fp32 in host
+ * memory, written when `stream` reaches the end of the call (synchronise the
+ * stream before reading it); grad_out: device [B][C] in `dtype`, as for
+ * ce_fwd_bwd (the gradient stays on the device for the backward pass).  The
+ * copies into library-owned device buffers, the kernel of ce_fwd_bwd and the
+ * copy of the loss back run in order on `stream`.  The library keeps per-stream
+ * device copies of the last inputs (B*C*elem + 4B bytes) until
+ * ce_release_workspaces.  Not capturable (CE_ERR_CAPTURE while `stream` is
+ * being captured).  Returns a ce_status; argument checks as for ce_fwd_bwd.
+ */
+int ce_fwd_bwd_host(const void *logits_host, const int32_t *targets_host, int64_t B, int64_t C,
+                    int dtype, float *loss_host, void *grad_out, void *stream);
+
+/*
  * ce_query_plan -- the launch that ce_fwd_bwd would make for this shape on
  * the current device (path, split, total CTAs, threads per CTA, dynamic shared
  * memory per CTA, kernel launches per call).  Any output pointer may be NULL.

@@ -48,7 +48,7 @@ STATUS = {0: "CE_OK", 1: "CE_ERR_NULL", 2: "CE_ERR_SHAPE", 3: "CE_ERR_DTYPE",
 EXPORTS = ("ce_fwd_bwd", "ce_fwd_bwd_path", "ce_query_plan", "ce_get_device_errors",
            "ce_release_workspaces", "ce_status_string", "ce_last_cuda_error",
            "ce_fwd_bwd_noalloc", "ce_fwd_bwd_ex", "ce_fwd_bwd_ex_path", "ce_forward",
-           "ce_softmax_fwd", "ce_softmax_fwd_path", "ce_softmax_bwd")
+           "ce_softmax_fwd", "ce_softmax_fwd_path", "ce_softmax_bwd", "ce_fwd_bwd_host")
 
 
 class CEError(RuntimeError):
@@ -98,6 +98,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.ce_forward.restype = ci
     lib.ce_softmax_fwd.argtypes = [vp, i64, i64, ci, vp, vp]
     lib.ce_softmax_fwd.restype = ci
+    lib.ce_fwd_bwd_host.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp]
+    lib.ce_fwd_bwd_host.restype = ci
     lib.ce_softmax_fwd_path.argtypes = [vp, i64, i64, ci, vp, vp, ci, ci]
     lib.ce_softmax_fwd_path.restype = ci
     lib.ce_softmax_bwd.argtypes = [vp, vp, i64, i64, ci, vp, vp]
@@ -194,6 +196,26 @@ def ce_forward(logits, targets, loss_out, reduction=CE_REDUCE_MEAN, stream=None)
     B, C = logits.shape
     _check(lib.ce_forward(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
                           int(reduction), _ptr(loss_out), _stream_handle(stream)))
+
+
+def ce_fwd_bwd_host(logits_host, targets_host, loss_host, grad_out, stream=None) -> None:
+    """ce_fwd_bwd with the logits, targets and loss in host memory (CPU
+    tensors, page-locked for overlapped copies); the gradient goes to the CUDA
+    tensor ``grad_out``.  ``loss_host`` is written when ``stream`` reaches the
+    end of the call."""
+    lib = load_library()
+    if logits_host.device.type != "cpu" or targets_host.device.type != "cpu" or \
+            loss_host.device.type != "cpu":
+        raise ValueError("logits_host, targets_host and loss_host must be CPU tensors")
+    if logits_host.dim() != 2 or not logits_host.is_contiguous():
+        raise ValueError("logits_host must be a contiguous [B, C] tensor")
+    if grad_out.shape != logits_host.shape or grad_out.dtype != logits_host.dtype or \
+            not grad_out.is_contiguous():
+        raise ValueError("grad_out must be a contiguous tensor of the logits' shape and dtype")
+    B, C = logits_host.shape
+    _check(lib.ce_fwd_bwd_host(_ptr(logits_host), _ptr(targets_host), B, C,
+                               _dtype_code(logits_host), _ptr(loss_host), _ptr(grad_out),
+                               _stream_handle(stream)))
 
 
 def ce_softmax_fwd(logits, probs_out, stream=None, path=CE_PATH_AUTO, split=0) -> None:

@@ -6,6 +6,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -296,6 +297,18 @@ cudaError_t launch_split_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, 
                             pl.slice, pl.smem, split_stage_enabled() ? 1 : 0, s);
 }
 
+cudaError_t launch_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, cudaStream_t s) {
+    switch (pl.path) {
+        case CE_PATH_ROWS_WARP:
+            return ce::launch_rows_warp(p, dtype, pl.per_sm, pl.ctas, pl.nslots, pl.rows_per_tile,
+                                        pl.slot_bytes, pl.smem, s);
+        case CE_PATH_ROW_SPLIT:
+            return launch_split_plan(p, dtype, pl, s);
+        default:
+            return ce::launch_stream(p, dtype, pl.chunks, s);
+    }
+}
+
 int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -337,7 +350,18 @@ std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
 // ce_release_workspaces.
 std::vector<std::pair<int, unsigned char *>> g_ws_retired;
 
+// Host-buffer entry point: per (device, stream) device copies of the logits
+// and targets.  Guarded by g_ws_mu.
+struct HostStage {
+    unsigned char *z = nullptr;
+    size_t zbytes = 0;
+    unsigned char *t = nullptr;
+    size_t tbytes = 0;
+};
+std::map<std::pair<int, uintptr_t>, HostStage> g_hs;
+
 constexpr size_t kHeaderBytes = 256;
+constexpr size_t kLossSlot = 64;  // header bytes holding the host entry's device copy of L
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -485,19 +509,7 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     p.scale_per_row = grad_scale != nullptr && reduction == CE_REDUCE_NONE;
     p.softmax = softmax ? 1 : 0;
 
-    switch (pl.path) {
-        case CE_PATH_ROWS_WARP:
-            e = ce::launch_rows_warp(p, dtype, pl.per_sm, pl.ctas, pl.nslots, pl.rows_per_tile,
-                                     pl.slot_bytes, pl.smem, s);
-            break;
-        case CE_PATH_ROW_SPLIT:
-            e = launch_split_plan(p, dtype, pl, s);
-            break;
-        default:
-            e = ce::launch_stream(p, dtype, pl.chunks, s);
-            break;
-    }
-    if (e != cudaSuccess) return cuda_fail(e);
+    if ((e = launch_plan(p, dtype, pl, s)) != cudaSuccess) return cuda_fail(e);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return CE_OK;
@@ -672,6 +684,123 @@ int run_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int
     return CE_OK;
 }
 
+// ------------------------------------------------------ host-buffer entry
+//
+// ce_fwd_bwd_host: the copies of the logits and targets into the stream's
+// staging buffers, the launch of ce_fwd_bwd on them and the copy of the loss
+// back, in order on the caller's stream.  A copy engine moves ~160-200 GB/s
+// from page-locked memory on GB300, so the copy dominates the call;
+// splitting the batch into chunks whose copies overlap the kernels of the
+// chunks before (on a second stream) measured no faster.
+
+int host_stage(int dev, cudaStream_t s, size_t zbytes, size_t tbytes, HostStage **out) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    HostStage &h = g_hs[{dev, reinterpret_cast<uintptr_t>(s)}];
+    cudaError_t e;
+    // outgrown staging buffers may still be read by queued kernels: retired
+    if (h.zbytes < zbytes) {
+        if (h.z) g_ws_retired.push_back({dev, h.z});
+        h.z = nullptr;
+        h.zbytes = 0;
+        void *p = nullptr;
+        const size_t bytes = align_up(zbytes, 1 << 20);
+        if ((e = cudaMalloc(&p, bytes)) != cudaSuccess) return cuda_fail(e);
+        h.z = static_cast<unsigned char *>(p);
+        h.zbytes = bytes;
+    }
+    if (h.tbytes < tbytes) {
+        if (h.t) g_ws_retired.push_back({dev, h.t});
+        h.t = nullptr;
+        h.tbytes = 0;
+        void *p = nullptr;
+        const size_t bytes = align_up(tbytes, 1 << 16);
+        if ((e = cudaMalloc(&p, bytes)) != cudaSuccess) return cuda_fail(e);
+        h.t = static_cast<unsigned char *>(p);
+        h.tbytes = bytes;
+    }
+    *out = &h;  // map nodes are stable; entries are erased only by ce_release_workspaces
+    return CE_OK;
+}
+
+int run_host(const void *logits_host, const int32_t *targets_host, int64_t B, int64_t C,
+             int dtype, float *loss_host, void *grad_out, void *stream) {
+    if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_DTYPE;
+    if (!logits_host || !targets_host || !loss_host || !grad_out) return CE_ERR_NULL;
+    if (B < 1 || C < 1 || B > 0x7fffffffLL || C > 0x7fffffffLL) return CE_ERR_SHAPE;
+    const int es = dtype == CE_F32 ? 4 : 2;
+    if ((unsigned long long)B * (unsigned long long)C > (1ull << 61) / (unsigned)es)
+        return CE_ERR_SHAPE;
+    const uintptr_t lz = reinterpret_cast<uintptr_t>(logits_host);
+    const uintptr_t gz = reinterpret_cast<uintptr_t>(grad_out);
+    if (lz % es || gz % es || reinterpret_cast<uintptr_t>(targets_host) % 4 ||
+        reinterpret_cast<uintptr_t>(loss_host) % 4)
+        return CE_ERR_ALIGN;
+    const size_t nbytes = (size_t)B * (size_t)C * es;
+    if (ranges_overlap(gz, nbytes, lz, nbytes)) return CE_ERR_OVERLAP;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DeviceInfo d;
+    int rc = device_info(dev, &d);
+    if (rc != CE_OK) return rc;
+    if ((rc = check_pointer(grad_out, d)) != CE_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return cuda_fail(e);
+    if (cs != cudaStreamCaptureStatusNone) return CE_ERR_CAPTURE;
+
+    Plan pl;
+    if ((rc = make_plan(B, C, dtype, CE_PATH_AUTO, 0, &pl)) != CE_OK) return rc;
+    const size_t rows_bytes = align_up((size_t)B, 1024) * sizeof(float);
+    size_t need = kHeaderBytes + rows_bytes;
+    size_t parts_off = 0, zt_off = 0;
+    if (pl.path == CE_PATH_STREAM) {
+        parts_off = need;
+        need += align_up((size_t)B * (size_t)pl.chunks * sizeof(float2), 256);
+        zt_off = need;
+        need += align_up((size_t)B * sizeof(float), 256);
+    }
+    Workspace ws;
+    if ((rc = get_workspace(dev, s, need, &ws)) != CE_OK) return rc;
+    HostStage *h = nullptr;
+    if ((rc = host_stage(dev, s, nbytes, (size_t)B * 4, &h)) != CE_OK) return rc;
+
+    float *dloss = reinterpret_cast<float *>(ws.base + kLossSlot);
+    const uintptr_t zz = reinterpret_cast<uintptr_t>(h->z);
+    ce::ParamsEx p;
+    p.logits = h->z;
+    p.targets = reinterpret_cast<const int32_t *>(h->t);
+    p.grad = static_cast<unsigned char *>(grad_out);
+    p.loss_out = dloss;
+    p.loss_rows = reinterpret_cast<float *>(ws.base + kHeaderBytes);
+    p.ticket = reinterpret_cast<unsigned int *>(ws.base);
+    p.err = reinterpret_cast<int *>(ws.base + 4);
+    p.parts = pl.path == CE_PATH_STREAM ? reinterpret_cast<float2 *>(ws.base + parts_off) : nullptr;
+    p.zt = pl.path == CE_PATH_STREAM ? reinterpret_cast<float *>(ws.base + zt_off) : nullptr;
+    p.B = B;
+    p.C = C;
+    p.inv_b = (float)(1.0 / (double)B);
+    p.lo_clip = (uint64_t)((zz + 15) & ~(uintptr_t)15);
+    p.hi_clip = (uint64_t)((zz + nbytes) & ~(uintptr_t)15);
+    p.grad_vec_ok = ((gz - zz) % 16) == 0;
+    p.reduction = CE_REDUCE_MEAN;
+    p.grad_base = p.inv_b;
+    p.grad_scale = nullptr;
+    p.scale_per_row = 0;
+    p.softmax = 0;
+
+    if ((e = cudaMemcpyAsync(h->z, logits_host, nbytes, cudaMemcpyDefault, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->t, targets_host, (size_t)B * 4, cudaMemcpyDefault, s)) !=
+            cudaSuccess ||
+        (e = launch_plan(p, dtype, pl, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(loss_host, dloss, sizeof(float), cudaMemcpyDefault, s)) !=
+            cudaSuccess)
+        return cuda_fail(e);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? CE_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -686,6 +815,11 @@ int ce_softmax_fwd_path(const void *logits, int64_t B, int64_t C, int dtype, voi
                         void *stream, int path, int split) {
     return run(logits, nullptr, B, C, dtype, CE_REDUCE_NONE, nullptr, nullptr, probs_out, stream,
                path, split, true);
+}
+
+int ce_fwd_bwd_host(const void *logits_host, const int32_t *targets_host, int64_t B, int64_t C,
+                    int dtype, float *loss_host, void *grad_out, void *stream) {
+    return run_host(logits_host, targets_host, B, C, dtype, loss_host, grad_out, stream);
 }
 
 int ce_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int dtype,
@@ -777,12 +911,22 @@ int ce_release_workspaces(void) {
         cudaError_t e = cudaFree(kv.second.base);
         if (e != cudaSuccess) rc = cuda_fail(e);
     }
+    for (auto &kv : g_hs) {
+        HostStage &h = kv.second;
+        cudaSetDevice(kv.first.first);
+        for (void *b : {(void *)h.z, (void *)h.t})
+            if (b) {
+                cudaError_t e = cudaFree(b);
+                if (e != cudaSuccess) rc = cuda_fail(e);
+            }
+    }
     for (auto &r : g_ws_retired) {
         cudaSetDevice(r.first);
         cudaError_t e = cudaFree(r.second);
         if (e != cudaSuccess) rc = cuda_fail(e);
     }
     g_ws.clear();
+    g_hs.clear();
     g_ws_retired.clear();
     cudaSetDevice(cur);
     return rc;

@@ -96,6 +96,19 @@ def test_host_side_errors_of_the_softmax_entry_points(lib):
     assert bw(1 << 20, 1 << 24, 4, 4, 0, (1 << 24) - 16, None) == 6
 
 
+def test_host_side_errors_of_the_host_buffer_entry(lib):
+    """ce_fwd_bwd_host checks its arguments before any CUDA call as well."""
+    h = lib.ce_fwd_bwd_host
+    assert h(None, 512, 4, 4, 0, 1024, 4096, None) == 1      # NULL logits
+    assert h(256, 512, 4, 4, 0, 1024, None, None) == 1       # NULL gradient
+    assert h(256, 512, 4, 4, 0, None, 4096, None) == 1       # NULL loss
+    assert h(256, 512, 4, 4, 7, 1024, 4096, None) == 3       # dtype
+    assert h(256, 512, 0, 4, 0, 1024, 4096, None) == 2       # B = 0
+    assert h(258, 512, 4, 4, 0, 1024, 4096, None) == 4       # fp32 logits at 2 mod 4
+    assert h(256, 514, 4, 4, 0, 1024, 4096, None) == 4       # targets at 2 mod 4
+    assert h(1 << 20, 512, 4, 4, 0, 1024, (1 << 20) + 32, None) == 6  # gradient over logits
+
+
 def test_no_cpu_fallback_without_library(tmp_path):
     """The binding refuses to run when the CUDA library is absent."""
     import importlib
