@@ -25,7 +25,17 @@
  *     NaN) and its gradient is softmax/B with no one-hot term;
  *   - 1/B is applied once to the sum of the row losses (the shader divides each
  *     row's loss by B before summing; identical in exact arithmetic);
- *   - bf16 and f16 logits are widened exactly to fp64 before any arithmetic.
+ *   - bf16 and f16 logits are widened exactly to fp64 before any arithmetic
+ *     (f16 from the binary16 definition: rumus milestone M11 names f16
+ *     storage with f32 accumulation and fixes nothing more);
+ *   - the reductions sum and none, and an upstream gradient u (rumus M7a:
+ *     the backward scales the precomputed gradient by the upstream value):
+ *     the sum reduction's gradient has no 1/B, none's is d l_b / d z_b, and
+ *     u multiplies the gradient (a scalar, or one value per row for none);
+ *   - the row softmax of rumus milestone M8c (forward and backward kernels,
+ *     log-sum-exp stable; no formulas printed): p = exp(z - m) / sum exp(z - m)
+ *     and dx = p * (dy - sum_c p_c dy_c), with p and dy read in the logits'
+ *     element type.
  *
  * Accumulation is in double, in class order within a row and row order for L.
  * Rows are independent and may run on several OpenMP threads; each row's
