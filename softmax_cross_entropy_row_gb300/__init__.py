@@ -144,10 +144,33 @@ def _ptr(t) -> int:
     return 0 if t is None else t.data_ptr()
 
 
+def _check_io(logits, targets, loss_out, reduction=CE_REDUCE_MEAN, grad_scale=None,
+              device="cuda") -> None:
+    """Types, sizes and placement of the tensors a call reads or writes: the
+    C layer receives plain pointers and cannot check how large they are."""
+    import torch
+
+    B = logits.shape[0]
+    n = B if reduction == CE_REDUCE_NONE else 1
+    for name, t in (("logits", logits), ("targets", targets), ("loss_out", loss_out),
+                    ("grad_scale", grad_scale)):
+        if t is not None and t.device.type != device:
+            raise ValueError(f"{name} must be a {device.upper()} tensor")
+    if (targets is None or targets.dtype != torch.int32 or targets.dim() != 1
+            or targets.numel() != B or not targets.is_contiguous()):
+        raise ValueError("targets must be a contiguous [B] int32 tensor")
+    if (loss_out is None or loss_out.dtype != torch.float32 or loss_out.numel() < n
+            or not loss_out.is_contiguous()):
+        raise ValueError(f"loss_out must be a contiguous float32 tensor of at least {n} element(s)")
+    if grad_scale is not None and (grad_scale.dtype != torch.float32 or grad_scale.numel() != n
+                                   or not grad_scale.is_contiguous()):
+        raise ValueError(f"grad_scale must be a contiguous float32 tensor of {n} element(s)")
+
+
 def ce_fwd_bwd(logits, targets, loss_out, grad_out, stream=None) -> None:
     """Loss (one fp32 on the device) and gradient of softmax cross-entropy.
 
-    logits   [B, C] float32 or bfloat16 CUDA tensor, contiguous
+    logits   [B, C] float32, bfloat16 or float16 CUDA tensor, contiguous
     targets  [B] int32 CUDA tensor
     loss_out one-element float32 CUDA tensor
     grad_out [B, C] CUDA tensor of the logits' dtype, contiguous
@@ -164,6 +187,7 @@ def ce_fwd_bwd_path(logits, targets, loss_out, grad_out, stream=None, path=CE_PA
         raise ValueError("logits must be a contiguous [B, C] tensor")
     if grad_out.shape != logits.shape or grad_out.dtype != logits.dtype or not grad_out.is_contiguous():
         raise ValueError("grad_out must be a contiguous tensor of the logits' shape and dtype")
+    _check_io(logits, targets, loss_out)
     B, C = logits.shape
     _check(lib.ce_fwd_bwd_path(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
                                _ptr(loss_out), _ptr(grad_out), _stream_handle(stream),
@@ -182,6 +206,7 @@ def ce_fwd_bwd_ex(logits, targets, loss_out, grad_out=None, reduction=CE_REDUCE_
     if grad_out is not None and (grad_out.shape != logits.shape or grad_out.dtype != logits.dtype
                                  or not grad_out.is_contiguous()):
         raise ValueError("grad_out must be a contiguous tensor of the logits' shape and dtype")
+    _check_io(logits, targets, loss_out, reduction, grad_scale)
     B, C = logits.shape
     _check(lib.ce_fwd_bwd_ex_path(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
                                   int(reduction), _ptr(grad_scale), _ptr(loss_out),
@@ -193,6 +218,7 @@ def ce_forward(logits, targets, loss_out, reduction=CE_REDUCE_MEAN, stream=None)
     lib = load_library()
     if logits.dim() != 2 or not logits.is_contiguous():
         raise ValueError("logits must be a contiguous [B, C] tensor")
+    _check_io(logits, targets, loss_out, reduction)
     B, C = logits.shape
     _check(lib.ce_forward(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
                           int(reduction), _ptr(loss_out), _stream_handle(stream)))
@@ -200,18 +226,18 @@ def ce_forward(logits, targets, loss_out, reduction=CE_REDUCE_MEAN, stream=None)
 
 def ce_fwd_bwd_host(logits_host, targets_host, loss_host, grad_out, stream=None) -> None:
     """ce_fwd_bwd with the logits, targets and loss in host memory (CPU
-    tensors, page-locked for overlapped copies); the gradient goes to the CUDA
+    tensors, page-locked for asynchronous copies); the gradient goes to the CUDA
     tensor ``grad_out``.  ``loss_host`` is written when ``stream`` reaches the
     end of the call."""
     lib = load_library()
-    if logits_host.device.type != "cpu" or targets_host.device.type != "cpu" or \
-            loss_host.device.type != "cpu":
-        raise ValueError("logits_host, targets_host and loss_host must be CPU tensors")
     if logits_host.dim() != 2 or not logits_host.is_contiguous():
         raise ValueError("logits_host must be a contiguous [B, C] tensor")
     if grad_out.shape != logits_host.shape or grad_out.dtype != logits_host.dtype or \
             not grad_out.is_contiguous():
         raise ValueError("grad_out must be a contiguous tensor of the logits' shape and dtype")
+    _check_io(logits_host, targets_host, loss_host, device="cpu")
+    if grad_out.device.type != "cuda":
+        raise ValueError("grad_out must be a CUDA tensor")
     B, C = logits_host.shape
     _check(lib.ce_fwd_bwd_host(_ptr(logits_host), _ptr(targets_host), B, C,
                                _dtype_code(logits_host), _ptr(loss_host), _ptr(grad_out),
@@ -262,6 +288,7 @@ def ce_fwd_bwd_noalloc(logits, targets, loss_out, grad_out, stream=None) -> None
         raise ValueError("logits must be a contiguous [B, C] tensor")
     if grad_out.shape != logits.shape or grad_out.dtype != logits.dtype or not grad_out.is_contiguous():
         raise ValueError("grad_out must be a contiguous tensor of the logits' shape and dtype")
+    _check_io(logits, targets, loss_out)
     B, C = logits.shape
     _check(lib.ce_fwd_bwd_noalloc(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
                                   _ptr(loss_out), _ptr(grad_out), _stream_handle(stream)))

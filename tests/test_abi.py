@@ -127,3 +127,29 @@ def test_product_does_not_touch_the_oracle(lib):
     code = ("import sys, softmax_cross_entropy_row_gb300 as ce; ce.load_library(); "
             "assert 'oracle' not in sys.modules and 'workloads' not in sys.modules")
     subprocess.run([sys.executable, "-c", code], check=True, cwd=ROOT)
+
+
+def test_binding_checks_what_the_c_layer_cannot(lib):
+    """The wrappers refuse target, loss and upstream-gradient tensors of the
+    wrong type or size before calling the library (which sees plain pointers):
+    checked here with CPU tensors, which the device entry points refuse too."""
+    torch = pytest.importorskip("torch")
+    z = torch.zeros(4, 8)
+    t = torch.zeros(4, dtype=torch.int32)
+    loss = torch.zeros(1)
+    g = torch.zeros(4, 8)
+    with pytest.raises(ValueError, match="CUDA"):
+        ce.ce_fwd_bwd(z, t, loss, g)
+    with pytest.raises(ValueError, match="targets"):
+        ce.ce_fwd_bwd_host(z, t.long(), loss, g)
+    with pytest.raises(ValueError, match="targets"):
+        ce.ce_fwd_bwd_host(z, t[:3], loss, g)
+    with pytest.raises(ValueError, match="loss_out"):
+        ce.ce_fwd_bwd_host(z, t, torch.zeros(1, dtype=torch.float64), g)
+    with pytest.raises(ValueError, match="CUDA"):  # the gradient stays on the device
+        ce.ce_fwd_bwd_host(z, t, loss, g)
+    with pytest.raises(ValueError):  # per-row losses need B elements
+        ce._check_io(z, t, loss, ce.CE_REDUCE_NONE, device="cpu")
+    with pytest.raises(ValueError, match="grad_scale"):
+        ce._check_io(z, t, torch.zeros(4), ce.CE_REDUCE_NONE, torch.zeros(1), device="cpu")
+    ce._check_io(z, t, torch.zeros(4), ce.CE_REDUCE_NONE, torch.zeros(4), device="cpu")
