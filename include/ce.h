@@ -89,12 +89,14 @@ typedef enum {
  *   stream    a cudaStream_t (NULL = the legacy default stream).
  *
  * Pointers must be aligned to their element size (4 bytes for fp32 and
- * int32, 2 for bf16) and accessible from the current device.  The call is
- * asynchronous on `stream` and never synchronises, except that the first call
- * on a stream (or the first with a larger B than before) allocates the
- * stream's small workspace (B floats plus counters) and waits for that
- * stream's earlier work when it has to grow it.  Calls on one stream are
- * ordered; calls on different streams use different workspaces and may run
+ * int32, 2 for bf16 and f16) and accessible from the current device.  The call is
+ * asynchronous on `stream`; the first call on a stream (or the first that
+ * needs more than before: a larger B, or the streaming path's partials)
+ * allocates the stream's small workspace (B floats plus counters) with
+ * cudaMalloc, which may synchronise the device.  The outgrown workspace is
+ * kept, not freed, until ce_release_workspaces (kernels in flight and CUDA
+ * graphs captured earlier still use it).  Calls on one stream are ordered;
+ * calls on different streams use different workspaces and may run
  * concurrently.  Returns a ce_status.
  */
 int ce_fwd_bwd(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
