@@ -153,3 +153,23 @@ def test_binding_checks_what_the_c_layer_cannot(lib):
     with pytest.raises(ValueError, match="grad_scale"):
         ce._check_io(z, t, torch.zeros(4), ce.CE_REDUCE_NONE, torch.zeros(1), device="cpu")
     ce._check_io(z, t, torch.zeros(4), ce.CE_REDUCE_NONE, torch.zeros(4), device="cpu")
+
+
+def test_the_abi_from_plain_c(lib, tmp_path):
+    """A C program that includes include/ce.h and links libce.so (no Python
+    in between) gets the documented status codes from every entry point."""
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(ce.build())
+    exe = tmp_path / "abi_from_c"
+    src = os.path.join(ROOT, "tests", "c", "abi_from_c.c")
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    src, "-o", str(exe), f"-L{libdir}", "-lce", f"-Wl,-rpath,{libdir}"],
+                   check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "ok"
+
