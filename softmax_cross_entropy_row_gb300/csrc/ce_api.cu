@@ -783,6 +783,7 @@ int run_host(const void *logits_host, const int32_t *targets_host, int64_t B, in
     p.inv_b = (float)(1.0 / (double)B);
     p.lo_clip = (uint64_t)((zz + 15) & ~(uintptr_t)15);
     p.hi_clip = (uint64_t)((zz + nbytes) & ~(uintptr_t)15);
+    if (p.hi_clip < p.lo_clip) p.hi_clip = p.lo_clip;
     p.grad_vec_ok = ((gz - zz) % 16) == 0;
     p.reduction = CE_REDUCE_MEAN;
     p.grad_base = p.inv_b;
