@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <climits>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -103,7 +104,7 @@ struct Plan {
     int slot_bytes = 0;
     long long slice = 0;  // classes per slice (split path)
     int rows_per_tile = 0;
-    int per_sm = 1;       // warp path: the build for 1 or 2 resident CTAs per SM
+    int per_sm = 1;       // warp path: the build for 1, 2 or 3 resident CTAs per SM
     int vecs = 8;         // split path: 16-byte vectors per thread (8, 12 or 16)
     bool pipe = false;    // split path: the pipelined kernel (slices of at most 8 vectors)
     long long chunks = 0; // stream path
@@ -115,7 +116,7 @@ constexpr long long kWarpTileTarget = 2048;    // bytes of rows per warp tile
 
 int round_up(long long v, long long a) { return (int)((v + a - 1) / a * a); }
 
-// Tuning knob: CE_WARP_PER_SM=1 or 2 forces the warp path's CTAs per SM
+// Tuning knob: CE_WARP_PER_SM=1, 2 or 3 forces the warp path's CTAs per SM
 // (0 or unset: chosen from the shape).  Read once.
 int warp_per_sm_override() {
     static const int n = [] {
@@ -153,22 +154,35 @@ int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, 
     if (R > B) R = B;
     const int slot_bytes = round_up(R * row_bytes + 32, 128);
     const long long ntiles = (B + R - 1) / R;
-    const int NW = ce::kWarpKernelWarps;
-    // Two CTAs per SM with one staged tile per warp when every tile then has
-    // a warp of its own (all copies in flight at once, twice the warps to hide
-    // latency); otherwise one CTA per SM with a ring of up to four tiles per warp.
+    // Two or three CTAs per SM with one staged tile per warp when every tile
+    // then has a warp of its own (all copies in flight at once): 2 x 16 or
+    // 3 x 9 warps, whichever leaves fewer tiles on the busiest SM (2 x 16 on a
+    // tie); otherwise one CTA per SM with a ring of up to four tiles per warp.
+    // The multi-CTA builds hold four 16-byte vectors per lane without
+    // spilling; fp32 rows of up to eight (a few spilled registers) still ran
+    // faster there than with one CTA per SM (4096 x 1000 fp32: 10.6 vs 11.3 us).
     int want = 1;
     int slots = 1;
-    const int half_budget = d.smem_optin / 2 - kStaticSmemReserve;
     const int force = warp_per_sm_override();
-    // the two-CTA build holds four 16-byte vectors per lane without spilling;
-    // fp32 rows of up to eight (a few spilled registers) still ran faster
-    // there than with one CTA per SM (4096 x 1000 fp32: 10.6 vs 11.3 us)
     const bool light = (C * es / 16 + 31) / 32 <= (es == 4 ? 8 : 4);
-    if (force != 1 && (force == 2 || (ntiles <= 2LL * NW * d.sms && light)) &&
-        (long long)slot_bytes * NW <= half_budget) {
-        want = 2;
-    } else {
+    auto fits = [&](int per_sm) {
+        return (long long)slot_bytes * ce::warp_kernel_warps(per_sm) <=
+               d.smem_optin / per_sm - kStaticSmemReserve;
+    };
+    auto busiest = [&](int per_sm) {  // tiles on the busiest SM, all CTAs resident
+        const long long nw = ce::warp_kernel_warps(per_sm);
+        const long long ctas = (ntiles + nw - 1) / nw;
+        if (!fits(per_sm) || ctas > (long long)per_sm * d.sms) return LLONG_MAX;
+        return (ctas + d.sms - 1) / d.sms * nw;
+    };
+    if (force == 2 || force == 3) {
+        if (fits(force)) want = force;
+    } else if (force != 1 && light) {
+        const long long b2 = busiest(2), b3 = busiest(3);
+        if (b2 != LLONG_MAX || b3 != LLONG_MAX) want = b3 < b2 ? 3 : 2;
+    }
+    const int NW = ce::warp_kernel_warps(want);
+    if (want == 1) {
         const int budget = d.smem_optin - kStaticSmemReserve;
         slots = ce::kMaxWarpSlots;
         while (slots > 1 && (long long)slots * slot_bytes * NW > budget) --slots;

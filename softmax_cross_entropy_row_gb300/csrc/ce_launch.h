@@ -16,6 +16,12 @@ cudaError_t ensure_smem_attr(const void *func, int smem);
 constexpr int kSplitThreads = 512;
 constexpr int kSplitMaxVecs = 16;  // 16-byte vectors per thread: slices of at most 128 KB
 constexpr int kWarpKernelWarps = 16;
+// The warp path's build for three resident CTAs per SM has 9 warps each (27
+// per SM), so a batch of up to 27 rows per SM spreads evenly over the SMs.
+constexpr int kWarpKernelWarps3 = 9;
+__host__ __device__ constexpr int warp_kernel_warps(int per_sm) {
+    return per_sm >= 3 ? kWarpKernelWarps3 : kWarpKernelWarps;
+}
 constexpr int kStreamThreads = 256;
 constexpr int kStreamPerThread = 16;  // elements each thread keeps in registers
 constexpr int kStreamChunk = kStreamThreads * kStreamPerThread;
@@ -45,8 +51,8 @@ cudaError_t launch_split_pipe(const ParamsEx &p, int dtype, int K, int ctas, int
 cudaError_t split_pipe_max_clusters(int dtype, int K, int smem, int *clusters);
 
 // Warp-per-row path: tiles of `rows_per_tile` consecutive rows, `slots` tiles
-// staged per warp; `per_sm` (1 or 2) selects the build made for that many
-// resident CTAs per SM.
+// staged per warp; `per_sm` (1, 2 or 3) selects the build made for that many
+// resident CTAs per SM (16 warps each for 1 and 2, 9 for 3).
 cudaError_t launch_rows_warp(const ParamsEx &p, int dtype, int per_sm, int ctas, int slots,
                              int rows_per_tile, int slot_bytes, int smem, cudaStream_t s);
 cudaError_t rows_warp_max_ctas_per_sm(int dtype, int per_sm, long long C, int smem, int *ctas);

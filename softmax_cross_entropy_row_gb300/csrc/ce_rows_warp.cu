@@ -19,10 +19,10 @@ namespace ce {
 namespace {
 
 template <typename T, int MAXV, int MINB, typename P>
-__global__ void __launch_bounds__(kWarpKernelWarps * 32, MINB)
+__global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
     rows_warp_kernel(P p, int slots, int rows_per_tile, int slot_bytes) {
     using E = Elem<T>;
-    constexpr int NW = kWarpKernelWarps;
+    constexpr int NW = warp_kernel_warps(MINB);
     constexpr int ES = E::kBytes;
     constexpr int W = E::kVec;
     constexpr int W2 = W / 2;
@@ -304,7 +304,7 @@ cudaError_t launch_p(const P &p, int ctas, int slots, int rows_per_tile, int slo
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas, 1, 1);
-    cfg.blockDim = dim3(kWarpKernelWarps * 32, 1, 1);
+    cfg.blockDim = dim3(warp_kernel_warps(MINB) * 32, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -330,7 +330,8 @@ cudaError_t occ_v(int smem, int *ctas) {
     auto kern = rows_warp_kernel<T, MAXV, MINB, Params>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, kWarpKernelWarps * 32, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, warp_kernel_warps(MINB) * 32,
+                                                         smem);
 }
 
 // Vectors per lane: a row of C elements holds at most C*ES/16 whole vectors.
@@ -364,13 +365,15 @@ cudaError_t occ_m(long long C, int smem, int *ctas) {
 template <typename T>
 cudaError_t launch_t(const ParamsEx &p, int per_sm, int ctas, int slots, int rows_per_tile,
                      int slot_bytes, int smem, cudaStream_t s) {
-    if (per_sm >= 2) return launch_m<T, 2>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+    if (per_sm >= 3) return launch_m<T, 3>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
+    if (per_sm == 2) return launch_m<T, 2>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
     return launch_m<T, 1>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
 }
 
 template <typename T>
 cudaError_t occ_t(int per_sm, long long C, int smem, int *ctas) {
-    if (per_sm >= 2) return occ_m<T, 2>(C, smem, ctas);
+    if (per_sm >= 3) return occ_m<T, 3>(C, smem, ctas);
+    if (per_sm == 2) return occ_m<T, 2>(C, smem, ctas);
     return occ_m<T, 1>(C, smem, ctas);
 }
 
