@@ -45,8 +45,8 @@ typedef enum {
     CE_ERR_CAPTURE = 8,  /* the call needs to grow its workspace while the
                             stream is being captured; call once uncaptured first */
     CE_ERR_PATH = 9,     /* a forced path/split cannot run this shape           */
-    CE_ERR_SCRATCH = 10, /* ce_fwd_bwd_noalloc: the shape needs more scratch than
-                            its static array holds                               */
+    CE_ERR_SCRATCH = 10, /* ce_fwd_bwd_noalloc: more rows than its static scratch
+                            array holds                                          */
     CE_ERR_REDUCTION = 11 /* reduction is not a ce_reduction                    */
 } ce_status;
 
@@ -63,8 +63,12 @@ typedef enum {
     CE_PATH_ROWS_WARP = 1, /* small rows: one warp per row, rows staged by TMA       */
     CE_PATH_ROW_SPLIT = 2, /* rows (or row slices across a cluster of `split` CTAs)
                               staged once in shared memory by TMA                    */
-    CE_PATH_STREAM = 3     /* rows too large for a cluster's shared memory: chunk
-                              partials, then a recompute-and-write pass               */
+    CE_PATH_STREAM = 3,    /* any row: chunk partials, then a recompute-and-write
+                              pass (a second launch; logits read twice from HBM)    */
+    CE_PATH_ROW_TWOPASS = 4 /* any row, one CTA per row: a running max and sum over
+                              chunks staged by TMA, then the gradient from a second
+                              read of the row (served by L2).  CE_PATH_AUTO takes it
+                              for rows one CTA cannot hold in registers             */
 } ce_path;
 
 /*
@@ -246,10 +250,9 @@ int ce_release_workspaces(void);
  * statically sized device array of the library, which every GPU that loads
  * the library holds until the process exits.
  *
- *   Arguments, layout, ownership and results are those of ce_fwd_bwd.
- *   Limits: B <= 262144, and rows short enough to be staged in shared memory
- *   (under 64 KB per CTA of a cluster of up to 8: C <= 131008 fp32 or 262080
- *   bf16 classes); anything larger returns CE_ERR_SCRATCH before any launch.
+ *   Arguments, layout, ownership, checks and results are those of ce_fwd_bwd
+ *   (the same kernels, the same bits).  Limit: B <= 262144 rows, any C; a
+ *   larger B returns CE_ERR_SCRATCH before any launch.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.  Every call shares the one array and clears its

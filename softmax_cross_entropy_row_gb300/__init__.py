@@ -32,13 +32,14 @@ CE_PATH_AUTO = 0
 CE_PATH_ROWS_WARP = 1
 CE_PATH_ROW_SPLIT = 2
 CE_PATH_STREAM = 3
+CE_PATH_ROW_TWOPASS = 4
 
 CE_REDUCE_MEAN = 0
 CE_REDUCE_SUM = 1
 CE_REDUCE_NONE = 2
 
 PATH_NAMES = {CE_PATH_ROWS_WARP: "rows_warp", CE_PATH_ROW_SPLIT: "row_split",
-              CE_PATH_STREAM: "stream"}
+              CE_PATH_STREAM: "stream", CE_PATH_ROW_TWOPASS: "row_twopass"}
 
 STATUS = {0: "CE_OK", 1: "CE_ERR_NULL", 2: "CE_ERR_SHAPE", 3: "CE_ERR_DTYPE",
           4: "CE_ERR_ALIGN", 5: "CE_ERR_CUDA", 6: "CE_ERR_OVERLAP", 7: "CE_ERR_POINTER",
@@ -49,6 +50,15 @@ EXPORTS = ("ce_fwd_bwd", "ce_fwd_bwd_path", "ce_query_plan", "ce_get_device_erro
            "ce_release_workspaces", "ce_status_string", "ce_last_cuda_error",
            "ce_fwd_bwd_noalloc", "ce_fwd_bwd_ex", "ce_fwd_bwd_ex_path", "ce_forward",
            "ce_softmax_fwd", "ce_softmax_fwd_path", "ce_softmax_bwd", "ce_fwd_bwd_host")
+# Symbols declared in include/ce_testing.h (test hooks).
+TEST_EXPORTS = ("ce_fwd_bwd_test",)
+
+
+class TestHooks(ctypes.Structure):
+    """ce_test_hooks of include/ce_testing.h."""
+
+    _fields_ = [("skip_copy_row", ctypes.c_int64), ("wait_limit_cycles", ctypes.c_int64),
+                ("grad_f32_out", ctypes.c_void_p)]
 
 
 class CEError(RuntimeError):
@@ -104,6 +114,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.ce_softmax_fwd_path.restype = ci
     lib.ce_softmax_bwd.argtypes = [vp, vp, i64, i64, ci, vp, vp]
     lib.ce_softmax_bwd.restype = ci
+    lib.ce_fwd_bwd_test.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp, ci, ci,
+                                    ctypes.POINTER(TestHooks)]
+    lib.ce_fwd_bwd_test.restype = ci
     if path is None:
         _lib = lib
     return lib
@@ -292,6 +305,31 @@ def ce_fwd_bwd_noalloc(logits, targets, loss_out, grad_out, stream=None) -> None
     B, C = logits.shape
     _check(lib.ce_fwd_bwd_noalloc(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
                                   _ptr(loss_out), _ptr(grad_out), _stream_handle(stream)))
+
+
+def ce_fwd_bwd_test(logits, targets, loss_out, grad_out, stream=None, path=CE_PATH_AUTO, split=0,
+                    skip_copy_row=-1, wait_limit_cycles=0, grad_f32_out=None) -> None:
+    """ce_fwd_bwd_path with the test hooks of include/ce_testing.h: leave out
+    the copy of one row (its bounded wait must give up), shorten the copy
+    waits, or record the fp32 gradient before rounding (``grad_f32_out``, a
+    contiguous float32 CUDA tensor of the logits' shape).  Tests only."""
+    lib = load_library()
+    if logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous [B, C] tensor")
+    if grad_out.shape != logits.shape or grad_out.dtype != logits.dtype or not grad_out.is_contiguous():
+        raise ValueError("grad_out must be a contiguous tensor of the logits' shape and dtype")
+    _check_io(logits, targets, loss_out)
+    import torch
+
+    if grad_f32_out is not None and (grad_f32_out.shape != logits.shape or not
+                                     grad_f32_out.is_contiguous() or
+                                     grad_f32_out.dtype != torch.float32):
+        raise ValueError("grad_f32_out must be a contiguous float32 tensor of the logits' shape")
+    hooks = TestHooks(int(skip_copy_row), int(wait_limit_cycles), _ptr(grad_f32_out) or None)
+    B, C = logits.shape
+    _check(lib.ce_fwd_bwd_test(_ptr(logits), _ptr(targets), B, C, _dtype_code(logits),
+                               _ptr(loss_out), _ptr(grad_out), _stream_handle(stream), int(path),
+                               int(split), ctypes.byref(hooks)))
 
 
 def ce_query_plan(B: int, C: int, dtype: int) -> dict:

@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "../../include/ce.h"
+#include "../../include/ce_testing.h"
 #include "ce_launch.h"
 
 namespace {
@@ -290,6 +291,46 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     return CE_OK;
 }
 
+// Tuning knob: CE_TWOPASS_HINT=0 leaves the L2 eviction hints off the
+// two-pass path's copies (to measure what they are worth).  Read once.
+int twopass_hint() {
+    static const int h = [] {
+        const char *e = getenv("CE_TWOPASS_HINT");
+        return (e && atoi(e) == 0) ? 0 : 1;
+    }();
+    return h;
+}
+
+// Two-pass path: one CTA per SM, a row at a time, with a ring of chunks as
+// deep as shared memory allows (7 x 32 KB on GB300: deeper than one pass over
+// a 200 KB row, so the next row's first pass is read from HBM while the
+// current row's second pass is served by L2); any row length.
+int plan_twopass(long long B, const DeviceInfo &d, int dtype, Plan *pl) {
+    const int chb = ce::kTwoPassChunkBytes;
+    int nslots = (d.smem_optin - kStaticSmemReserve) / chb;
+    if (nslots > ce::kTwoPassMaxSlots) nslots = ce::kTwoPassMaxSlots;
+    if (nslots < 2) return CE_ERR_PATH;
+    const int smem = nslots * chb;
+    int per_sm = 0;
+    int rc = cached_occupancy(
+        dtype, CE_PATH_ROW_TWOPASS, 0, smem,
+        [&](int *v) { return ce::twopass_max_ctas_per_sm(dtype, smem, v); }, &per_sm);
+    if (rc != CE_OK) return rc;
+    if (per_sm < 1) return CE_ERR_PATH;
+    long long ctas = (long long)d.sms;
+    if (ctas > B) ctas = B;
+    pl->path = CE_PATH_ROW_TWOPASS;
+    pl->split = 1;
+    pl->ctas = (int)ctas;
+    pl->threads = ce::kTwoPassThreads;
+    pl->smem = smem;
+    pl->launches = 1;
+    pl->nslots = nslots;
+    pl->slot_bytes = chb;
+    pl->per_sm = 1;
+    return CE_OK;
+}
+
 int plan_stream(long long B, long long C, Plan *pl) {
     const long long chunks = (C + ce::kStreamChunk - 1) / ce::kStreamChunk;
     if (B * chunks > 0x7fffffffLL) return CE_ERR_SHAPE;
@@ -318,6 +359,8 @@ cudaError_t launch_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, cudaSt
                                         pl.slot_bytes, pl.smem, s);
         case CE_PATH_ROW_SPLIT:
             return launch_split_plan(p, dtype, pl, s);
+        case CE_PATH_ROW_TWOPASS:
+            return ce::launch_twopass(p, dtype, pl.ctas, pl.nslots, pl.smem, twopass_hint(), s);
         default:
             return ce::launch_stream(p, dtype, pl.chunks, s);
     }
@@ -334,15 +377,21 @@ int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl
     const long long row_bytes = C * es;
     switch (path) {
         case CE_PATH_AUTO:
+            // rows of at most 8 KB: a warp each; rows one CTA holds in
+            // registers: the split kernel at K = 1; longer rows: two passes
+            // through one CTA (measured faster on GB300 than splitting a row
+            // across a cluster or the streaming path)
             if (row_bytes <= kWarpRowMax) return plan_warp(B, C, es, d, dtype, pl);
             rc = plan_split(B, C, es, d, dtype, 0, pl);
-            if (rc == CE_ERR_PATH) return plan_stream(B, C, pl);
-            return rc;
+            if (rc == CE_OK && pl->split == 1) return rc;
+            if (rc != CE_OK && rc != CE_ERR_PATH) return rc;
+            return plan_twopass(B, d, dtype, pl);
         case CE_PATH_ROWS_WARP: return plan_warp(B, C, es, d, dtype, pl);
         case CE_PATH_ROW_SPLIT: return plan_split(B, C, es, d, dtype, split, pl);
         case CE_PATH_STREAM:
             if (split != 0 && split != ce::kStreamChunk) return CE_ERR_PATH;
             return plan_stream(B, C, pl);
+        case CE_PATH_ROW_TWOPASS: return plan_twopass(B, d, dtype, pl);
         default: return CE_ERR_PATH;
     }
 }
@@ -432,9 +481,10 @@ int check_pointer(const void *p, const DeviceInfo &d) {
 // sum) or [B] fp32 (none).  loss_out: one fp32 (mean, sum) or [B] (none).
 // softmax: the row softmax forward -- no targets and no loss; grad_out
 // receives softmax(z_b).
+// hooks: the test entry point's (NULL for every other call).
 int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
         int reduction, const float *grad_scale, float *loss_out, void *grad_out, void *stream,
-        int path, int split, bool softmax = false) {
+        int path, int split, bool softmax = false, const ce_test_hooks *hooks = nullptr) {
     if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_DTYPE;
     if (softmax) {
         if (!logits || !grad_out) return CE_ERR_NULL;
@@ -471,6 +521,17 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
             return CE_ERR_OVERLAP;
     }
 
+    float *grad_f32 = hooks ? hooks->grad_f32_out : nullptr;
+    if (grad_f32) {
+        const uintptr_t fz = reinterpret_cast<uintptr_t>(grad_f32);
+        const size_t fbytes = (size_t)B * (size_t)C * 4;
+        if (fz % 4) return CE_ERR_ALIGN;
+        if (ranges_overlap(fz, fbytes, lz, nbytes) || ranges_overlap(fz, fbytes, tz, (size_t)B * 4) ||
+            (grad_out && ranges_overlap(fz, fbytes, gz, nbytes)) ||
+            (loss_out && ranges_overlap(fz, fbytes, oz, per_row)))
+            return CE_ERR_OVERLAP;
+    }
+
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -478,12 +539,16 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     int rc = device_info(dev, &d);
     if (rc != CE_OK) return rc;
     for (const void *ptr : {logits, (const void *)targets, (const void *)loss_out,
-                            (const void *)grad_out, (const void *)grad_scale}) {
+                            (const void *)grad_out, (const void *)grad_scale,
+                            (const void *)grad_f32}) {
         if (ptr && (rc = check_pointer(ptr, d)) != CE_OK) return rc;
     }
 
     Plan pl;
     if ((rc = make_plan(B, C, dtype, path, split, &pl)) != CE_OK) return rc;
+    const bool hooked = hooks && (hooks->skip_copy_row >= 0 || hooks->wait_limit_cycles > 0 ||
+                                  hooks->grad_f32_out);
+    if (hooked && pl.path == CE_PATH_STREAM) return CE_ERR_PATH;  // stages nothing
 
     const size_t rows_bytes = align_up((size_t)B, 1024) * sizeof(float);
     size_t need = kHeaderBytes + rows_bytes;
@@ -522,6 +587,11 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     p.grad_scale = grad_scale;
     p.scale_per_row = grad_scale != nullptr && reduction == CE_REDUCE_NONE;
     p.softmax = softmax ? 1 : 0;
+    if (hooks) {
+        if (hooks->wait_limit_cycles > 0) p.copy_wait_limit = hooks->wait_limit_cycles;
+        p.skip_copy_row = hooks->skip_copy_row >= 0 ? hooks->skip_copy_row : -1;
+        p.grad_f32 = grad_f32;
+    }
 
     if ((e = launch_plan(p, dtype, pl, s)) != cudaSuccess) return cuda_fail(e);
     e = cudaGetLastError();
@@ -582,7 +652,8 @@ int run_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C
     if (lz % es || gz % es || tz % 4 || oz % 4) return CE_ERR_ALIGN;
     const size_t nbytes = (size_t)B * (size_t)C * es;
     if (ranges_overlap(gz, nbytes, lz, nbytes) || ranges_overlap(gz, nbytes, tz, (size_t)B * 4) ||
-        ranges_overlap(gz, nbytes, oz, 4))
+        ranges_overlap(gz, nbytes, oz, 4) || ranges_overlap(oz, 4, lz, nbytes) ||
+        ranges_overlap(oz, 4, tz, (size_t)B * 4))
         return CE_ERR_OVERLAP;
 
     int dev = 0;
@@ -595,10 +666,10 @@ int run_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C
                             (const void *)grad_out}) {
         if ((rc = check_pointer(ptr, d)) != CE_OK) return rc;
     }
+    // Every plan the planner makes for itself (warp, split at K = 1, two-pass)
+    // needs no scratch beyond the ticket, the counters and the row losses.
     Plan pl;
     if ((rc = make_plan(B, C, dtype, CE_PATH_AUTO, 0, &pl)) != CE_OK) return rc;
-    // the streaming path needs per-chunk partials the static scratch does not hold
-    if (pl.path == CE_PATH_STREAM) return CE_ERR_SCRATCH;
 
     unsigned char *base = nullptr;
     if ((rc = noalloc_scratch(dev, &base)) != CE_OK) return rc;
@@ -630,11 +701,7 @@ int run_noalloc(const void *logits, const int32_t *targets, int64_t B, int64_t C
     p.scale_per_row = 0;
     p.softmax = 0;
 
-    if (pl.path == CE_PATH_ROWS_WARP)
-        e = ce::launch_rows_warp(p, dtype, pl.per_sm, pl.ctas, pl.nslots, pl.rows_per_tile,
-                                 pl.slot_bytes, pl.smem, s);
-    else
-        e = launch_split_plan(p, dtype, pl, s);
+    e = launch_plan(p, dtype, pl, s);
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
@@ -876,6 +943,14 @@ int ce_forward(const void *logits, const int32_t *targets, int64_t B, int64_t C,
                CE_PATH_AUTO, 0);
 }
 
+int ce_fwd_bwd_test(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dtype,
+                    float *loss_out, void *grad_out, void *stream, int path, int split,
+                    const ce_test_hooks *hooks) {
+    if (!grad_out) return CE_ERR_NULL;
+    return run(logits, targets, B, C, dtype, CE_REDUCE_MEAN, nullptr, loss_out, grad_out, stream,
+               path, split, false, hooks);
+}
+
 int ce_query_plan(int64_t B, int64_t C, int dtype, int *path, int *split, int *ctas,
                   int *threads, int *smem_bytes, int *launches) {
     if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_DTYPE;
@@ -960,8 +1035,7 @@ const char *ce_status_string(int status) {
         case CE_ERR_CAPTURE: return "workspace must grow while the stream is being captured";
         case CE_ERR_PATH: return "the forced path cannot run this shape";
         case CE_ERR_SCRATCH:
-            return "shape exceeds the static scratch of ce_fwd_bwd_noalloc (B <= 262144, "
-                   "rows held in shared memory)";
+            return "more rows than the static scratch of ce_fwd_bwd_noalloc holds (B <= 262144)";
         case CE_ERR_REDUCTION: return "reduction is not a ce_reduction";
         default: return "unknown status";
     }

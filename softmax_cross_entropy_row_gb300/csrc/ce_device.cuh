@@ -57,6 +57,11 @@ struct ParamsEx : Params {
     const float *grad_scale;      // nullptr (1), one fp32, or [B] fp32 (scale_per_row)
     int scale_per_row;
     int softmax;                  // 1: row softmax forward (no targets, no loss; grad = probabilities)
+    // Test hooks (the library's test entry point sets them; the defaults
+    // leave every kernel as it is):
+    long long copy_wait_limit = kWaitLimitCycles;  // limit of the waits for row copies
+    long long skip_copy_row = -1;  // the copy holding this row is never issued
+    float *grad_f32 = nullptr;     // [B][C] fp32: the gradient before its rounding
 };
 
 constexpr int kReduceMean = 0;
@@ -105,7 +110,36 @@ __device__ __forceinline__ float row_grad_factor(const ParamsEx &p, float scalar
 // The plain call, which runs the Params build of the kernels.
 inline bool is_plain(const ParamsEx &p) {
     return p.reduction == kReduceMean && p.grad_scale == nullptr && p.grad != nullptr &&
-           !p.softmax;
+           !p.softmax && p.copy_wait_limit == kWaitLimitCycles && p.skip_copy_row < 0 &&
+           p.grad_f32 == nullptr;
+}
+
+// Test hooks; the plain build has none.
+__host__ __device__ __forceinline__ constexpr long long copy_wait_limit(const Params &) {
+    return kWaitLimitCycles;
+}
+__host__ __device__ __forceinline__ long long copy_wait_limit(const ParamsEx &p) {
+    return p.copy_wait_limit;
+}
+// Whether the copy of rows [r0, r1) is left out (its wait can only give up).
+__host__ __device__ __forceinline__ constexpr bool skips_copy(const Params &, long long,
+                                                              long long) {
+    return false;
+}
+__host__ __device__ __forceinline__ bool skips_copy(const ParamsEx &p, long long r0,
+                                                    long long r1) {
+    return p.skip_copy_row >= r0 && p.skip_copy_row < r1;
+}
+__host__ __device__ __forceinline__ constexpr float *grad_f32_of(const Params &) {
+    return nullptr;
+}
+__host__ __device__ __forceinline__ float *grad_f32_of(const ParamsEx &p) { return p.grad_f32; }
+
+// Records the fp32 gradient value v of the element whose gradient lives at
+// byte `g` of p.grad (before it is rounded to the logits' type).
+template <int ES, typename P>
+__device__ __forceinline__ void grad_f32_store(const P &p, const unsigned char *g, float v) {
+    if (float *d = grad_f32_of(p)) d[(g - p.grad) / ES] = v;
 }
 
 // Packed fp32 pairs (Blackwell f32x2 arithmetic: each half is rounded exactly
@@ -324,6 +358,39 @@ struct Elem<__half> {
     }
 };
 
+// Element d of a 16-byte vector of type E, widened to fp32 (selects, no
+// indexing).
+template <typename E>
+__device__ __forceinline__ float element_of(const uint4 &w, int d) {
+    if constexpr (E::kVec == 4) {
+        const uint32_t q = (d & 2) ? ((d & 1) ? w.w : w.z) : ((d & 1) ? w.y : w.x);
+        return __uint_as_float(q);
+    } else {
+        const uint32_t q = (d & 4) ? ((d & 2) ? w.w : w.z) : ((d & 2) ? w.y : w.x);
+        return E::widen((uint16_t)((d & 1) ? (q >> 16) : (q & 0xffffu)));
+    }
+}
+
+// The vector w with its element d set to -inf.
+template <typename E>
+__device__ __forceinline__ uint4 with_neg_inf(uint4 w, int d) {
+    if constexpr (E::kVec == 4) {
+        if (d == 0) w.x = E::kNegInfWord;
+        if (d == 1) w.y = E::kNegInfWord;
+        if (d == 2) w.z = E::kNegInfWord;
+        if (d == 3) w.w = E::kNegInfWord;
+    } else {
+        const uint32_t mask = (d & 1) ? 0xffff0000u : 0x0000ffffu;
+        const uint32_t ninf = E::kNegInfWord & mask;
+        const int q = d >> 1;
+        if (q == 0) w.x = (w.x & ~mask) | ninf;
+        if (q == 1) w.y = (w.y & ~mask) | ninf;
+        if (q == 2) w.z = (w.z & ~mask) | ninf;
+        if (q == 3) w.w = (w.w & ~mask) | ninf;
+    }
+    return w;
+}
+
 // ---------------------------------------------------------------- arithmetic
 
 __device__ __forceinline__ float ex2(float x) {
@@ -425,16 +492,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // warps that compute.
 constexpr int kPollsPerClockRead = 8;
 
-// Wait for phase `parity` of an mbarrier, for at most kWaitLimitCycles (plus
-// at most kPollsPerClockRead suspended polls).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier, for at most `limit` cycles (plus at
+// most kPollsPerClockRead suspended polls).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          long long limit = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
 #pragma unroll
         for (int i = 0; i < kPollsPerClockRead; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > kWaitLimitCycles) return false;
+        if (clock64() - t0 > limit) return false;
+    }
+}
+
+// Wait for phase `parity` of an mbarrier unless the shared flag `*flag`
+// becomes non-zero first: 1 when the phase completed, 0 when the flag was
+// seen, -1 after `limit` cycles.
+__device__ __forceinline__ int mbar_wait_or_flag(uint64_t *bar, uint32_t parity,
+                                                 const int *flag, long long limit) {
+    if (mbar_try_wait(bar, parity)) return 1;
+    const long long t0 = clock64();
+    for (;;) {
+#pragma unroll
+        for (int i = 0; i < kPollsPerClockRead; ++i)
+            if (mbar_try_wait(bar, parity)) return 1;
+        if (*reinterpret_cast<const volatile int *>(flag) != 0) return 0;
+        if (clock64() - t0 > limit) return -1;
     }
 }
 
@@ -447,6 +531,30 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
             "r"(smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// The same copy with an L2 eviction policy (a createpolicy value) for the
+// lines it reads.
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 eviction policies covering every access made with them: lines to keep
+// (read again soon) and lines to drop first (read for the last time).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 // One TMA bulk copy of this CTA's shared memory to global memory, in the

@@ -57,6 +57,20 @@ cudaError_t launch_rows_warp(const ParamsEx &p, int dtype, int per_sm, int ctas,
                              int rows_per_tile, int slot_bytes, int smem, cudaStream_t s);
 cudaError_t rows_warp_max_ctas_per_sm(int dtype, int per_sm, long long C, int smem, int *ctas);
 
+// Two-pass row path (ce_row_twopass.cu): one CTA per SM, a row at a time,
+// rows of any length streamed twice through a ring of `nslots` chunks of
+// kTwoPassChunkBytes (the second pass served by L2); kTwoPassConsumerWarps
+// consumer warps and one producer warp.  `hint` = 1: L2 eviction hints on the
+// copies (keep for the first pass, drop first for the second).
+constexpr int kTwoPassConsumerWarps = 16;
+constexpr int kTwoPassVecs = 4;  // 16-byte vectors per consumer thread per chunk
+constexpr int kTwoPassChunkBytes = kTwoPassConsumerWarps * 32 * kTwoPassVecs * 16;
+constexpr int kTwoPassThreads = (kTwoPassConsumerWarps + 1) * 32;
+constexpr int kTwoPassMaxSlots = 16;
+cudaError_t launch_twopass(const ParamsEx &p, int dtype, int ctas, int nslots, int smem, int hint,
+                           cudaStream_t s);
+cudaError_t twopass_max_ctas_per_sm(int dtype, int smem, int *ctas);
+
 // Streaming path: pass A (chunk partials) and pass B (combine, gradient, loss).
 cudaError_t launch_stream(const ParamsEx &p, int dtype, long long chunks, cudaStream_t s);
 

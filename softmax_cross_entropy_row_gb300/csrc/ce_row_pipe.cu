@@ -73,18 +73,6 @@ __device__ __forceinline__ void exps_of(const uint4 &xv, unsigned long long (&e2
     }
 }
 
-// Element d of a 16-byte vector, widened to fp32 (selects, no indexing).
-template <typename E>
-__device__ __forceinline__ float element_of(const uint4 &w, int d) {
-    if constexpr (E::kVec == 4) {
-        const uint32_t q = (d & 2) ? ((d & 1) ? w.w : w.z) : ((d & 1) ? w.y : w.x);
-        return __uint_as_float(q);
-    } else {
-        const uint32_t q = (d & 4) ? ((d & 2) ? w.w : w.z) : ((d & 2) ? w.y : w.x);
-        return E::widen((uint16_t)((d & 1) ? (q >> 16) : (q & 0xffffu)));
-    }
-}
-
 template <typename T, int K, int NT, int VPT, typename P>
 __global__ void __launch_bounds__(NT, 1)
     row_pipe_kernel(P p, int nslots, int slot_bytes, long long SE) {
@@ -152,6 +140,7 @@ __global__ void __launch_bounds__(NT, 1)
         return g;
     };
     auto issue = [&](int j, int s) {  // row j of this cluster into slot s
+        if (skips_copy(p, cid + j * ncl, cid + j * ncl + 1)) return;  // test hook
         const Geom g = geom(cid + j * ncl);
         const uint64_t g0 = lbase + (uint64_t)g.e0 * ES - (uint64_t)g.head * ES;
         const uint64_t lo = g0 > p.lo_clip ? g0 : p.lo_clip;
@@ -195,10 +184,9 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t ph_cur = 0;
     int t_next = nrows > 0 ? target_at(p, cid) : 0;
 
-    auto fail = [&]() {
+    auto fail = [&]() {  // one timeout counted per CTA
         failed = true;
-        cta_failed = 1;
-        atomicAdd(&p.err[kErrTimeout], 1);
+        if (atomicExch(&cta_failed, 1) == 0) atomicAdd(&p.err[kErrTimeout], 1);
     };
 
     // ---------------------------------------------------------------- A(j)
@@ -215,7 +203,7 @@ __global__ void __launch_bounds__(NT, 1)
         unsigned char *slot = smem + (size_t)s_cur * slot_bytes;
 
         if (!failed) {
-            if (mbar_wait(&full[s_cur], ph_cur))
+            if (mbar_wait(&full[s_cur], ph_cur, copy_wait_limit(p)))
                 consumed = j + 1;
             else
                 fail();
@@ -323,6 +311,9 @@ __global__ void __launch_bounds__(NT, 1)
             const float Mc = warp_max(q.x);
             float sc = q.y != 0.f ? q.y * ex2(q.x - Mc) : 0.f;
             sc = warp_sum(sc);
+            // a CTA that gave up publishes a NaN sum: every CTA of the cluster
+            // then computes NaN rows (loss and gradient) from here on
+            if (*reinterpret_cast<volatile int *>(&cta_failed)) sc = NAN;
             const float zt = has_t ? zt_sh[par] : 0.f;
             // re-arm the exchange slot of row j-2 for row j-2+NB before this
             // CTA's push of row j (which any peer's push of row j-2+NB follows)
@@ -397,6 +388,16 @@ __global__ void __launch_bounds__(NT, 1)
                     exps_of<E, kKeepExp>(x[k], g2, kL2E2, nM2);
 #pragma unroll
                     for (int i = 0; i < W2; ++i) g2[i] = f2_mul(g2[i], esc2);
+                    if (grad_f32_of(p)) {
+#pragma unroll
+                        for (int i = 0; i < W2; ++i) {
+                            float a, bb;
+                            f2_unpack(g2[i], a, bb);
+                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i) * ES, a);
+                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i + 1) * ES, bb);
+                        }
+                        if (v == v_t) grad_f32_store<ES>(p, gbase + (size_t)tl * ES, g_t);
+                    }
                     if (vec_store) {
                         *reinterpret_cast<uint4 *>(gbase + 16 * v) = E::pack2(g2);
                     } else {
@@ -423,21 +424,28 @@ __global__ void __launch_bounds__(NT, 1)
                         for (int i = 0; i < W2; ++i) {
                             float a, bb;
                             f2_unpack(f2_mul(e2[i], esc2), a, bb);
-                            if ((unsigned)(l0 + 2 * i) < (unsigned)slice_n)
-                                E::store(gbase + 16 * v + (2 * i) * ES,
-                                         v * W + 2 * i == tl ? g_t : a);
-                            if ((unsigned)(l0 + 2 * i + 1) < (unsigned)slice_n)
-                                E::store(gbase + 16 * v + (2 * i + 1) * ES,
-                                         v * W + 2 * i + 1 == tl ? g_t : bb);
+                            if (v * W + 2 * i == tl) a = g_t;
+                            if (v * W + 2 * i + 1 == tl) bb = g_t;
+                            if ((unsigned)(l0 + 2 * i) < (unsigned)slice_n) {
+                                E::store(gbase + 16 * v + (2 * i) * ES, a);
+                                grad_f32_store<ES>(p, gbase + 16 * v + (2 * i) * ES, a);
+                            }
+                            if ((unsigned)(l0 + 2 * i + 1) < (unsigned)slice_n) {
+                                E::store(gbase + 16 * v + (2 * i + 1) * ES, bb);
+                                grad_f32_store<ES>(p, gbase + 16 * v + (2 * i + 1) * ES, bb);
+                            }
                         }
                     }
                 }
             }
         }
-        // Step 3: the row's loss, by one thread of rank 0
-        if (rank == 0 && warp == kLossWarp && lane == 0 && !skip && !is_softmax(p)) {
+        // Step 3: the row's loss, by one thread of rank 0 (NaN for a row this
+        // CTA did not compute)
+        if (rank == 0 && warp == kLossWarp && lane == 0 && !is_softmax(p)) {
             float l;
-            if (has_t) {
+            if (skip) {
+                l = NAN;
+            } else if (has_t) {
                 l = row_loss(s_rest, e_t, S, zt, M);
             } else {
                 l = NAN;
@@ -471,10 +479,13 @@ __global__ void __launch_bounds__(NT, 1)
         tp = tc;
     }
 
-    // A CTA that gave up still owns copies in flight: wait for them (bounded)
-    // before its shared memory is released.
+    // A CTA that gave up still owns copies in flight: the issuer waits for
+    // them (each for up to the full limit) before its shared memory is
+    // released.  A copy that has not landed after that never will; the CTA
+    // then leaves rather than hang.
     if (issuer && (failed || cta_failed)) {
         for (int j = consumed; j < issued; ++j) {
+            if (skips_copy(p, cid + j * ncl, cid + j * ncl + 1)) continue;  // never issued
             if (!mbar_wait(&full[j % nslots], (uint32_t)((j / nslots) & 1))) break;
         }
     }

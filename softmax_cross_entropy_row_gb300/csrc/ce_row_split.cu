@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(NT, 1)
     auto issue = [&](long long j) {
         const int s = (int)(j % nslots);
         uint64_t gs, ge, g0, lo, hi;
+        if (skips_copy(p, cid + j * ncl, cid + j * ncl + 1)) return;  // test hook
         span(cid + j * ncl, gs, ge, g0, lo, hi);
         unsigned char *slot = smem + (size_t)s * slot_bytes;
         if (hi > lo) {
@@ -113,7 +114,8 @@ __global__ void __launch_bounds__(NT, 1)
         for (; issued < nrows && issued < nslots; ++issued) issue(issued);
     }
 
-    bool failed = false;
+    bool failed = false;      // this thread saw a copy wait give up
+    bool failed_cta = false;  // some thread of the CTA did (uniform)
     long long consumed = 0;
     int t_next = nrows > 0 ? target_at(p, cid) : 0;
 
@@ -141,12 +143,10 @@ __global__ void __launch_bounds__(NT, 1)
         const int v_t = has_t ? tl / W : -1;                       // the target's vector
 
         if (!failed) {
-            if (mbar_wait(&full[s], parity)) {
+            if (mbar_wait(&full[s], parity, copy_wait_limit(p)))
                 consumed = j + 1;
-            } else {
-                failed = true;
-                atomicAdd(&p.err[kErrTimeout], 1);
-            }
+            else
+                failed = true;  // made CTA-wide (and counted) at the next barrier
         }
         // Elements the copy could not cover (only at the very beginning or end
         // of an unaligned tensor): plain loads, then a barrier before use.
@@ -215,7 +215,11 @@ __global__ void __launch_bounds__(NT, 1)
         float mx = E::max_value(macc);
         mx = warp_max(mx);
         if (lane == 0) red_max[par][warp] = mx;
-        failed = __syncthreads_or(failed);
+        {
+            const bool was = failed_cta;
+            failed = failed_cta = __syncthreads_or(failed);
+            if (failed && !was && tid == 0) atomicAdd(&p.err[kErrTimeout], 1);
+        }
         if (tid == 0 && !failed && issued < nrows) {
             if (stage) {
                 // the slot of row j-1 comes back once its gradient has been
@@ -301,7 +305,9 @@ __global__ void __launch_bounds__(NT, 1)
                 float v = lane < NW ? *reinterpret_cast<volatile float *>(&red_sum[par][lane]) : 0.f;
                 v = warp_sum(v);
                 if (lane == 0) {
-                    part[par] = make_float4(M_loc, v, zt, has_t ? 1.f : 0.f);
+                    // a CTA that gave up publishes a NaN sum: every CTA of the
+                    // cluster then computes a NaN row (loss and gradient)
+                    part[par] = make_float4(M_loc, failed ? NAN : v, zt, has_t ? 1.f : 0.f);
                     warps_summed[par] = 0u;
                 }
                 __syncwarp();
@@ -369,6 +375,16 @@ __global__ void __launch_bounds__(NT, 1)
                     exps(x[k], g2);
 #pragma unroll
                     for (int i = 0; i < W2; ++i) g2[i] = f2_mul(g2[i], esc2);
+                    if (grad_f32_of(p)) {
+#pragma unroll
+                        for (int i = 0; i < W2; ++i) {
+                            float a, b;
+                            f2_unpack(g2[i], a, b);
+                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i) * ES, a);
+                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i + 1) * ES, b);
+                        }
+                        if (v == v_t) grad_f32_store<ES>(p, gbase + (size_t)tl * ES, g_t);
+                    }
                     if (stage) {
                         // in place of the vector's logits, which this thread alone read
                         *reinterpret_cast<uint4 *>(slot + 16 * v) = E::pack2(g2);
@@ -401,12 +417,16 @@ __global__ void __launch_bounds__(NT, 1)
                         for (int i = 0; i < W2; ++i) {
                             float a, b;
                             f2_unpack(f2_mul(e2[i], esc2), a, b);
-                            if ((unsigned)(l0 + 2 * i) < (unsigned)slice_n)
-                                E::store(gbase + 16 * v + (2 * i) * ES,
-                                         v * W + 2 * i == tl ? g_t : a);
-                            if ((unsigned)(l0 + 2 * i + 1) < (unsigned)slice_n)
-                                E::store(gbase + 16 * v + (2 * i + 1) * ES,
-                                         v * W + 2 * i + 1 == tl ? g_t : b);
+                            if (v * W + 2 * i == tl) a = g_t;
+                            if (v * W + 2 * i + 1 == tl) b = g_t;
+                            if ((unsigned)(l0 + 2 * i) < (unsigned)slice_n) {
+                                E::store(gbase + 16 * v + (2 * i) * ES, a);
+                                grad_f32_store<ES>(p, gbase + 16 * v + (2 * i) * ES, a);
+                            }
+                            if ((unsigned)(l0 + 2 * i + 1) < (unsigned)slice_n) {
+                                E::store(gbase + 16 * v + (2 * i + 1) * ES, b);
+                                grad_f32_store<ES>(p, gbase + 16 * v + (2 * i + 1) * ES, b);
+                            }
                         }
                     }
                 }
@@ -424,10 +444,13 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
 
-        // ---- Step 3: the row's loss (one writer per row)
-        if (rank == 0 && tid == 0 && !failed && !is_softmax(p)) {
+        // ---- Step 3: the row's loss (one writer per row); NaN for a row
+        // this CTA did not compute (a copy wait gave up)
+        if (rank == 0 && tid == 0 && !is_softmax(p)) {
             float l;
-            if (has_t) {
+            if (failed) {
+                l = NAN;
+            } else if (has_t) {
                 l = row_loss(s_rest, e_t, S, zt, M);
             } else {
                 l = NAN;
@@ -438,10 +461,13 @@ __global__ void __launch_bounds__(NT, 1)
     }
 
     if (stage && tid == 0) bulk_wait_all();  // the last gradient stores have landed
-    // A CTA that gave up still owns copies in flight: wait for them (bounded)
-    // before its shared memory is released.
+    // A CTA that gave up still owns copies in flight: it waits for them
+    // (each for up to the full limit) before its shared memory is released.
+    // A copy that has not landed after that never will; the CTA then leaves
+    // rather than hang.
     if (tid == 0 && failed) {
         for (long long j = consumed; j < issued; ++j) {
+            if (skips_copy(p, cid + j * ncl, cid + j * ncl + 1)) continue;  // never issued
             if (!mbar_wait(&full[j % nslots], (uint32_t)((j / nslots) & 1))) break;
         }
     }

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
         long long r0, r1;
         uint64_t gs, ge, g0, lo, hi;
         span(gw + i * TW, r0, r1, gs, ge, g0, lo, hi);
+        if (skips_copy(p, r0, r1)) return;  // test hook: this tile's wait must give up
         unsigned char *slot = my_slots + (size_t)s * slot_bytes;
         if (hi > lo) {
             mbar_arrive_expect_tx(&my_full[s], (uint32_t)(hi - lo));
@@ -88,8 +89,7 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
         for (; issued < ntl && issued < slots; ++issued) issue(issued);
     }
 
-    bool failed = false;
-    long long consumed = 0;
+    long long failed_at = ntl;  // the first tile whose copy wait gave up (ntl: none)
 
     for (long long i = 0; i < ntl; ++i) {
         const int s = (int)(i % slots);
@@ -101,16 +101,12 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
         // the tile's first targets, in flight while the copy lands
         int tchunk = r0 + lane < r1 ? target_at(p, r0 + lane) : 0;
 
-        if (!failed) {
-            if (mbar_wait(&my_full[s], parity)) {
-                consumed = i + 1;
-            } else {
-                failed = true;
-                if (lane == 0) atomicAdd(&p.err[kErrTimeout], 1);
-            }
+        // the warp goes on only if every lane saw the copy land
+        if (!__all_sync(0xffffffffu, mbar_wait(&my_full[s], parity, copy_wait_limit(p)))) {
+            failed_at = i;
+            if (lane == 0) atomicAdd(&p.err[kErrTimeout], 1);
+            break;
         }
-        failed = __any_sync(0xffffffffu, failed);
-        if (failed) continue;
 
         // Elements of an unaligned tensor's first/last 16 bytes: plain loads.
         if (g0 < p.lo_clip || ((ge + 15) & ~15ull) > p.hi_clip) {
@@ -244,6 +240,16 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
                             }
                             g2[j] = f2_mul(g2[j], sc2);
                         }
+                        if (grad_f32_of(p)) {
+#pragma unroll
+                            for (int j = 0; j < W2; ++j) {
+                                float a, b;
+                                f2_unpack(g2[j], a, b);
+                                grad_f32_store<ES>(p, gvec + (v * W + 2 * j) * ES, a);
+                                grad_f32_store<ES>(p, gvec + (v * W + 2 * j + 1) * ES, b);
+                            }
+                            if (v == v_t) grad_f32_store<ES>(p, grow + (size_t)t * ES, g_t);
+                        }
                         if (vec_store) {
                             *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack2(g2);
                         } else {
@@ -260,10 +266,16 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
                     }
                 }
                 if (ragged) {
-                    if (lane < nh) E::store(grow + lane * ES, lane == t ? g_t : eh * scale);
+                    if (lane < nh) {
+                        const float gh = lane == t ? g_t : eh * scale;
+                        E::store(grow + lane * ES, gh);
+                        grad_f32_store<ES>(p, grow + lane * ES, gh);
+                    }
                     if (lane < nt) {
                         const int c = nh + nvec * W + lane;
-                        E::store(grow + c * ES, c == t ? g_t : et * scale);
+                        const float gc = c == t ? g_t : et * scale;
+                        E::store(grow + c * ES, gc);
+                        grad_f32_store<ES>(p, grow + c * ES, gc);
                     }
                 }
             }
@@ -288,9 +300,29 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
         }
     }
 
-    if (lane == 0 && failed) {
-        for (long long i = consumed; i < issued; ++i) {
-            if (!mbar_wait(&my_full[i % slots], (uint32_t)((i / slots) & 1))) break;
+    if (failed_at < ntl) {
+        // The tiles from the one whose wait gave up on were not computed:
+        // their rows' losses are NaN, so the batch loss shows the failure
+        // (their gradient is not written).
+        for (long long i = failed_at; i < ntl; ++i) {
+            long long r0, r1;
+            uint64_t gs, ge, g0, lo, hi;
+            span(gw + i * TW, r0, r1, gs, ge, g0, lo, hi);
+            if (!is_softmax(p))
+                for (long long r = r0 + lane; r < r1; r += 32) p.loss_rows[r] = NAN;
+        }
+        // The warp still owns copies in flight: it waits for them (each for
+        // up to the full limit) before the CTA's shared memory is released.
+        // A copy that has not landed after that never will; the warp then
+        // leaves rather than hang.
+        if (lane == 0) {
+            for (long long i = failed_at; i < issued; ++i) {
+                long long r0, r1;
+                uint64_t gs, ge, g0, lo, hi;
+                span(gw + i * TW, r0, r1, gs, ge, g0, lo, hi);
+                if (skips_copy(p, r0, r1)) continue;  // never issued
+                if (!mbar_wait(&my_full[i % slots], (uint32_t)((i / slots) & 1))) break;
+            }
         }
     }
     finish_cta(p, &tail_flag, tail_scratch);

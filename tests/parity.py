@@ -112,12 +112,17 @@ def check_full(inp, loss, grad, what: str = "") -> None:
     check_grad(grad_rows_host(grad), g_ref, inp.workload.B, inp.workload.dtype, what, valid)
 
 
-def check_sampled(inp, loss, grad, rows, what: str = "") -> None:
-    """Full-size check: L against the oracle over every row, gradients on sampled rows."""
+def check_all_rows(inp, loss, grad, what: str = "", block: int = 256) -> None:
+    """Full-size check of every element: L against the oracle over every row,
+    then the gradient compared element by element with the oracle's, streamed
+    through the oracle in blocks of rows (an fp64 [B, C] of the largest
+    workloads would not fit in host memory at once)."""
+    B, C = inp.workload.B, inp.workload.C
     l_all = oracle.rows(inp.logits, inp.targets, grad=False)
     check_loss(float(loss.item()), oracle.batch_loss(l_all))
-    rows = np.unique(np.asarray(rows, dtype=np.int64))
-    _, g_ref = oracle.rows(inp.logits, inp.targets, row_ids=rows)
-    t = inp.targets[rows]
-    check_grad(grad_rows_host(grad, rows), g_ref, inp.workload.B, inp.workload.dtype, what,
-               (t >= 0) & (t < inp.workload.C))
+    valid = (inp.targets >= 0) & (inp.targets < C)
+    for r0 in range(0, B, block):
+        r1 = min(B, r0 + block)
+        _, g_ref = oracle.rows(inp.logits, inp.targets, row_ids=np.arange(r0, r1))
+        g = grad[r0:r1].float().cpu().numpy().astype(np.float64)
+        check_grad(g, g_ref, B, inp.workload.dtype, f"{what} rows {r0}..{r1 - 1}", valid[r0:r1])

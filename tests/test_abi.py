@@ -10,10 +10,11 @@ import softmax_cross_entropy_row_gb300 as ce
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "ce.h")
+TEST_HEADER = os.path.join(ROOT, "include", "ce_testing.h")
 
 
-def _declared_functions():
-    text = open(HEADER).read()
+def _declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(ce_[a-z0-9_]+)\s*\(", text)))
 
@@ -31,8 +32,24 @@ def test_header_declares_the_boundary():
 
 
 def test_library_exports_every_declared_symbol(lib):
-    for name in _declared_functions():
+    for name in _declared_functions() + _declared_functions(TEST_HEADER):
         assert hasattr(lib, name), f"libce.so does not export {name}"
+
+
+def test_test_header_declares_the_hooks():
+    assert set(_declared_functions(TEST_HEADER)) == set(ce.TEST_EXPORTS)
+
+
+def test_host_side_errors_of_the_test_entry(lib):
+    """The test entry point checks its hooks before any CUDA call."""
+    f = lib.ce_fwd_bwd_test
+    none = ce.TestHooks(-1, 0, None)
+    assert f(256, 512, 4, 4, 0, 1024, None, None, 0, 0, ctypes.byref(none)) == 1   # NULL grad
+    assert f(256, 512, 4, 4, 7, 1024, 4096, None, 0, 0, None) == 3                 # dtype
+    bad = ce.TestHooks(-1, 0, 8194)                                                  # 2 mod 4
+    assert f(256, 512, 4, 4, 0, 1024, 4096, None, 0, 0, ctypes.byref(bad)) == 4
+    over = ce.TestHooks(-1, 0, 1 << 20)                  # fp32 record over the logits
+    assert f(1 << 20, 1 << 24, 4, 4, 0, 1 << 25, 1 << 26, None, 0, 0, ctypes.byref(over)) == 6
 
 
 def test_status_strings_need_no_gpu(lib):

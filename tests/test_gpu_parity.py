@@ -1,9 +1,10 @@
 """GPU parity: the CUDA path through the C-ABI against the fp64 oracle.
 
-Small cases are compared element by element; the full-size workloads are
-compared on the batch loss (oracle over every row) and on sampled gradient
-rows (the structured rows, the first and last rows and a seeded random
-sample), plus the row-sum property on every row.
+Every case is compared element by element: the small ones at once, the
+full-size workloads (in the launch configuration the benchmark times) on the
+batch loss over every row and on every gradient element, streamed through the
+oracle in blocks of rows; the row-sum property is checked on every row, for
+16-bit gradients also on the fp32 values before their rounding.
 """
 
 import numpy as np
@@ -11,8 +12,8 @@ import pytest
 
 import workloads as wl
 
-from parity import (GRAD_ATOL_TIMES_B, ROWSUM_ATOL_TIMES_B, check_full, check_grad, check_loss,
-                    check_sampled, device_inputs, grad_rows_host, run, ulp_bf16)
+from parity import (ROWSUM_ATOL_TIMES_B, check_all_rows, check_full, check_grad, device_inputs,
+                    grad_rows_host, run)
 
 pytestmark = pytest.mark.gpu
 
@@ -23,8 +24,9 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 import softmax_cross_entropy_row_gb300 as ce  # noqa: E402
 import oracle  # noqa: E402
 
-AUTO, WARP, SPLIT, STREAM = (ce.CE_PATH_AUTO, ce.CE_PATH_ROWS_WARP, ce.CE_PATH_ROW_SPLIT,
-                             ce.CE_PATH_STREAM)
+AUTO, WARP, SPLIT, STREAM, TWOPASS = (ce.CE_PATH_AUTO, ce.CE_PATH_ROWS_WARP,
+                                      ce.CE_PATH_ROW_SPLIT, ce.CE_PATH_STREAM,
+                                      ce.CE_PATH_ROW_TWOPASS)
 SPLIT_MAX_SLICE_BYTES = 512 * 16 * 16 - 32  # threads x vectors x 16 bytes, less the partial vectors
 
 
@@ -59,6 +61,11 @@ WARP_SHAPES = [(1, 1), (3, 2), (8, 3), (5, 5), (7, 7), (64, 10), (33, 31), (9, 3
 SPLIT_SHAPES = [(1, 1), (2, 3), (3, 17), (5, 1000), (4, 4099), (3, 8191), (6, 16385), (2, 40000),
                 (3, 50257)]
 STREAM_SHAPES = [(1, 1), (3, 5), (2, 4095), (2, 4096), (3, 4097), (2, 10000), (2, 50257)]
+# the two-pass kernel's chunks hold 4096 fp32 / 8192 16-bit elements: rows
+# inside one chunk, across a chunk boundary, many chunks, and long rows
+TWOPASS_SHAPES = [(1, 1), (3, 2), (5, 5), (7, 31), (4, 1000), (3, 4095), (3, 4096), (2, 4097),
+                  (5, 8191), (3, 8193), (6, 16385), (3, 32000), (2, 50257), (2, 128256),
+                  (2, 300007)]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -97,6 +104,28 @@ def test_stream_path_shapes(B, C, dtype):
     loss, grad = run(z, t, STREAM)
     torch.cuda.synchronize()
     check_full(inp, loss, grad, f"stream {B}x{C} {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("B,C", TWOPASS_SHAPES)
+def test_twopass_path_shapes(B, C, dtype):
+    inp = _case(B, C, dtype, seed=B * 7 + C + 3, sigma=3.0)
+    z, t = device_inputs(inp)
+    loss, grad = run(z, t, TWOPASS)
+    torch.cuda.synchronize()
+    check_full(inp, loss, grad, f"two-pass {B}x{C} {dtype}")
+
+
+def test_twopass_many_rows_per_cta():
+    """More rows than CTAs, so every CTA's ring of chunks wraps many times,
+    with ragged rows that start at every 4-byte offset."""
+    for B, C, dtype in [(700, 5003, "f32"), (400, 50257, "f32"), (330, 32000, "bf16"),
+                        (160, 128256, "bf16"), (2000, 999, "f16")]:
+        inp = _case(B, C, dtype, seed=C, sigma=2.0)
+        z, t = device_inputs(inp)
+        loss, grad = run(z, t, TWOPASS)
+        torch.cuda.synchronize()
+        check_full(inp, loss, grad, f"two-pass ring wrap {dtype} {B}x{C}")
 
 
 def test_many_rows_per_cluster():
@@ -149,7 +178,8 @@ def test_f16_refuses_slices_beyond_64kb():
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("path,split,C", [(WARP, 0, 37), (WARP, 0, 1001), (SPLIT, 1, 5003),
-                                          (SPLIT, 4, 7001), (STREAM, 0, 5003)])
+                                          (SPLIT, 4, 7001), (STREAM, 0, 5003),
+                                          (TWOPASS, 0, 3), (TWOPASS, 0, 5003)])
 @pytest.mark.parametrize("zoff,goff", [(1, 0), (0, 1), (3, 2), (1, 1)])
 def test_unaligned_tensors(dtype, path, split, C, zoff, goff):
     """Logits and grad starting at any element offset (not 16-byte aligned),
@@ -175,7 +205,8 @@ def test_unaligned_tensors(dtype, path, split, C, zoff, goff):
 # ------------------------------------------------------------- data errors
 
 @pytest.mark.parametrize("path,split,C,dtype", [(WARP, 0, 100, "f32"), (SPLIT, 1, 9000, "bf16"),
-                                                (SPLIT, 4, 9000, "f32"), (STREAM, 0, 9000, "f32")])
+                                                (SPLIT, 4, 9000, "f32"), (STREAM, 0, 9000, "f32"),
+                                                (TWOPASS, 0, 9000, "f32")])
 def test_out_of_range_targets(path, split, C, dtype):
     """Reading: an out-of-range target gives a NaN loss, a softmax/B gradient
     row (no one-hot term) and one count per bad row; other rows unaffected."""
@@ -197,7 +228,9 @@ def test_out_of_range_targets(path, split, C, dtype):
 # ------------------------------------------------------ stated properties
 
 @pytest.mark.parametrize("path,split,C,dtype", [(WARP, 0, 1000, "f32"), (SPLIT, 1, 32000, "bf16"),
-                                                (SPLIT, 4, 50257, "f32"), (STREAM, 0, 9000, "bf16")])
+                                                (SPLIT, 4, 50257, "f32"), (STREAM, 0, 9000, "bf16"),
+                                                (TWOPASS, 0, 50257, "f32"),
+                                                (TWOPASS, 0, 128256, "bf16")])
 def test_bitwise_deterministic(path, split, C, dtype):
     inp = _case(64, C, dtype, seed=77)
     z, t = device_inputs(inp)
@@ -215,8 +248,9 @@ def test_structured_rows_small():
     stress = wl.Workload("stress_small", 400, 5003, "f32", seed=4, sigma=30.0,
                          uniform_frac=0.01, spike=80.0)
     peaked = wl.Workload("peaked_small", 256, 12829, "bf16", seed=3, sigma=3.0, peak=8.0)
-    for w, paths in [(stress, [(AUTO, 0), (SPLIT, 1), (SPLIT, 2), (SPLIT, 4), (STREAM, 0)]),
-                     (peaked, [(AUTO, 0), (SPLIT, 1), (SPLIT, 8), (STREAM, 0)])]:
+    for w, paths in [(stress, [(AUTO, 0), (SPLIT, 1), (SPLIT, 2), (SPLIT, 4), (STREAM, 0),
+                               (TWOPASS, 0)]),
+                     (peaked, [(AUTO, 0), (SPLIT, 1), (SPLIT, 8), (STREAM, 0), (TWOPASS, 0)])]:
         inp = wl.make_inputs(w)
         z, t = device_inputs(inp)
         for path, split in paths:
@@ -230,18 +264,9 @@ def test_structured_rows_small():
 EXPECTED_PLAN = {
     "classifier_4096x1000_f32": ("rows_warp", 1),
     "lm_head_8192x32000_bf16": ("row_split", 1),
-    "lm_head_4096x128256_bf16_peaked": ("row_split", 4),
-    "stress_16384x50257_f32": ("row_split", 2),
+    "lm_head_4096x128256_bf16_peaked": ("row_twopass", 1),
+    "stress_16384x50257_f32": ("row_twopass", 1),
 }
-
-
-def _sample_rows(inp, n=40):
-    B = inp.workload.B
-    g = np.random.default_rng(inp.workload.seed + 1000)
-    rows = [0, 1, B // 2, B - 2, B - 1]
-    rows += list(g.choice(B, size=n, replace=False))
-    rows += list(inp.uniform_rows[:8]) + list(inp.spike_rows[:8])
-    return np.array(rows, dtype=np.int64)
 
 
 def _row_sums_ok(grad, B, dtype):
@@ -270,7 +295,7 @@ def test_full_size_workload(name):
     z, t = device_inputs(inp)
     loss, grad = run(z, t)
     torch.cuda.synchronize()
-    check_sampled(inp, loss, grad, _sample_rows(inp), name)
+    check_all_rows(inp, loss, grad, name)
     _row_sums_ok(grad, w.B, w.dtype)
     # uniform rows: softmax is exactly 1/C
     for r in inp.uniform_rows[:4]:
@@ -282,14 +307,42 @@ def test_full_size_workload(name):
     assert (bad, tmo) == (0, 0)
 
 
-def test_stress_workload_stream_path():
-    """The streaming path on the full ragged stress workload (sampled rows)."""
+@pytest.mark.parametrize("name", ["lm_head_8192x32000_bf16", "lm_head_4096x128256_bf16_peaked"])
+def test_bf16_row_sums_before_rounding(name):
+    """The row-sum bound 1e-6/B on the fp32 gradient values the kernel rounds
+    to bf16 (the test hook records them): a bf16 output can only hold it to
+    its rounding.  The recorded values round to exactly the bf16 gradient, and
+    recording them leaves the gradient's bits unchanged."""
+    w = wl.WORKLOADS_BY_NAME[name]
+    inp = wl.make_inputs(w)
+    z, t = device_inputs(inp)
+    loss0, grad0 = run(z, t)
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    grad = torch.empty_like(z)
+    g32 = torch.empty(z.shape, dtype=torch.float32, device="cuda")
+    ce.ce_fwd_bwd_test(z, t, loss, grad, None, AUTO, 0, grad_f32_out=g32)
+    torch.cuda.synchronize()
+    assert torch.equal(loss, loss0) and torch.equal(grad.view(torch.int16), grad0.view(torch.int16))
+    worst = 0.0
+    for r0 in range(0, w.B, 512):
+        blk = g32[r0:r0 + 512]
+        assert torch.equal(blk.to(torch.bfloat16).view(torch.int16),
+                           grad[r0:r0 + 512].view(torch.int16)), "recorded values are not the rounded ones"
+        worst = max(worst, float(blk.double().sum(dim=1).abs().max()) * w.B)
+    assert worst <= ROWSUM_ATOL_TIMES_B, f"{name}: fp32 row sum {worst:.3g}/B before rounding"
+
+
+def test_stress_workload_other_paths():
+    """The streaming path and the cluster split (K = 2) on the full ragged
+    stress workload, every element."""
     w = wl.WORKLOADS_BY_NAME["stress_16384x50257_f32"]
     inp = wl.make_inputs(w)
     z, t = device_inputs(inp)
-    loss, grad = run(z, t, STREAM)
-    torch.cuda.synchronize()
-    check_sampled(inp, loss, grad, _sample_rows(inp, 16), "stress via stream path")
+    for path, split in ((STREAM, 0), (SPLIT, 2)):
+        loss, grad = run(z, t, path, split)
+        torch.cuda.synchronize()
+        check_all_rows(inp, loss, grad, f"stress via path {path} K={split}")
+        del loss, grad
 
 
 # --------------------------------------------------------------- runtime

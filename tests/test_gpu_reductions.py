@@ -26,13 +26,14 @@ import softmax_cross_entropy_row_gb300 as ce  # noqa: E402
 import oracle  # noqa: E402
 
 WARP, SPLIT, STREAM = ce.CE_PATH_ROWS_WARP, ce.CE_PATH_ROW_SPLIT, ce.CE_PATH_STREAM
+TWOPASS = ce.CE_PATH_ROW_TWOPASS
 MEAN, SUM, NONE = ce.CE_REDUCE_MEAN, ce.CE_REDUCE_SUM, ce.CE_REDUCE_NONE
 
 # (path, split, B, C): the warp kernel, the barrier-per-row split kernel at
 # K = 1 and with 100 KB fp32 slices, the pipelined split kernel, the streaming
-# path
+# path, the two-pass path
 PATHS = [(WARP, 0, 300, 1000), (SPLIT, 1, 5, 20000), (SPLIT, 4, 6, 40000),
-         (SPLIT, 2, 3, 50257), (STREAM, 0, 3, 10000)]
+         (SPLIT, 2, 3, 50257), (STREAM, 0, 3, 10000), (TWOPASS, 0, 5, 50257)]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -32,16 +32,20 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 import softmax_cross_entropy_row_gb300 as ce  # noqa: E402
 import oracle  # noqa: E402
 
-AUTO, WARP, SPLIT, STREAM = (ce.CE_PATH_AUTO, ce.CE_PATH_ROWS_WARP, ce.CE_PATH_ROW_SPLIT,
-                             ce.CE_PATH_STREAM)
+AUTO, WARP, SPLIT, STREAM, TWOPASS = (ce.CE_PATH_AUTO, ce.CE_PATH_ROWS_WARP,
+                                      ce.CE_PATH_ROW_SPLIT, ce.CE_PATH_STREAM,
+                                      ce.CE_PATH_ROW_TWOPASS)
 TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 # (path, split, B, C): the warp kernel (ragged and exact rows), the split
 # kernel at K = 1 (barrier per row), K = 4 (staged slices) and the pipelined
-# K = 2, the streaming path
+# K = 2, the streaming path, the two-pass path (short, chunk-sized and long
+# rows)
 PATHS = [(WARP, 0, 1, 1), (WARP, 0, 7, 7), (WARP, 0, 300, 1000), (WARP, 0, 5, 2047),
          (SPLIT, 1, 3, 17), (SPLIT, 1, 5, 20000), (SPLIT, 4, 6, 40000), (SPLIT, 2, 3, 50257),
-         (SPLIT, 8, 2, 128256), (STREAM, 0, 1, 1), (STREAM, 0, 3, 10000), (STREAM, 0, 2, 4097)]
+         (SPLIT, 8, 2, 128256), (STREAM, 0, 1, 1), (STREAM, 0, 3, 10000), (STREAM, 0, 2, 4097),
+         (TWOPASS, 0, 1, 1), (TWOPASS, 0, 7, 7), (TWOPASS, 0, 5, 4099), (TWOPASS, 0, 3, 50257),
+         (TWOPASS, 0, 2, 300001)]
 
 
 @pytest.fixture(scope="module", autouse=True)
