@@ -3,11 +3,11 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--headline-only]
 
-Prints ONE JSON line.  The headline ``value`` is rows/s of the classifier-head
-workload (B=4096, C=1000, fp32) processed by the library's kernels with the
-inputs resident in HBM; ``workloads`` carries the same measurement for every
-workload (all five, in the same run).  A step is one ``ce_fwd_bwd`` call: the
-loss and the full gradient of one batch.
+Prints ONE JSON line.  The headline ``value`` is rows/s of the largest
+workload, the ragged stress case (B=16384, C=50257, fp32), processed by the
+library's kernels with the inputs resident in HBM; ``workloads`` carries the
+same measurement for every workload (all five, in the same run).  A step is
+one ``ce_fwd_bwd`` call: the loss and the full gradient of one batch.
 
 Timing: steps run from a CUDA graph (one library call per step, captured
 once), cycling through enough buffer sets that every step reads inputs that
@@ -43,7 +43,8 @@ import numpy as np  # noqa: E402
 import workloads as wl  # noqa: E402
 
 METRIC = "fused CE fwd+grad rows/s and achieved HBM GB/s vs ~8 TB/s roofline (1×GB300)"
-HEADLINE = "classifier_4096x1000_f32"
+HEADLINE = "stress_16384x50257_f32"
+TIMED_PARTS = 5            # the timed region is split into parts for a spread
 FALLBACK_HBM_GBS = 6800.0
 TARGET_REGION_S = 1.5      # timed work per workload when --steps is not given
 HOLD_CYCLES = 400_000      # device-side wait (~0.2 ms) queued ahead of each timed region
@@ -176,10 +177,24 @@ def cpu_cores() -> int:
 
 def time_oracle(inp, budget_s: float = CPU_SAMPLE_S):
     """Rows/s of the fp64 oracle's forward + gradient on a bounded sample of
-    the workload's rows (whole batch repeated, or a leading block of rows)."""
+    the workload's rows, on every host core the process may use; and, on a
+    sample of a quarter of the budget, on one thread."""
     import oracle
 
     oracle.build()
+    cores = cpu_cores()
+    oracle.set_threads(1)
+    one = _time_oracle_threads(inp, 0.25 * budget_s)
+    oracle.set_threads(cores)
+    res = _time_oracle_threads(inp, 0.75 * budget_s)
+    res["one_thread"] = {"value": one["value"], "unit": "rows/s", "cores": 1,
+                         "sample": one["sample"]}
+    return res
+
+
+def _time_oracle_threads(inp, budget_s):
+    import oracle
+
     B, C = inp.logits.shape
     # calibrate on a small block, then size the sample to the budget
     probe = max(1, min(B, 64))
@@ -296,17 +311,27 @@ def bench_workload(w, inp, steps, warmup, device, l2_bytes, hbm_peak, peak_note,
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize(device)
+        # the replays split into TIMED_PARTS parts, an event after each
+        cuts = [round(replays * k / TIMED_PARTS) for k in range(TIMED_PARTS + 1)]
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(TIMED_PARTS + 1)]
+        part_steps = [(cuts[k + 1] - cuts[k]) * per_graph for k in range(TIMED_PARTS)]
+        part_steps[-1] += rest
         sampler = ClockSampler(sampler_gpu)
         with sampler:
             # keep the stream busy while the host submits the timed graphs, so
             # that the start event does not wait on host launch latency
             torch.cuda._sleep(HOLD_CYCLES)
             e0.record(s)
-            for _ in range(replays):
-                graph.replay()
-            if tail is not None:
-                tail.replay()
+            marks[0] = e0
+            for k in range(TIMED_PARTS):
+                for _ in range(cuts[k + 1] - cuts[k]):
+                    graph.replay()
+                if k == TIMED_PARTS - 1 and tail is not None:
+                    tail.replay()
+                if k < TIMED_PARTS - 1:
+                    marks[k + 1].record(s)
             e1.record(s)
+            marks[-1] = e1
             e1.synchronize()
         torch.cuda.synchronize(device)
         elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, device)
@@ -314,6 +339,9 @@ def bench_workload(w, inp, steps, warmup, device, l2_bytes, hbm_peak, peak_note,
             torch.distributed.barrier()
         bad, tmo = ce.ce_get_device_errors(s)
     del graph, tail
+    # per-step time of each part of the timed region (events only, no
+    # synchronisation between the parts)
+    part_ms = [a.elapsed_time(b) / n for a, b, n in zip(marks[:-1], marks[1:], part_steps) if n]
     per_step = elapsed / n_steps
     per_launch = per_step / plan["launches"] if plan["launches"] == 1 else None
     achieved = w.min_bytes / per_step / 1e9
@@ -326,6 +354,8 @@ def bench_workload(w, inp, steps, warmup, device, l2_bytes, hbm_peak, peak_note,
         "achieved_gbs": achieved, "frac_of_peak": achieved / hbm_peak,
         "min_bytes_per_step": w.min_bytes, "device_errors": [bad, tmo],
         "clocks": sampler.summary(),
+        "ms_per_step_parts": {"median": statistics.median(part_ms), "min": min(part_ms),
+                              "max": max(part_ms), "parts": len(part_ms)} if part_ms else None,
     }
     if per_launch is not None:
         res["kernel_ms_per_launch"] = per_launch * 1e3
@@ -593,7 +623,7 @@ def main():
     out = {
         "metric": METRIC, "value": head["rows_per_s"], "unit": "rows/s", "n_gpus": world,
         "steps": head["steps"], "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "C": w.C, "logits_dtype": w.dtype,
                    "l2": l2_note(head, w, l2_bytes),
@@ -607,6 +637,7 @@ def main():
         "e2e": ({k: head["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step",
                                              "d2h_bytes_per_step")} if "e2e" in head else None),
         "gpu_launches": world * head["steps"] * head["launches_per_step"],
+        "ms_per_step_parts": head["ms_per_step_parts"],
         "clocks": head["clocks"],
         "workloads": [dict(results[n], l2=l2_note(results[n], wl.WORKLOADS_BY_NAME[n], l2_bytes))
                       for n in names],
