@@ -72,29 +72,38 @@ def measured_peaks():
 
 
 # The host-side C-ABI layer: argument checks, workspaces and the planner.  Its
-# launch decisions are recorded with the traffic (PLAN_KEYS), so the hash
-# covers the device code only.
+# launch decisions are recorded with the traffic (PLAN_KEYS), so the hashes
+# cover the device code only: each kernel's own file and the headers every
+# kernel includes.
 HOST_ONLY_SOURCES = ("ce_api.cu",)
+SHARED_DEVICE_SOURCES = ("ce_device.cuh", "ce_launch.h")
+KERNEL_SOURCES = {"rows_warp": "ce_rows_warp.cu", "row_split": "ce_row_split.cu",
+                  "row_pipe": "ce_row_pipe.cu", "row_twopass": "ce_row_twopass.cu",
+                  "stream": "ce_stream.cu"}
 PLAN_KEYS = ("path", "split", "ctas", "threads", "smem_bytes")
 
 
-def source_hash() -> str:
-    """Hash of the kernels' sources (every csrc file but the host-only ones)."""
+def source_hash(kernel: str | None = None) -> str:
+    """Hash of a kernel's device sources (its file and the shared headers), or
+    of every csrc file but the host-only ones when no kernel is named."""
+    csrc = os.path.join(ROOT, "softmax_cross_entropy_row_gb300", "csrc")
+    if kernel is None:
+        names = sorted(os.path.basename(p) for p in glob.glob(os.path.join(csrc, "*"))
+                       if os.path.basename(p) not in HOST_ONLY_SOURCES)
+    else:
+        names = sorted((KERNEL_SOURCES[kernel],) + SHARED_DEVICE_SOURCES)
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "softmax_cross_entropy_row_gb300", "csrc", "*")))
-    for p in files:
-        if os.path.basename(p) in HOST_ONLY_SOURCES:
-            continue
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str, plan=None):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None if the kernels or their launch (path, split, CTAs,
-    threads, shared memory) changed since it was taken."""
+    summary, or None if that kernel's sources or its launch (path, split,
+    CTAs, threads, shared memory) changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -102,7 +111,9 @@ def recorded_traffic(workload: str, plan=None):
     except (OSError, ValueError):
         return None
     e = d.get(workload)
-    if not e or e.get("source_sha") != source_hash():
+    if not e or e.get("kernel") not in KERNEL_SOURCES:
+        return None
+    if e.get("source_sha") != source_hash(e["kernel"]):
         return None
     if plan is not None and e.get("plan") != {k: plan.get(k) for k in PLAN_KEYS}:
         return None

@@ -388,16 +388,6 @@ __global__ void __launch_bounds__(NT, 1)
                     exps_of<E, kKeepExp>(x[k], g2, kL2E2, nM2);
 #pragma unroll
                     for (int i = 0; i < W2; ++i) g2[i] = f2_mul(g2[i], esc2);
-                    if (grad_f32_of(p)) {
-#pragma unroll
-                        for (int i = 0; i < W2; ++i) {
-                            float a, bb;
-                            f2_unpack(g2[i], a, bb);
-                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i) * ES, a);
-                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i + 1) * ES, bb);
-                        }
-                        if (v == v_t) grad_f32_store<ES>(p, gbase + (size_t)tl * ES, g_t);
-                    }
                     if (vec_store) {
                         *reinterpret_cast<uint4 *>(gbase + 16 * v) = E::pack2(g2);
                     } else {
@@ -410,6 +400,26 @@ __global__ void __launch_bounds__(NT, 1)
                         }
                     }
                     if (v == v_t) E::store(gbase + (size_t)tl * ES, g_t);
+                }
+            }
+            // test hook: the whole vectors' fp32 values, before their rounding
+            // (recomputed here so that the loop above carries none of it)
+            if (grad_f32_of(p)) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = tid + k * NT;
+                    if (v >= g.vf0 && v < g.vf1) {
+                        unsigned long long g2[W2];
+                        exps_of<E, kKeepExp>(x[k], g2, kL2E2, nM2);
+#pragma unroll
+                        for (int i = 0; i < W2; ++i) {
+                            float a, bb;
+                            f2_unpack(f2_mul(g2[i], esc2), a, bb);
+                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i) * ES, a);
+                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i + 1) * ES, bb);
+                        }
+                        if (v == v_t) grad_f32_store<ES>(p, gbase + (size_t)tl * ES, g_t);
+                    }
                 }
             }
             if ((g.head_partial || g.tail_partial) && (tid == 0 || tid == (g.nv - 1) % NT)) {

@@ -375,16 +375,6 @@ __global__ void __launch_bounds__(NT, 1)
                     exps(x[k], g2);
 #pragma unroll
                     for (int i = 0; i < W2; ++i) g2[i] = f2_mul(g2[i], esc2);
-                    if (grad_f32_of(p)) {
-#pragma unroll
-                        for (int i = 0; i < W2; ++i) {
-                            float a, b;
-                            f2_unpack(g2[i], a, b);
-                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i) * ES, a);
-                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i + 1) * ES, b);
-                        }
-                        if (v == v_t) grad_f32_store<ES>(p, gbase + (size_t)tl * ES, g_t);
-                    }
                     if (stage) {
                         // in place of the vector's logits, which this thread alone read
                         *reinterpret_cast<uint4 *>(slot + 16 * v) = E::pack2(g2);
@@ -402,6 +392,26 @@ __global__ void __launch_bounds__(NT, 1)
                     }
                     // the owner of the target's vector overwrites the target
                     if (!stage && v == v_t) E::store(gbase + (size_t)tl * ES, g_t);
+                }
+            }
+            // test hook: the whole vectors' fp32 values, before their rounding
+            // (recomputed here so that the loop above carries none of it)
+            if (grad_f32_of(p)) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = tid + k * NT;
+                    if (v >= vf0 && v < vf1) {
+                        unsigned long long g2[W2];
+                        exps(x[k], g2);
+#pragma unroll
+                        for (int i = 0; i < W2; ++i) {
+                            float a, b;
+                            f2_unpack(f2_mul(g2[i], esc2), a, b);
+                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i) * ES, a);
+                            grad_f32_store<ES>(p, gbase + 16 * v + (2 * i + 1) * ES, b);
+                        }
+                        if (v == v_t) grad_f32_store<ES>(p, gbase + (size_t)tl * ES, g_t);
+                    }
                 }
             }
             // the partial vectors: element by element, by their owners

@@ -240,16 +240,6 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
                             }
                             g2[j] = f2_mul(g2[j], sc2);
                         }
-                        if (grad_f32_of(p)) {
-#pragma unroll
-                            for (int j = 0; j < W2; ++j) {
-                                float a, b;
-                                f2_unpack(g2[j], a, b);
-                                grad_f32_store<ES>(p, gvec + (v * W + 2 * j) * ES, a);
-                                grad_f32_store<ES>(p, gvec + (v * W + 2 * j + 1) * ES, b);
-                            }
-                            if (v == v_t) grad_f32_store<ES>(p, grow + (size_t)t * ES, g_t);
-                        }
                         if (vec_store) {
                             *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack2(g2);
                         } else {
@@ -263,6 +253,31 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
                         }
                         // the owner of the target's vector overwrites the target
                         if (v == v_t) E::store(grow + (size_t)t * ES, g_t);
+                    }
+                }
+                // test hook: the whole vectors' fp32 values, before their
+                // rounding (recomputed so that the loop above carries none of it)
+                if (grad_f32_of(p)) {
+#pragma unroll
+                    for (int k = 0; k < MAXV; ++k) {
+                        const int v = lane + 32 * k;
+                        if (v < nvec) {
+                            unsigned long long g2[W2];
+                            E::unpack2(x[k], g2);
+#pragma unroll
+                            for (int j = 0; j < W2; ++j) {
+                                if (!kKeepExp) {
+                                    float a, b;
+                                    f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
+                                    g2[j] = f2_pack(ex2(a), ex2(b));
+                                }
+                                float a, b;
+                                f2_unpack(f2_mul(g2[j], sc2), a, b);
+                                grad_f32_store<ES>(p, gvec + (v * W + 2 * j) * ES, a);
+                                grad_f32_store<ES>(p, gvec + (v * W + 2 * j + 1) * ES, b);
+                            }
+                            if (v == v_t) grad_f32_store<ES>(p, grow + (size_t)t * ES, g_t);
+                        }
                     }
                 }
                 if (ragged) {

@@ -25,27 +25,33 @@ def test_algorithmic_bytes():
 
 def test_recorded_traffic_applies_only_to_the_captured_kernel_and_launch(tmp_path, monkeypatch):
     plan = {"path": "rows_warp", "split": 1, "ctas": 256, "threads": 512, "smem_bytes": 65536}
-    rec = {"w": {"dram_bytes_per_launch": 123, "source_sha": bench.source_hash(), "plan": plan}}
+    rec = {"w": {"dram_bytes_per_launch": 123, "kernel": "rows_warp",
+                 "source_sha": bench.source_hash("rows_warp"), "plan": plan}}
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "source_hash", lambda: rec["w"]["source_sha"])
+    monkeypatch.setattr(bench, "source_hash", lambda kernel=None: rec["w"]["source_sha"])
     assert bench.recorded_traffic("w", plan) == 123
     assert bench.recorded_traffic("w", dict(plan, ctas=152)) is None
     assert bench.recorded_traffic("other", plan) is None
-    monkeypatch.setattr(bench, "source_hash", lambda: "0" * 16)
+    monkeypatch.setattr(bench, "source_hash", lambda kernel=None: "0" * 16)
     assert bench.recorded_traffic("w", plan) is None
 
 
-def test_device_code_hash_ignores_the_host_layer():
-    """The hash covers every csrc file but the host-only C-ABI layer."""
+def test_device_code_hashes_ignore_the_host_layer():
+    """The hashes cover device code only: all of it, or one kernel's file and
+    the shared headers (so a change to one kernel leaves the others' records
+    valid)."""
     import glob
     import os
 
     files = glob.glob(os.path.join(bench.ROOT, "softmax_cross_entropy_row_gb300", "csrc", "*"))
     names = {os.path.basename(f) for f in files}
     assert "ce_api.cu" in names and set(bench.HOST_ONLY_SOURCES) <= names
+    assert set(bench.KERNEL_SOURCES.values()) | set(bench.SHARED_DEVICE_SOURCES) <= names
     assert len(bench.source_hash()) == 16
+    hashes = {k: bench.source_hash(k) for k in bench.KERNEL_SOURCES}
+    assert len(set(hashes.values())) == len(hashes)
 
 
 @pytest.mark.parametrize("name", ["classifier_4096x1000_f32", "lm_head_8192x32000_bf16",
@@ -56,9 +62,12 @@ def test_committed_traffic_matches_the_current_kernels(name):
     capture (the bench then reports the traffic as null)."""
     with open(f"{bench.ROOT}/profiles/traffic.json") as f:
         rec = json.load(f)[name]
-    if rec["source_sha"] != bench.source_hash():
-        pytest.skip("kernels changed since the capture")
-    # DRAM reads match the logits' bytes: the logits cross HBM once
+    if rec["source_sha"] != bench.source_hash(rec["kernel"]):
+        pytest.skip("the kernel changed since the capture")
+    # DRAM reads match the logits' bytes: the logits cross HBM once; and the
+    # traffic per launch is the reads and writes of that launch
     w = wl.WORKLOADS_BY_NAME[name]
     logits = rec["captured_rows"] * w.C * w.elem_bytes
-    assert abs(rec["dram_read_bytes_captured"] / logits - 1.0) < 0.01
+    assert abs(rec["dram_read_bytes_per_launch"] / logits - 1.0) < 0.01
+    assert rec["dram_bytes_per_launch"] == (rec["dram_read_bytes_per_launch"]
+                                            + rec["dram_write_bytes_per_launch"])
