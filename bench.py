@@ -12,8 +12,8 @@ one ``ce_fwd_bwd`` call: the loss and the full gradient of one batch.
 Timing: steps run from a CUDA graph (one library call per step, captured
 once), cycling through enough buffer sets that every step reads inputs that
 are not in L2; CUDA events on the launching stream bracket the timed steps.
-``e2e`` times the host-buffer call ce_fwd_bwd_host, eagerly: every step copies
-its inputs from pinned host memory and its loss back.  ``--impl reference`` times
+``e2e`` times the host-buffer call ce_fwd_bwd_host_grad, eagerly: every step
+copies its inputs from pinned host memory and its gradient and loss back.  ``--impl reference`` times
 the fp64 CPU oracle (the only reference this path has) on the host cores.
 
 With torchrun (N > 1) every rank runs an independent replica of the workload
@@ -380,9 +380,10 @@ def bench_workload(w, inp, steps, warmup, device, l2_bytes, hbm_peak, peak_note,
 
 
 def bench_e2e(w, inp, device, steps, world=1):
-    """The public call with host buffers, ce_fwd_bwd_host: every step copies
-    the pinned logits and targets to the device, runs the fused kernel and
-    copies the 4-byte loss back to the host."""
+    """The public call with host buffers, ce_fwd_bwd_host_grad: every step
+    copies the pinned logits and targets to the device, runs the kernels and
+    copies the gradient and the loss back to pinned host memory (chunk by
+    chunk, the copies in and out overlapping)."""
     import torch
 
     import softmax_cross_entropy_row_gb300 as ce
@@ -393,11 +394,11 @@ def bench_e2e(w, inp, device, steps, world=1):
         hz = torch.from_numpy(inp.logits).pin_memory()
     ht = torch.from_numpy(inp.targets).pin_memory()
     hl = torch.empty(1, dtype=torch.float32).pin_memory()
-    dg = torch.empty(hz.shape, dtype=hz.dtype, device=device)
+    hg = torch.empty(hz.shape, dtype=hz.dtype).pin_memory()
     s = torch.cuda.Stream(device)
 
     def step():
-        ce.ce_fwd_bwd_host(hz, ht, hl, dg, s)
+        ce.ce_fwd_bwd_host_grad(hz, ht, hl, hg, s)
 
     with torch.cuda.stream(s):
         for _ in range(3):
@@ -413,10 +414,13 @@ def bench_e2e(w, inp, device, steps, world=1):
         e1.synchronize()
     per_step = max_over_ranks(e0.elapsed_time(e1) / 1e3, device) / steps
     h2d = hz.numel() * hz.element_size() + ht.numel() * ht.element_size()
-    # whole-job figures: every replica copies its own inputs and loss
+    d2h = hg.numel() * hg.element_size() + hl.numel() * hl.element_size()
+    del hg
+    # whole-job figures: every replica copies its own inputs and results
     return {"value": replica_rows_per_s(w.B, world, per_step), "unit": "rows/s",
-            "h2d_bytes_per_step": int(world * h2d), "d2h_bytes_per_step": 4 * world,
-            "steps": steps, "ms_per_step": per_step * 1e3}
+            "h2d_bytes_per_step": int(world * h2d), "d2h_bytes_per_step": int(world * d2h),
+            "steps": steps, "ms_per_step": per_step * 1e3,
+            "call": "ce_fwd_bwd_host_grad (pinned host logits, targets, loss and gradient)"}
 
 
 # The rows beyond the plain fused step, measured the same way: (label, workload,

@@ -196,18 +196,35 @@ int ce_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int 
  * same L (the same bits) and gradient, with the copies to the device made by
  * the library.  logits_host [B][C] in `dtype` and targets_host [B] int32:
  * host memory (page-locked for asynchronous copies; pageable memory works,
- * with copies the host waits for); loss_host: one fp32 in host
- * memory, written when `stream` reaches the end of the call (synchronise the
- * stream before reading it); grad_out: device [B][C] in `dtype`, as for
- * ce_fwd_bwd (the gradient stays on the device for the backward pass).  The
- * copies into library-owned device buffers, the kernel of ce_fwd_bwd and the
- * copy of the loss back run in order on `stream`.  The library keeps per-stream
- * device copies of the last inputs (B*C*elem + 4B bytes) until
- * ce_release_workspaces.  Not capturable (CE_ERR_CAPTURE while `stream` is
- * being captured).  Returns a ce_status; argument checks as for ce_fwd_bwd.
+ * with copies the host waits for); loss_host: one fp32 in host memory,
+ * written when `stream` reaches the end of the call (synchronise the stream
+ * before reading it); grad_out: device [B][C] in `dtype`, as for ce_fwd_bwd
+ * (the gradient stays on the device for the backward pass).  The batch goes
+ * through in chunks of rows (a multiple of 16 rows, at most 64 MiB of
+ * logits each): a chunk's copy in runs on a library stream while the kernel
+ * of the chunk before runs on `stream`, and the call's work all lies between
+ * its start and its end on `stream`.  The gradient has the bits of ce_fwd_bwd
+ * whenever grad_out is 16-byte aligned.  The library keeps per-stream staging
+ * buffers (two chunks) and two helper streams until ce_release_workspaces.
+ * Not capturable (CE_ERR_CAPTURE while `stream` is being captured).  Returns a
+ * ce_status; argument checks as for ce_fwd_bwd.
  */
 int ce_fwd_bwd_host(const void *logits_host, const int32_t *targets_host, int64_t B, int64_t C,
                     int dtype, float *loss_host, void *grad_out, void *stream);
+
+/*
+ * ce_fwd_bwd_host_grad -- ce_fwd_bwd_host with the gradient returned to host
+ * memory too: grad_host [B][C] in `dtype`, host memory (page-locked for
+ * asynchronous copies), written when `stream` reaches the end of the call.
+ * Each chunk's gradient is copied out on a second library stream while later
+ * chunks are copied in and computed, so the two directions of the copy
+ * engines overlap.  The loss and the gradient have the bits of ce_fwd_bwd on
+ * 16-byte aligned device buffers.  Staging: two chunks of logits and two of
+ * gradient per stream.  Outputs may not overlap the inputs.  Otherwise as
+ * ce_fwd_bwd_host.
+ */
+int ce_fwd_bwd_host_grad(const void *logits_host, const int32_t *targets_host, int64_t B,
+                         int64_t C, int dtype, float *loss_host, void *grad_host, void *stream);
 
 /*
  * ce_query_plan -- the launch that ce_fwd_bwd would make for this shape on

@@ -49,7 +49,8 @@ STATUS = {0: "CE_OK", 1: "CE_ERR_NULL", 2: "CE_ERR_SHAPE", 3: "CE_ERR_DTYPE",
 EXPORTS = ("ce_fwd_bwd", "ce_fwd_bwd_path", "ce_query_plan", "ce_get_device_errors",
            "ce_release_workspaces", "ce_status_string", "ce_last_cuda_error",
            "ce_fwd_bwd_noalloc", "ce_fwd_bwd_ex", "ce_fwd_bwd_ex_path", "ce_forward",
-           "ce_softmax_fwd", "ce_softmax_fwd_path", "ce_softmax_bwd", "ce_fwd_bwd_host")
+           "ce_softmax_fwd", "ce_softmax_fwd_path", "ce_softmax_bwd", "ce_fwd_bwd_host",
+           "ce_fwd_bwd_host_grad")
 # Symbols declared in include/ce_testing.h (test hooks).
 TEST_EXPORTS = ("ce_fwd_bwd_test",)
 
@@ -110,6 +111,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.ce_softmax_fwd.restype = ci
     lib.ce_fwd_bwd_host.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp]
     lib.ce_fwd_bwd_host.restype = ci
+    lib.ce_fwd_bwd_host_grad.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp]
+    lib.ce_fwd_bwd_host_grad.restype = ci
     lib.ce_softmax_fwd_path.argtypes = [vp, i64, i64, ci, vp, vp, ci, ci]
     lib.ce_softmax_fwd_path.restype = ci
     lib.ce_softmax_bwd.argtypes = [vp, vp, i64, i64, ci, vp, vp]
@@ -255,6 +258,25 @@ def ce_fwd_bwd_host(logits_host, targets_host, loss_host, grad_out, stream=None)
     _check(lib.ce_fwd_bwd_host(_ptr(logits_host), _ptr(targets_host), B, C,
                                _dtype_code(logits_host), _ptr(loss_host), _ptr(grad_out),
                                _stream_handle(stream)))
+
+
+def ce_fwd_bwd_host_grad(logits_host, targets_host, loss_host, grad_host, stream=None) -> None:
+    """ce_fwd_bwd with the logits, targets, loss and gradient all in host memory
+    (CPU tensors, page-locked for asynchronous copies).  The outputs are
+    written when ``stream`` reaches the end of the call."""
+    lib = load_library()
+    if logits_host.dim() != 2 or not logits_host.is_contiguous():
+        raise ValueError("logits_host must be a contiguous [B, C] tensor")
+    if grad_host.shape != logits_host.shape or grad_host.dtype != logits_host.dtype or \
+            not grad_host.is_contiguous():
+        raise ValueError("grad_host must be a contiguous tensor of the logits' shape and dtype")
+    _check_io(logits_host, targets_host, loss_host, device="cpu")
+    if grad_host.device.type != "cpu":
+        raise ValueError("grad_host must be a CPU tensor")
+    B, C = logits_host.shape
+    _check(lib.ce_fwd_bwd_host_grad(_ptr(logits_host), _ptr(targets_host), B, C,
+                                    _dtype_code(logits_host), _ptr(loss_host), _ptr(grad_host),
+                                    _stream_handle(stream)))
 
 
 def ce_softmax_fwd(logits, probs_out, stream=None, path=CE_PATH_AUTO, split=0) -> None:

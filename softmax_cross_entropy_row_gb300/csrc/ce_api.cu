@@ -413,15 +413,24 @@ std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
 // ce_release_workspaces.
 std::vector<std::pair<int, unsigned char *>> g_ws_retired;
 
-// Host-buffer entry point: per (device, stream) device copies of the logits
-// and targets.  Guarded by g_ws_mu.
-struct HostStage {
-    unsigned char *z = nullptr;
-    size_t zbytes = 0;
-    unsigned char *t = nullptr;
+// Host-buffer entry points: per (device, stream) staging buffers (two chunks
+// of logits, two of gradient, the targets), two helper streams for the copies
+// in and out, and the events that order the three streams.  Guarded by
+// g_ws_mu.
+struct HostPipe {
+    unsigned char *z[2] = {nullptr, nullptr};  // logits chunks
+    unsigned char *g[2] = {nullptr, nullptr};  // gradient chunks (gradient to the host)
+    size_t chunk_bytes = 0;                    // bytes of each z / g buffer
+    size_t g_bytes = 0;                        // bytes of each g buffer allocated (0: none)
+    unsigned char *t = nullptr;                // targets
     size_t tbytes = 0;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+    cudaEvent_t ev_in[2] = {nullptr, nullptr};   // chunk copied in
+    cudaEvent_t ev_k[2] = {nullptr, nullptr};    // chunk's kernel done
+    cudaEvent_t ev_out[2] = {nullptr, nullptr};  // chunk's gradient copied out
 };
-std::map<std::pair<int, uintptr_t>, HostStage> g_hs;
+std::map<std::pair<int, uintptr_t>, HostPipe> g_hs;
 
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kLossSlot = 64;  // header bytes holding the host entry's device copy of L
@@ -767,57 +776,102 @@ int run_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int
 
 // ------------------------------------------------------ host-buffer entry
 //
-// ce_fwd_bwd_host: the copies of the logits and targets into the stream's
-// staging buffers, the launch of ce_fwd_bwd on them and the copy of the loss
-// back, in order on the caller's stream.  A copy engine moves ~160-200 GB/s
-// from page-locked memory on GB300, so the copy dominates the call;
-// splitting the batch into chunks whose copies overlap the kernels of the
-// chunks before (on a second stream) measured no faster.
+// ce_fwd_bwd_host and ce_fwd_bwd_host_grad: the batch goes through in chunks
+// of rows.  A chunk's logits are copied in on one helper stream, its kernel
+// runs on the caller's stream, and (for ce_fwd_bwd_host_grad) its gradient is
+// copied out on the other helper stream, so the copies of one chunk overlap
+// the kernels and copies of its neighbours; a copy engine moves ~210 GB/s
+// each way from page-locked memory on GB300, ~340 GB/s both ways at once.
+// Each chunk's kernel writes its rows' losses; one last launch sums them in
+// the fixed order of the fused kernels, so the loss has the bits of
+// ce_fwd_bwd.  A chunk holds a multiple of 16 rows, so every row keeps the
+// alignment it has in a 16-byte aligned tensor, and with it the gradient's
+// bits.
 
-int host_stage(int dev, cudaStream_t s, size_t zbytes, size_t tbytes, HostStage **out) {
+// Logits bytes per chunk, at most.  Measured on GB300 (16384 x 50257 fp32,
+// gradient to the host): 64 MiB chunks keep the copies in and out running at
+// once (20 ms, ~330 GB/s both ways); 128 and 256 MiB chunks ran the two
+// directions one after the other (31-33 ms); 32 MiB chunks leave the host
+// issuing more calls than the copies take.
+constexpr size_t kHostChunkBytes = 64u << 20;
+
+// Tuning knob: CE_HOST_CHUNK_MB sets the chunk's logits bytes (MiB).  Read once.
+size_t host_chunk_bytes() {
+    static const size_t b = [] {
+        const char *e = getenv("CE_HOST_CHUNK_MB");
+        const long v = e ? atol(e) : 0;
+        return v > 0 ? (size_t)v << 20 : kHostChunkBytes;
+    }();
+    return b;
+}
+
+int host_pipe(int dev, cudaStream_t s, size_t chunk_bytes, bool grad_host, size_t tbytes,
+              HostPipe **out) {
     std::lock_guard<std::mutex> lk(g_ws_mu);
-    HostStage &h = g_hs[{dev, reinterpret_cast<uintptr_t>(s)}];
+    HostPipe &h = g_hs[{dev, reinterpret_cast<uintptr_t>(s)}];
     cudaError_t e;
-    // outgrown staging buffers may still be read by queued kernels: retired
-    if (h.zbytes < zbytes) {
-        if (h.z) g_ws_retired.push_back({dev, h.z});
-        h.z = nullptr;
-        h.zbytes = 0;
+    if (!h.s_in) {
+        if ((e = cudaStreamCreateWithFlags(&h.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&h.s_out, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e);
+        cudaEvent_t *evs[] = {&h.ev_start, &h.ev_end, &h.ev_in[0], &h.ev_in[1],
+                              &h.ev_k[0],  &h.ev_k[1], &h.ev_out[0], &h.ev_out[1]};
+        for (cudaEvent_t *ev : evs)
+            if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e);
+    }
+    // outgrown buffers may still be read by queued work: retired, not freed
+    auto grow = [&](unsigned char **b, size_t have, size_t need, size_t quantum) -> int {
+        if (have >= need && *b) return CE_OK;
+        if (*b) g_ws_retired.push_back({dev, *b});
+        *b = nullptr;
         void *p = nullptr;
-        const size_t bytes = align_up(zbytes, 1 << 20);
-        if ((e = cudaMalloc(&p, bytes)) != cudaSuccess) return cuda_fail(e);
-        h.z = static_cast<unsigned char *>(p);
-        h.zbytes = bytes;
+        cudaError_t err = cudaMalloc(&p, align_up(need, quantum));
+        if (err != cudaSuccess) return cuda_fail(err);
+        *b = static_cast<unsigned char *>(p);
+        return CE_OK;
+    };
+    int rc;
+    if (h.chunk_bytes < chunk_bytes) {
+        for (int b = 0; b < 2; ++b)
+            if ((rc = grow(&h.z[b], 0, chunk_bytes, 1 << 20)) != CE_OK) return rc;
+        h.chunk_bytes = align_up(chunk_bytes, 1 << 20);
+    }
+    if (grad_host && h.g_bytes < h.chunk_bytes) {
+        for (int b = 0; b < 2; ++b)
+            if ((rc = grow(&h.g[b], 0, h.chunk_bytes, 1 << 20)) != CE_OK) return rc;
+        h.g_bytes = h.chunk_bytes;
     }
     if (h.tbytes < tbytes) {
-        if (h.t) g_ws_retired.push_back({dev, h.t});
-        h.t = nullptr;
-        h.tbytes = 0;
-        void *p = nullptr;
-        const size_t bytes = align_up(tbytes, 1 << 16);
-        if ((e = cudaMalloc(&p, bytes)) != cudaSuccess) return cuda_fail(e);
-        h.t = static_cast<unsigned char *>(p);
-        h.tbytes = bytes;
+        if ((rc = grow(&h.t, 0, tbytes, 1 << 16)) != CE_OK) return rc;
+        h.tbytes = align_up(tbytes, 1 << 16);
     }
     *out = &h;  // map nodes are stable; entries are erased only by ce_release_workspaces
     return CE_OK;
 }
 
+// grad_dev: device gradient (ce_fwd_bwd_host); grad_host: host gradient
+// (ce_fwd_bwd_host_grad).  Exactly one is set.
 int run_host(const void *logits_host, const int32_t *targets_host, int64_t B, int64_t C,
-             int dtype, float *loss_host, void *grad_out, void *stream) {
+             int dtype, float *loss_host, void *grad_dev, void *grad_host, void *stream) {
     if (dtype != CE_F32 && dtype != CE_BF16 && dtype != CE_F16) return CE_ERR_DTYPE;
-    if (!logits_host || !targets_host || !loss_host || !grad_out) return CE_ERR_NULL;
+    if (!logits_host || !targets_host || !loss_host || !(grad_dev || grad_host))
+        return CE_ERR_NULL;
     if (B < 1 || C < 1 || B > 0x7fffffffLL || C > 0x7fffffffLL) return CE_ERR_SHAPE;
     const int es = dtype == CE_F32 ? 4 : 2;
     if ((unsigned long long)B * (unsigned long long)C > (1ull << 61) / (unsigned)es)
         return CE_ERR_SHAPE;
     const uintptr_t lz = reinterpret_cast<uintptr_t>(logits_host);
-    const uintptr_t gz = reinterpret_cast<uintptr_t>(grad_out);
-    if (lz % es || gz % es || reinterpret_cast<uintptr_t>(targets_host) % 4 ||
-        reinterpret_cast<uintptr_t>(loss_host) % 4)
-        return CE_ERR_ALIGN;
+    const uintptr_t gz = reinterpret_cast<uintptr_t>(grad_dev ? grad_dev : grad_host);
+    const uintptr_t tz = reinterpret_cast<uintptr_t>(targets_host);
+    const uintptr_t oz = reinterpret_cast<uintptr_t>(loss_host);
+    if (lz % es || gz % es || tz % 4 || oz % 4) return CE_ERR_ALIGN;
     const size_t nbytes = (size_t)B * (size_t)C * es;
     if (ranges_overlap(gz, nbytes, lz, nbytes)) return CE_ERR_OVERLAP;
+    if (grad_host && (ranges_overlap(gz, nbytes, tz, (size_t)B * 4) ||
+                      ranges_overlap(gz, nbytes, oz, 4) || ranges_overlap(oz, 4, lz, nbytes) ||
+                      ranges_overlap(oz, 4, tz, (size_t)B * 4)))
+        return CE_ERR_OVERLAP;
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -825,60 +879,108 @@ int run_host(const void *logits_host, const int32_t *targets_host, int64_t B, in
     DeviceInfo d;
     int rc = device_info(dev, &d);
     if (rc != CE_OK) return rc;
-    if ((rc = check_pointer(grad_out, d)) != CE_OK) return rc;
+    if (grad_dev && (rc = check_pointer(grad_dev, d)) != CE_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if ((e = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return cuda_fail(e);
     if (cs != cudaStreamCaptureStatusNone) return CE_ERR_CAPTURE;
 
+    // chunks: a multiple of 16 rows, at most kHostChunkBytes of logits (at
+    // least 16 rows)
+    const size_t row_bytes = (size_t)C * es;
+    long long chunk_rows = (long long)(host_chunk_bytes() / row_bytes) / 16 * 16;
+    if (chunk_rows < 16) chunk_rows = 16;
+    if (chunk_rows > B) chunk_rows = B;
     Plan pl;
-    if ((rc = make_plan(B, C, dtype, CE_PATH_AUTO, 0, &pl)) != CE_OK) return rc;
-    const size_t rows_bytes = align_up((size_t)B, 1024) * sizeof(float);
-    size_t need = kHeaderBytes + rows_bytes;
-    size_t parts_off = 0, zt_off = 0;
-    if (pl.path == CE_PATH_STREAM) {
-        parts_off = need;
-        need += align_up((size_t)B * (size_t)pl.chunks * sizeof(float2), 256);
-        zt_off = need;
-        need += align_up((size_t)B * sizeof(float), 256);
-    }
+    if ((rc = make_plan(chunk_rows, C, dtype, CE_PATH_AUTO, 0, &pl)) != CE_OK) return rc;
+    if (pl.path == CE_PATH_STREAM) return CE_ERR_PATH;  // never planned (needs partials per chunk)
     Workspace ws;
-    if ((rc = get_workspace(dev, s, need, &ws)) != CE_OK) return rc;
-    HostStage *h = nullptr;
-    if ((rc = host_stage(dev, s, nbytes, (size_t)B * 4, &h)) != CE_OK) return rc;
+    if ((rc = get_workspace(dev, s, kHeaderBytes + align_up((size_t)B, 1024) * sizeof(float),
+                            &ws)) != CE_OK)
+        return rc;
+    HostPipe *h = nullptr;
+    if ((rc = host_pipe(dev, s, (size_t)chunk_rows * row_bytes, grad_host != nullptr,
+                        (size_t)B * 4, &h)) != CE_OK)
+        return rc;
 
+    float *rows = reinterpret_cast<float *>(ws.base + kHeaderBytes);
     float *dloss = reinterpret_cast<float *>(ws.base + kLossSlot);
-    const uintptr_t zz = reinterpret_cast<uintptr_t>(h->z);
-    ce::ParamsEx p;
-    p.logits = h->z;
-    p.targets = reinterpret_cast<const int32_t *>(h->t);
-    p.grad = static_cast<unsigned char *>(grad_out);
-    p.loss_out = dloss;
-    p.loss_rows = reinterpret_cast<float *>(ws.base + kHeaderBytes);
-    p.ticket = reinterpret_cast<unsigned int *>(ws.base);
-    p.err = reinterpret_cast<int *>(ws.base + 4);
-    p.parts = pl.path == CE_PATH_STREAM ? reinterpret_cast<float2 *>(ws.base + parts_off) : nullptr;
-    p.zt = pl.path == CE_PATH_STREAM ? reinterpret_cast<float *>(ws.base + zt_off) : nullptr;
-    p.B = B;
-    p.C = C;
-    p.inv_b = (float)(1.0 / (double)B);
-    p.lo_clip = (uint64_t)((zz + 15) & ~(uintptr_t)15);
-    p.hi_clip = (uint64_t)((zz + nbytes) & ~(uintptr_t)15);
-    if (p.hi_clip < p.lo_clip) p.hi_clip = p.lo_clip;
-    p.grad_vec_ok = ((gz - zz) % 16) == 0;
-    p.reduction = CE_REDUCE_MEAN;
-    p.grad_base = p.inv_b;
-    p.grad_scale = nullptr;
-    p.scale_per_row = 0;
-    p.softmax = 0;
-
-    if ((e = cudaMemcpyAsync(h->z, logits_host, nbytes, cudaMemcpyDefault, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(h->t, targets_host, (size_t)B * 4, cudaMemcpyDefault, s)) !=
-            cudaSuccess ||
-        (e = launch_plan(p, dtype, pl, s)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(loss_host, dloss, sizeof(float), cudaMemcpyDefault, s)) !=
+    const float inv_b = (float)(1.0 / (double)B);
+    auto fail = [&](cudaError_t err) { return cuda_fail(err); };
+    if ((e = cudaEventRecord(h->ev_start, s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(h->s_in, h->ev_start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(h->s_out, h->ev_start, 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->t, targets_host, (size_t)B * 4, cudaMemcpyDefault, h->s_in)) !=
             cudaSuccess)
-        return cuda_fail(e);
+        return fail(e);
+    const long long nchunks = (B + chunk_rows - 1) / chunk_rows;
+    for (long long i = 0; i < nchunks; ++i) {
+        const int b = (int)(i & 1);
+        const long long r0 = i * chunk_rows;
+        const long long nr = r0 + chunk_rows <= B ? chunk_rows : B - r0;
+        const size_t off = (size_t)r0 * row_bytes, cb = (size_t)nr * row_bytes;
+        // copy in once the kernel two chunks back has read this buffer
+        if ((i >= 2 && (e = cudaStreamWaitEvent(h->s_in, h->ev_k[b], 0)) != cudaSuccess) ||
+            (e = cudaMemcpyAsync(h->z[b], static_cast<const unsigned char *>(logits_host) + off,
+                                 cb, cudaMemcpyDefault, h->s_in)) != cudaSuccess ||
+            (e = cudaEventRecord(h->ev_in[b], h->s_in)) != cudaSuccess)
+            return fail(e);
+        // the chunk's kernel, once its logits are in and (gradient to the
+        // host) the copy out two chunks back has read its gradient buffer
+        if ((e = cudaStreamWaitEvent(s, h->ev_in[b], 0)) != cudaSuccess ||
+            (grad_host && i >= 2 && (e = cudaStreamWaitEvent(s, h->ev_out[b], 0)) != cudaSuccess))
+            return fail(e);
+        unsigned char *gdst = grad_host ? h->g[b] : static_cast<unsigned char *>(grad_dev) + off;
+        const uintptr_t zz = reinterpret_cast<uintptr_t>(h->z[b]);
+        ce::ParamsEx p;
+        p.logits = h->z[b];
+        p.targets = reinterpret_cast<const int32_t *>(h->t) + r0;
+        p.grad = gdst;
+        p.loss_out = rows + r0;
+        p.loss_rows = rows + r0;  // the chunk's row losses, summed at the end
+        p.ticket = reinterpret_cast<unsigned int *>(ws.base);
+        p.err = reinterpret_cast<int *>(ws.base + 4);
+        p.parts = nullptr;
+        p.zt = nullptr;
+        p.B = nr;
+        p.C = C;
+        p.inv_b = inv_b;
+        p.lo_clip = (uint64_t)((zz + 15) & ~(uintptr_t)15);
+        p.hi_clip = (uint64_t)((zz + cb) & ~(uintptr_t)15);
+        if (p.hi_clip < p.lo_clip) p.hi_clip = p.lo_clip;
+        p.grad_vec_ok = ((reinterpret_cast<uintptr_t>(gdst) - zz) % 16) == 0;
+        p.reduction = CE_REDUCE_NONE;
+        p.grad_base = inv_b;  // the gradient of the mean over all B rows
+        p.grad_scale = nullptr;
+        p.scale_per_row = 0;
+        p.softmax = 0;
+        Plan cp = pl;
+        if (nr != chunk_rows && (rc = make_plan(nr, C, dtype, CE_PATH_AUTO, 0, &cp)) != CE_OK)
+            return rc;
+        if ((e = launch_plan(p, dtype, cp, s)) != cudaSuccess ||
+            (e = cudaEventRecord(h->ev_k[b], s)) != cudaSuccess)
+            return fail(e);
+        if (grad_host &&
+            ((e = cudaStreamWaitEvent(h->s_out, h->ev_k[b], 0)) != cudaSuccess ||
+             (e = cudaMemcpyAsync(static_cast<unsigned char *>(grad_host) + off, h->g[b], cb,
+                                  cudaMemcpyDefault, h->s_out)) != cudaSuccess ||
+             (e = cudaEventRecord(h->ev_out[b], h->s_out)) != cudaSuccess))
+            return fail(e);
+    }
+    // the batch loss over all rows, in the fused kernels' order, and its copy
+    // back; the call ends on `stream` once the last gradient chunk is out
+    ce::Params tp;
+    tp.loss_rows = rows;
+    tp.loss_out = dloss;
+    tp.ticket = reinterpret_cast<unsigned int *>(ws.base);
+    tp.B = B;
+    tp.inv_b = inv_b;
+    if ((e = ce::launch_batch_loss(tp, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(loss_host, dloss, sizeof(float), cudaMemcpyDefault, s)) !=
+            cudaSuccess ||
+        (e = cudaEventRecord(h->ev_end, h->s_out)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, h->ev_end, 0)) != cudaSuccess)
+        return fail(e);
     e = cudaGetLastError();
     return e == cudaSuccess ? CE_OK : cuda_fail(e);
 }
@@ -901,7 +1003,14 @@ int ce_softmax_fwd_path(const void *logits, int64_t B, int64_t C, int dtype, voi
 
 int ce_fwd_bwd_host(const void *logits_host, const int32_t *targets_host, int64_t B, int64_t C,
                     int dtype, float *loss_host, void *grad_out, void *stream) {
-    return run_host(logits_host, targets_host, B, C, dtype, loss_host, grad_out, stream);
+    if (!grad_out) return CE_ERR_NULL;
+    return run_host(logits_host, targets_host, B, C, dtype, loss_host, grad_out, nullptr, stream);
+}
+
+int ce_fwd_bwd_host_grad(const void *logits_host, const int32_t *targets_host, int64_t B,
+                         int64_t C, int dtype, float *loss_host, void *grad_host, void *stream) {
+    if (!grad_host) return CE_ERR_NULL;
+    return run_host(logits_host, targets_host, B, C, dtype, loss_host, nullptr, grad_host, stream);
 }
 
 int ce_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int dtype,
@@ -1002,13 +1111,19 @@ int ce_release_workspaces(void) {
         if (e != cudaSuccess) rc = cuda_fail(e);
     }
     for (auto &kv : g_hs) {
-        HostStage &h = kv.second;
+        HostPipe &h = kv.second;
         cudaSetDevice(kv.first.first);
-        for (void *b : {(void *)h.z, (void *)h.t})
+        for (void *b : {(void *)h.z[0], (void *)h.z[1], (void *)h.g[0], (void *)h.g[1],
+                        (void *)h.t})
             if (b) {
                 cudaError_t e = cudaFree(b);
                 if (e != cudaSuccess) rc = cuda_fail(e);
             }
+        for (cudaStream_t st : {h.s_in, h.s_out})
+            if (st) cudaStreamDestroy(st);
+        for (cudaEvent_t ev : {h.ev_start, h.ev_end, h.ev_in[0], h.ev_in[1], h.ev_k[0], h.ev_k[1],
+                               h.ev_out[0], h.ev_out[1]})
+            if (ev) cudaEventDestroy(ev);
     }
     for (auto &r : g_ws_retired) {
         cudaSetDevice(r.first);

@@ -71,6 +71,11 @@ cudaError_t launch_twopass(const ParamsEx &p, int dtype, int ctas, int nslots, i
                            cudaStream_t s);
 cudaError_t twopass_max_ctas_per_sm(int dtype, int smem, int *ctas);
 
+// The batch loss (mean or sum, as p's reduction says) of p.B row losses at
+// p.loss_rows written by earlier launches, in the fused kernels' fixed order:
+// one CTA of kTailThreads threads (ce_batch_loss.cu).
+cudaError_t launch_batch_loss(const Params &p, cudaStream_t s);
+
 // Streaming path: pass A (chunk partials) and pass B (combine, gradient, loss).
 cudaError_t launch_stream(const ParamsEx &p, int dtype, long long chunks, cudaStream_t s);
 

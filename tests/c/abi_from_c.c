@@ -39,6 +39,8 @@ int main(void) {
     EXPECT(ce_softmax_fwd(z, 4, 4, CE_F32, NULL, NULL), CE_ERR_NULL);
     EXPECT(ce_softmax_bwd(z, z, 4, 4, 9, g, NULL), CE_ERR_DTYPE);
     EXPECT(ce_fwd_bwd_host(z, t, 4, 4, CE_F32, loss, NULL, NULL), CE_ERR_NULL);
+    EXPECT(ce_fwd_bwd_host_grad(z, t, 4, 4, CE_F32, loss, NULL, NULL), CE_ERR_NULL);
+    EXPECT(ce_fwd_bwd_host_grad(z, t, 4, 4, CE_F32, loss, (char *)z + 8, NULL), CE_ERR_OVERLAP);
     EXPECT(ce_fwd_bwd_noalloc(z, t, 1LL << 40, 4, CE_F32, loss, g, NULL), CE_ERR_SHAPE);
     if (strcmp(ce_status_string(CE_OK), "unknown status") == 0) ++failures;
     if (strcmp(ce_status_string(12345), "unknown status") != 0) ++failures;

@@ -124,6 +124,11 @@ def test_host_side_errors_of_the_host_buffer_entry(lib):
     assert h(258, 512, 4, 4, 0, 1024, 4096, None) == 4       # fp32 logits at 2 mod 4
     assert h(256, 514, 4, 4, 0, 1024, 4096, None) == 4       # targets at 2 mod 4
     assert h(1 << 20, 512, 4, 4, 0, 1024, (1 << 20) + 32, None) == 6  # gradient over logits
+    g = lib.ce_fwd_bwd_host_grad
+    assert g(256, 512, 4, 4, 0, 1024, None, None) == 1                 # NULL host gradient
+    assert g(256, 512, 4, 4, 1, 1024, 4097, None) == 4                 # bf16 gradient at an odd address
+    assert g(1 << 20, 1 << 24, 4, 4, 0, 1 << 25, (1 << 24) - 16, None) == 6  # gradient over targets
+    assert g(1 << 20, 1 << 24, 4, 4, 0, (1 << 20) + 4, 1 << 26, None) == 6   # loss inside the logits
 
 
 def test_no_cpu_fallback_without_library(tmp_path):

@@ -1,7 +1,8 @@
-"""GPU parity of the host-buffer entry point ce_fwd_bwd_host: the same loss
-bits and gradient as ce_fwd_bwd on the same inputs (the same kernel on
-library-owned device copies), on every path, and the oracle's values on the
-small cases."""
+"""GPU parity of the host-buffer entry points ce_fwd_bwd_host (gradient on the
+device) and ce_fwd_bwd_host_grad (gradient back in host memory): the same loss
+bits and gradient as ce_fwd_bwd on the same inputs (the same kernels on
+library-owned device copies, chunk by chunk), on every path, and the oracle's
+values on the small cases."""
 
 import numpy as np
 import pytest
@@ -41,10 +42,16 @@ def _host_inputs(inp, pinned):
     return z, t, loss
 
 
-def _both(inp, pinned=True, stream=None):
+def _both(inp, pinned=True, stream=None, grad_to_host=False):
     zh, th, lh = _host_inputs(inp, pinned)
-    grad_h = torch.empty(zh.shape, dtype=zh.dtype, device="cuda")
-    ce.ce_fwd_bwd_host(zh, th, lh, grad_h, stream)
+    if grad_to_host:
+        grad_h = torch.empty(zh.shape, dtype=zh.dtype)
+        if pinned:
+            grad_h = grad_h.pin_memory()
+        ce.ce_fwd_bwd_host_grad(zh, th, lh, grad_h, stream)
+    else:
+        grad_h = torch.empty(zh.shape, dtype=zh.dtype, device="cuda")
+        ce.ce_fwd_bwd_host(zh, th, lh, grad_h, stream)
     z, t = device_inputs(inp)
     loss_d = torch.empty(1, device="cuda")
     grad_d = torch.empty_like(z)
@@ -53,22 +60,23 @@ def _both(inp, pinned=True, stream=None):
     return lh, grad_h, loss_d, grad_d
 
 
-# (B, C, dtype): the warp, split and streaming paths, f16, ragged rows, and
-# staging buffers of 160-260 MB
+# (B, C, dtype): the warp, split and two-pass kernels, f16, ragged rows, and
+# batches of several 64 MiB chunks (a last chunk of fewer rows included)
 CASES = [(8, 10, "f32"), (3, 200000, "f32"), (4096, 1000, "f32"), (1024, 32000, "bf16"),
          (512, 32000, "f16"), (7, 3001, "f32"), (40000, 1000, "f32"), (4096, 32000, "bf16"),
-         (110, 600000, "bf16")]
+         (110, 600000, "bf16"), (1500, 50257, "f32"), (1100, 128256, "bf16")]
 
 
 @pytest.mark.parametrize("B,C,dtype", CASES)
 @pytest.mark.parametrize("pinned", [True, False])
-def test_host_entry_matches_the_device_entry(B, C, dtype, pinned):
+@pytest.mark.parametrize("grad_to_host", [False, True])
+def test_host_entry_matches_the_device_entry(B, C, dtype, pinned, grad_to_host):
     inp = wl.random_case(B, C, dtype, seed=B + C, sigma=3.0)
-    lh, grad_h, loss_d, grad_d = _both(inp, pinned)
+    lh, grad_h, loss_d, grad_d = _both(inp, pinned, grad_to_host=grad_to_host)
     assert lh.item() == loss_d.item(), (lh.item(), loss_d.item())
-    assert torch.equal(grad_h, grad_d)
+    assert torch.equal(grad_h.cuda() if grad_to_host else grad_h, grad_d)
     if B * C <= 5_000_000:
-        check_full(inp, lh, grad_h, f"host entry {B}x{C} {dtype}")
+        check_full(inp, lh, grad_h.cuda() if grad_to_host else grad_h, f"host entry {B}x{C} {dtype}")
 
 
 def test_back_to_back_calls_on_one_stream():
@@ -87,6 +95,30 @@ def test_back_to_back_calls_on_one_stream():
     s.synchronize()
     check_full(a, la, ga, "first of two calls")
     check_full(b, lb, gb, "second of two calls")
+
+
+def test_back_to_back_calls_with_the_gradient_to_the_host():
+    """Consecutive calls of different sizes on one stream, gradients to the
+    host: the staging grows between them, the results are those of the device
+    entry point."""
+    s = torch.cuda.Stream()
+    cases = [wl.random_case(700, 50257, "f32", seed=5), wl.random_case(4096, 1000, "f32", seed=6),
+             wl.random_case(1400, 50257, "f32", seed=7)]
+    outs = []
+    with torch.cuda.stream(s):
+        for inp in cases:
+            zh, th, lh = _host_inputs(inp, True)
+            gh = torch.empty(zh.shape, dtype=zh.dtype).pin_memory()
+            ce.ce_fwd_bwd_host_grad(zh, th, lh, gh, s)
+            outs.append((lh, gh))
+    s.synchronize()
+    for inp, (lh, gh) in zip(cases, outs):
+        z, t = device_inputs(inp)
+        loss_d = torch.empty(1, device="cuda")
+        grad_d = torch.empty_like(z)
+        ce.ce_fwd_bwd(z, t, loss_d, grad_d)
+        torch.cuda.synchronize()
+        assert lh.item() == loss_d.item() and torch.equal(gh.cuda(), grad_d)
 
 
 def test_capture_is_refused_and_bad_targets_are_counted():
