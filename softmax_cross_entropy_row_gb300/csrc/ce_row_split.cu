@@ -85,8 +85,7 @@ __global__ void __launch_bounds__(NT, 1)
         const uint64_t ghi = (ge + 15) & ~15ull;
         hi = ghi < p.hi_clip ? ghi : p.hi_clip;
     };
-    auto issue = [&](long long j) {
-        const int s = (int)(j % nslots);
+    auto issue = [&](long long j, int s) {  // row j of this cluster into slot s
         uint64_t gs, ge, g0, lo, hi;
         if (skips_copy(p, cid + j * ncl, cid + j * ncl + 1)) return;  // test hook
         span(cid + j * ncl, gs, ge, g0, lo, hi);
@@ -110,9 +109,13 @@ __global__ void __launch_bounds__(NT, 1)
     const float gsc = scalar_grad_scale(p);
     __syncthreads();
     long long issued = 0;
+    int s_iss = 0;  // slot of the next copy
     if (tid == 0) {
-        for (; issued < nrows && issued < nslots; ++issued) issue(issued);
+        for (; issued < nrows && issued < nslots; ++issued) issue(issued, (int)issued);
+        s_iss = issued == nslots ? 0 : (int)issued;
     }
+    int s = 0;            // slot and phase parity of the next row
+    uint32_t parity = 0;
 
     bool failed = false;      // this thread saw a copy wait give up
     bool failed_cta = false;  // some thread of the CTA did (uniform)
@@ -121,10 +124,14 @@ __global__ void __launch_bounds__(NT, 1)
 
     for (long long j = 0; j < nrows; ++j) {
         const long long row = cid + j * ncl;
-        const int s = (int)(j % nslots);
         const int par = (int)(j & 1);
-        const uint32_t parity = (uint32_t)((j / nslots) & 1);
         unsigned char *slot = smem + (size_t)s * slot_bytes;
+        uint64_t *slot_full = &full[s];
+        const uint32_t slot_parity = parity;
+        if (++s == nslots) {
+            s = 0;
+            parity ^= 1u;
+        }
         const long long t = t_next;
         if (j + 1 < nrows) t_next = target_at(p, row + ncl);
 
@@ -143,7 +150,7 @@ __global__ void __launch_bounds__(NT, 1)
         const int v_t = has_t ? tl / W : -1;                       // the target's vector
 
         if (!failed) {
-            if (mbar_wait(&full[s], parity, copy_wait_limit(p)))
+            if (mbar_wait(slot_full, slot_parity, copy_wait_limit(p)))
                 consumed = j + 1;
             else
                 failed = true;  // made CTA-wide (and counted) at the next barrier
@@ -227,14 +234,16 @@ __global__ void __launch_bounds__(NT, 1)
                 if (j > 0) {
                     bulk_wait_read_all();
                     fence_proxy_async();
-                    issue(issued);
+                    issue(issued, s_iss);
                     ++issued;
+                    if (++s_iss == nslots) s_iss = 0;
                 }
             } else {
                 // the slot is no longer read: back to the copy engine
                 fence_proxy_async();
-                issue(issued);
+                issue(issued, s_iss);
                 ++issued;
+                if (++s_iss == nslots) s_iss = 0;
             }
         }
         float m = lane < NW ? red_max[par][lane] : -INFINITY;

@@ -31,17 +31,25 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint64_t full[NW * kMaxWarpSlots];
     __shared__ float2 tail_scratch[kTailWarps];
+    __shared__ unsigned int warps_done;  // warps whose last row loss is stored
     __shared__ int tail_flag;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const long long B = p.B;
     const int C = (int)p.C;  // at most 4096 on this path
-    const long long R = rows_per_tile;
-    const long long ntiles = (B + R - 1) / R;
-    const long long gw = (long long)blockIdx.x * NW + warp;
-    const long long TW = (long long)gridDim.x * NW;
-    const long long ntl = ntiles > gw ? (ntiles - gw + TW - 1) / TW : 0;
+    // tiles and warps in 32 bits (B < 2^31, rows_per_tile <= 2048)
+    const unsigned R = (unsigned)rows_per_tile;
+    const unsigned ntiles = ((unsigned)B + R - 1u) / R;
+    const unsigned gw = blockIdx.x * NW + warp;
+    const unsigned TW = gridDim.x * NW;
+    const unsigned ntl = ntiles > gw ? (ntiles - gw + TW - 1u) / TW : 0u;
+    // The batch loss (mean, sum): each warp, once its last row's loss is
+    // stored and before that row's gradient, counts itself done; the CTA's
+    // last warp takes the grid's ticket, so the ticket's release covers the
+    // row losses and not the gradient stores, and the last CTA's sum overlaps
+    // the other CTAs' gradient stores.
+    const bool needs_tail = reduction_of(p) != kReduceNone && !is_softmax(p);
     const uint64_t lbase = reinterpret_cast<uint64_t>(p.logits);
     unsigned char *my_slots = smem + (size_t)warp * slots * slot_bytes;
     uint64_t *my_full = full + warp * kMaxWarpSlots;
@@ -49,10 +57,10 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
     const bool write_grad = writes_grad(p);  // false: loss only
     const unsigned long long kL2E2 = f2_pack(kLog2e, kLog2e);
 
-    auto span = [&](long long tile, long long &r0, long long &r1, uint64_t &gs, uint64_t &ge,
+    auto span = [&](unsigned tile, long long &r0, long long &r1, uint64_t &gs, uint64_t &ge,
                     uint64_t &g0, uint64_t &lo, uint64_t &hi) {
-        r0 = tile * R;
-        r1 = min(r0 + R, B);
+        r0 = (long long)tile * R;
+        r1 = min(r0 + (long long)R, B);
         gs = lbase + (uint64_t)(r0 * C) * ES;
         ge = lbase + (uint64_t)(r1 * C) * ES;
         g0 = gs & ~15ull;
@@ -60,8 +68,7 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
         const uint64_t ghi = (ge + 15) & ~15ull;
         hi = ghi < p.hi_clip ? ghi : p.hi_clip;
     };
-    auto issue = [&](long long i) {
-        const int s = (int)(i % slots);
+    auto issue = [&](unsigned i, int s) {  // tile i of this warp into slot s
         long long r0, r1;
         uint64_t gs, ge, g0, lo, hi;
         span(gw + i * TW, r0, r1, gs, ge, g0, lo, hi);
@@ -76,24 +83,53 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
         }
     };
 
+    // The warp's count toward the batch loss (once per warp, by lane 0; the
+    // row losses it covers were stored by lane 0).
+    auto warp_done = [&]() {
+        if (!needs_tail) return;
+        __syncwarp();
+        if (lane == 0) {
+            unsigned int c;
+            asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                         : "=r"(c)
+                         : "r"(smem_addr(&warps_done))
+                         : "memory");
+            if (c == NW - 1u) {
+                unsigned int prev;
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                             : "=r"(prev)
+                             : "l"(p.ticket)
+                             : "memory");
+                tail_flag = prev == gridDim.x - 1u;
+            }
+        }
+    };
+
     if (lane == 0) {
         for (int s = 0; s < slots; ++s) mbar_init(&my_full[s], 1);
         fence_mbar_init();
     }
+    if (threadIdx.x == 0) {
+        warps_done = 0u;
+        tail_flag = 0;
+    }
     pdl_trigger();
     pdl_wait();  // nothing above touched global memory
     const float gsc = scalar_grad_scale(p);
-    __syncwarp();
-    long long issued = 0;
+    __syncthreads();
+    unsigned issued = 0;
+    int s_iss = 0;  // slot of the next copy
     if (lane == 0) {
-        for (; issued < ntl && issued < slots; ++issued) issue(issued);
+        for (; issued < ntl && issued < (unsigned)slots; ++issued) issue(issued, (int)issued);
+        s_iss = (int)issued == slots ? 0 : (int)issued;
     }
+    if (ntl == 0) warp_done();
 
-    long long failed_at = ntl;  // the first tile whose copy wait gave up (ntl: none)
+    unsigned failed_at = ntl;  // the first tile whose copy wait gave up (ntl: none)
+    int s = 0;                 // slot and phase parity of the next tile
+    uint32_t parity = 0;
 
-    for (long long i = 0; i < ntl; ++i) {
-        const int s = (int)(i % slots);
-        const uint32_t parity = (uint32_t)((i / slots) & 1);
+    for (unsigned i = 0; i < ntl; ++i) {
         unsigned char *slot = my_slots + (size_t)s * slot_bytes;
         long long r0, r1;
         uint64_t gs, ge, g0, lo, hi;
@@ -106,6 +142,10 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
             failed_at = i;
             if (lane == 0) atomicAdd(&p.err[kErrTimeout], 1);
             break;
+        }
+        if (++s == slots) {
+            s = 0;
+            parity ^= 1u;
         }
 
         // Elements of an unaligned tensor's first/last 16 bytes: plain loads.
@@ -222,27 +262,53 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
             const float scale = fast_rcp(S) * row_grad_factor(p, gsc, r);
             const unsigned long long sc2 = f2_pack(scale, scale);
             const float g_t = -s_rest * scale;
+
+            // Step 3: loss of the row, log(S / e_t) -- before the gradient, so
+            // that the warp's last row can count it done first
+            if (lane == 0 && !is_softmax(p)) {
+                float l;
+                if (has_t) {
+                    l = row_loss(s_rest, e_t, S, zt, M);
+                } else {
+                    l = NAN;
+                    atomicAdd(&p.err[kErrBadTarget], 1);
+                }
+                p.loss_rows[r] = l;
+            }
+            if (i + 1 == ntl && r + 1 == r1) warp_done();
+
             if (write_grad) {
                 unsigned char *grow = p.grad + (size_t)r * C * ES;
                 unsigned char *gvec = grow + nh * ES;
+                auto grad2 = [&](const uint4 &xv, unsigned long long (&g2)[W2]) {
+                    E::unpack2(xv, g2);
 #pragma unroll
-                for (int k = 0; k < MAXV; ++k) {
-                    const int v = lane + 32 * k;
-                    if (v < nvec) {
-                        unsigned long long g2[W2];
-                        E::unpack2(x[k], g2);
-#pragma unroll
-                        for (int j = 0; j < W2; ++j) {
-                            if (!kKeepExp) {
-                                float a, b;
-                                f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
-                                g2[j] = f2_pack(ex2(a), ex2(b));
-                            }
-                            g2[j] = f2_mul(g2[j], sc2);
+                    for (int j = 0; j < W2; ++j) {
+                        if (!kKeepExp) {
+                            float a, b;
+                            f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
+                            g2[j] = f2_pack(ex2(a), ex2(b));
                         }
-                        if (vec_store) {
+                        g2[j] = f2_mul(g2[j], sc2);
+                    }
+                };
+                if (vec_store) {
+#pragma unroll
+                    for (int k = 0; k < MAXV; ++k) {
+                        const int v = lane + 32 * k;
+                        if (v < nvec) {
+                            unsigned long long g2[W2];
+                            grad2(x[k], g2);
                             *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack2(g2);
-                        } else {
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < MAXV; ++k) {
+                        const int v = lane + 32 * k;
+                        if (v < nvec) {
+                            unsigned long long g2[W2];
+                            grad2(x[k], g2);
 #pragma unroll
                             for (int j = 0; j < W2; ++j) {
                                 float a, b;
@@ -251,10 +317,11 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
                                 E::store(gvec + (v * W + 2 * j + 1) * ES, b);
                             }
                         }
-                        // the owner of the target's vector overwrites the target
-                        if (v == v_t) E::store(grow + (size_t)t * ES, g_t);
                     }
                 }
+                // the owner of the target's vector overwrites the target,
+                // after its vector's store
+                if (v_t >= 0 && lane == (v_t & 31)) E::store(grow + (size_t)t * ES, g_t);
                 // test hook: the whole vectors' fp32 values, before their
                 // rounding (recomputed so that the loop above carries none of it)
                 if (grad_f32_of(p)) {
@@ -295,23 +362,13 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
                 }
             }
 
-            // Step 3: loss of the row, log(S / e_t)
-            if (lane == 0 && !is_softmax(p)) {
-                float l;
-                if (has_t) {
-                    l = row_loss(s_rest, e_t, S, zt, M);
-                } else {
-                    l = NAN;
-                    atomicAdd(&p.err[kErrBadTarget], 1);
-                }
-                p.loss_rows[r] = l;
-            }
         }
         __syncwarp();
         if (lane == 0 && issued < ntl) {
             fence_proxy_async();
-            issue(issued);
+            issue(issued, s_iss);
             ++issued;
+            if (++s_iss == slots) s_iss = 0;
         }
     }
 
@@ -319,28 +376,33 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
         // The tiles from the one whose wait gave up on were not computed:
         // their rows' losses are NaN, so the batch loss shows the failure
         // (their gradient is not written).
-        for (long long i = failed_at; i < ntl; ++i) {
+        for (unsigned i = failed_at; i < ntl; ++i) {
             long long r0, r1;
             uint64_t gs, ge, g0, lo, hi;
             span(gw + i * TW, r0, r1, gs, ge, g0, lo, hi);
             if (!is_softmax(p))
                 for (long long r = r0 + lane; r < r1; r += 32) p.loss_rows[r] = NAN;
         }
+        warp_done();  // (lane 0 stored NaN rows too; the others before the warp's sync)
         // The warp still owns copies in flight: it waits for them (each for
         // up to the full limit) before the CTA's shared memory is released.
         // A copy that has not landed after that never will; the warp then
         // leaves rather than hang.
         if (lane == 0) {
-            for (long long i = failed_at; i < issued; ++i) {
+            for (unsigned i = failed_at; i < issued; ++i) {
                 long long r0, r1;
                 uint64_t gs, ge, g0, lo, hi;
                 span(gw + i * TW, r0, r1, gs, ge, g0, lo, hi);
                 if (skips_copy(p, r0, r1)) continue;  // never issued
-                if (!mbar_wait(&my_full[i % slots], (uint32_t)((i / slots) & 1))) break;
+                if (!mbar_wait(&my_full[i % slots], (i / slots) & 1u)) break;
             }
         }
     }
-    finish_cta(p, &tail_flag, tail_scratch);
+    // the batch loss, in the CTA that took the grid's last ticket
+    if (needs_tail) {
+        __syncthreads();
+        if (tail_flag) batch_tail(p, tail_scratch);
+    }
 }
 
 template <typename T, int MAXV, int MINB, typename P>
