@@ -201,7 +201,7 @@ int ce_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int 
  * before reading it); grad_out: device [B][C] in `dtype`, as for ce_fwd_bwd
  * (the gradient stays on the device for the backward pass).  The batch goes
  * through in chunks of rows (a multiple of 16 rows, at most 64 MiB of
- * logits each): a chunk's copy in runs on a library stream while the kernel
+ * logits each, about a quarter of a smaller batch): a chunk's copy in runs on a library stream while the kernel
  * of the chunk before runs on `stream`, and the call's work all lies between
  * its start and its end on `stream`.  The gradient has the bits of ce_fwd_bwd
  * whenever grad_out is 16-byte aligned.  The library keeps per-stream staging

@@ -794,6 +794,7 @@ int run_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int
 // directions one after the other (31-33 ms); 32 MiB chunks leave the host
 // issuing more calls than the copies take.
 constexpr size_t kHostChunkBytes = 64u << 20;
+constexpr size_t kHostChunkMin = 4u << 20;
 
 // Tuning knob: CE_HOST_CHUNK_MB sets the chunk's logits bytes (MiB).  Read once.
 size_t host_chunk_bytes() {
@@ -885,10 +886,13 @@ int run_host(const void *logits_host, const int32_t *targets_host, int64_t B, in
     if ((e = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return cuda_fail(e);
     if (cs != cudaStreamCaptureStatusNone) return CE_ERR_CAPTURE;
 
-    // chunks: a multiple of 16 rows, at most kHostChunkBytes of logits (at
-    // least 16 rows)
+    // chunks: a multiple of 16 rows, at most kHostChunkBytes of logits and
+    // (so that a small batch's copies overlap too) about a quarter of the
+    // batch when that is at least kHostChunkMin; at least 16 rows
     const size_t row_bytes = (size_t)C * es;
-    long long chunk_rows = (long long)(host_chunk_bytes() / row_bytes) / 16 * 16;
+    size_t want = nbytes / 4 > kHostChunkMin ? nbytes / 4 : kHostChunkMin;
+    if (want > host_chunk_bytes()) want = host_chunk_bytes();
+    long long chunk_rows = (long long)(want / row_bytes) / 16 * 16;
     if (chunk_rows < 16) chunk_rows = 16;
     if (chunk_rows > B) chunk_rows = B;
     Plan pl;
