@@ -406,13 +406,16 @@ def bench_e2e(w, inp, device, steps, world=1):
         s.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        for _ in range(steps):
+        # an event after every step as well: the per-step spread (the copies
+        # share the host's memory with whatever else runs on the machine)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        marks[0].record(s)
+        for k in range(steps):
             step()
-        e1.record(s)
-        e1.synchronize()
-    per_step = max_over_ranks(e0.elapsed_time(e1) / 1e3, device) / steps
+            marks[k + 1].record(s)
+        marks[-1].synchronize()
+    per_step = max_over_ranks(marks[0].elapsed_time(marks[-1]) / 1e3, device) / steps
+    each = [a.elapsed_time(b) for a, b in zip(marks[:-1], marks[1:])]
     h2d = hz.numel() * hz.element_size() + ht.numel() * ht.element_size()
     d2h = hg.numel() * hg.element_size() + hl.numel() * hl.element_size()
     del hg
@@ -420,6 +423,7 @@ def bench_e2e(w, inp, device, steps, world=1):
     return {"value": replica_rows_per_s(w.B, world, per_step), "unit": "rows/s",
             "h2d_bytes_per_step": int(world * h2d), "d2h_bytes_per_step": int(world * d2h),
             "steps": steps, "ms_per_step": per_step * 1e3,
+            "ms_per_step_median": statistics.median(each), "ms_per_step_max": max(each),
             "call": "ce_fwd_bwd_host_grad (pinned host logits, targets, loss and gradient)"}
 
 
@@ -650,7 +654,9 @@ def main():
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": ({k: head["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step",
-                                             "d2h_bytes_per_step")} if "e2e" in head else None),
+                                             "d2h_bytes_per_step", "ms_per_step",
+                                             "ms_per_step_median", "ms_per_step_max")}
+                if "e2e" in head else None),
         "gpu_launches": world * head["steps"] * head["launches_per_step"],
         "ms_per_step_parts": head["ms_per_step_parts"],
         "clocks": head["clocks"],
