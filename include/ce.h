@@ -196,7 +196,8 @@ int ce_softmax_bwd(const void *probs, const void *dy, int64_t B, int64_t C, int 
  * same L (the same bits) and gradient, with the copies to the device made by
  * the library.  logits_host [B][C] in `dtype` and targets_host [B] int32:
  * host memory (page-locked for asynchronous copies; pageable memory works,
- * with copies the host waits for); loss_host: one fp32 in host memory,
+ * with copies the host waits for), left unchanged until `stream` reaches the
+ * end of the call; loss_host: one fp32 in host memory,
  * written when `stream` reaches the end of the call (synchronise the stream
  * before reading it); grad_out: device [B][C] in `dtype`, as for ce_fwd_bwd
  * (the gradient stays on the device for the backward pass).  The batch goes

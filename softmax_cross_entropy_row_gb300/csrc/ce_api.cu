@@ -821,31 +821,33 @@ int host_pipe(int dev, cudaStream_t s, size_t chunk_bytes, bool grad_host, size_
             if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess)
                 return cuda_fail(e);
     }
-    // outgrown buffers may still be read by queued work: retired, not freed
-    auto grow = [&](unsigned char **b, size_t have, size_t need, size_t quantum) -> int {
-        if (have >= need && *b) return CE_OK;
+    // A new buffer for *b; the outgrown one may still be read by queued work,
+    // so it is retired, not freed.
+    auto replace = [&](unsigned char **b, size_t bytes) -> int {
         if (*b) g_ws_retired.push_back({dev, *b});
         *b = nullptr;
         void *p = nullptr;
-        cudaError_t err = cudaMalloc(&p, align_up(need, quantum));
+        cudaError_t err = cudaMalloc(&p, bytes);
         if (err != cudaSuccess) return cuda_fail(err);
         *b = static_cast<unsigned char *>(p);
         return CE_OK;
     };
     int rc;
     if (h.chunk_bytes < chunk_bytes) {
+        const size_t bytes = align_up(chunk_bytes, 1 << 20);
         for (int b = 0; b < 2; ++b)
-            if ((rc = grow(&h.z[b], 0, chunk_bytes, 1 << 20)) != CE_OK) return rc;
-        h.chunk_bytes = align_up(chunk_bytes, 1 << 20);
+            if ((rc = replace(&h.z[b], bytes)) != CE_OK) return rc;
+        h.chunk_bytes = bytes;
     }
     if (grad_host && h.g_bytes < h.chunk_bytes) {
         for (int b = 0; b < 2; ++b)
-            if ((rc = grow(&h.g[b], 0, h.chunk_bytes, 1 << 20)) != CE_OK) return rc;
+            if ((rc = replace(&h.g[b], h.chunk_bytes)) != CE_OK) return rc;
         h.g_bytes = h.chunk_bytes;
     }
     if (h.tbytes < tbytes) {
-        if ((rc = grow(&h.t, 0, tbytes, 1 << 16)) != CE_OK) return rc;
-        h.tbytes = align_up(tbytes, 1 << 16);
+        const size_t bytes = align_up(tbytes, 1 << 16);
+        if ((rc = replace(&h.t, bytes)) != CE_OK) return rc;
+        h.tbytes = bytes;
     }
     *out = &h;  // map nodes are stable; entries are erased only by ce_release_workspaces
     return CE_OK;
