@@ -293,7 +293,19 @@ __global__ void __launch_bounds__(NT, 1)
         float S;
         if (K == 1) {
             if (lane == 0) red_sum[par][warp] = ssum;
-            __syncthreads();
+            if (!write_grad && !is_softmax(p)) {
+                // the loss alone: only warp 0 (the loss's writer) needs the
+                // row's sum, so the other warps arrive without waiting and go
+                // on to the next row (whose first barrier warp 0 reaches only
+                // once this row's loss is written)
+                if (warp != 0) {
+                    named_arrive(1, NT);
+                    continue;
+                }
+                named_sync(1, NT);
+            } else {
+                __syncthreads();
+            }
             S = lane < NW ? red_sum[par][lane] : 0.f;
             S = warp_sum(S);
         } else {
