@@ -33,9 +33,16 @@ namespace {
 
 constexpr int kVecThreads = 512;
 constexpr int kVecPerThread = 8;  // 64 KB rows of each tensor at most
+constexpr size_t kPrefetchPiece = 16384;  // bytes per L2 prefetch request (4 cover a row)
 constexpr int kAnyThreads = 512;
 constexpr int kWarpCtaThreads = 256;
 constexpr int kWarpMaxVpl = 8;  // 4 KB rows of each tensor at most
+
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) from global
+// memory into L2; nothing is written to shared memory and nothing waits.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 
 template <int NT>
 __device__ __forceinline__ float block_sum_fixed(float v, float *red) {
@@ -61,20 +68,41 @@ __global__ void __launch_bounds__(kVecThreads, 1)
     pdl_wait();
     const int tid = threadIdx.x;
     const long long nvec = C / W;  // whole vectors per row (C * es is a multiple of 16)
-    for (long long b = blockIdx.x; b < B; b += gridDim.x) {
-        const uint4 *prow = reinterpret_cast<const uint4 *>(P + (size_t)b * C * E::kBytes);
-        const uint4 *drow = reinterpret_cast<const uint4 *>(DY + (size_t)b * C * E::kBytes);
-        uint4 *xrow = reinterpret_cast<uint4 *>(DX + (size_t)b * C * E::kBytes);
-        uint4 pv[kVecPerThread], dv[kVecPerThread];
+    const size_t row_bytes = (size_t)C * E::kBytes;
+    // The CTA's rows are b, b + grid, ...; the next row's reads overlap the
+    // current row.  fp32: a thread's vectors of the next row are loaded into
+    // its registers as soon as it has written the same vectors of the current
+    // row.  16-bit (whose unpacked pairs leave no registers for that): the
+    // next row of p and dy is prefetched into L2 by one bulk request each when
+    // the current row starts, so its loads are served by L2.
+    constexpr bool kRegPipe = sizeof(T) == 4;
+    uint4 pv[kVecPerThread], dv[kVecPerThread];
+    auto load_vec = [&](long long b, int k) {
+        const long long v = tid + (long long)k * kVecThreads;
+        pv[k] = make_uint4(0u, 0u, 0u, 0u);
+        dv[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (b < B && v < nvec) {
+            pv[k] = __ldcs(reinterpret_cast<const uint4 *>(P + (size_t)b * row_bytes) + v);
+            dv[k] = __ldcs(reinterpret_cast<const uint4 *>(DY + (size_t)b * row_bytes) + v);
+        }
+    };
+    if (kRegPipe) {
 #pragma unroll
-        for (int k = 0; k < kVecPerThread; ++k) {
-            const long long v = tid + (long long)k * kVecThreads;
-            pv[k] = make_uint4(0u, 0u, 0u, 0u);
-            dv[k] = make_uint4(0u, 0u, 0u, 0u);
-            if (v < nvec) {
-                pv[k] = __ldcs(prow + v);  // read once: streaming
-                dv[k] = __ldcs(drow + v);
+        for (int k = 0; k < kVecPerThread; ++k) load_vec(blockIdx.x, k);
+    }
+    for (long long b = blockIdx.x; b < B; b += gridDim.x) {
+        uint4 *xrow = reinterpret_cast<uint4 *>(DX + (size_t)b * row_bytes);
+        if (!kRegPipe) {
+            // 16 KB pieces of the next row of p (threads 0-3) and dy (4-7)
+            const long long bn = b + gridDim.x;
+            const size_t off = (size_t)(tid & 3) * kPrefetchPiece;
+            if (tid < 8 && bn < B && off < row_bytes) {
+                const unsigned char *src = (tid < 4 ? P : DY) + (size_t)bn * row_bytes + off;
+                const size_t left = row_bytes - off;
+                bulk_prefetch_l2(src, (uint32_t)(left < kPrefetchPiece ? left : kPrefetchPiece));
             }
+#pragma unroll
+            for (int k = 0; k < kVecPerThread; ++k) load_vec(b, k);
         }
         unsigned long long acc = 0ull;
 #pragma unroll
@@ -100,6 +128,7 @@ __global__ void __launch_bounds__(kVecThreads, 1)
                 for (int i = 0; i < W2; ++i) p2[i] = f2_mul(p2[i], f2_add(d2[i], nd2));
                 __stcs(xrow + v, E::pack2(p2));
             }
+            if (kRegPipe) load_vec(b + gridDim.x, k);
         }
     }
 }
