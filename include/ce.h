@@ -60,7 +60,10 @@ typedef enum {
 /* Kernel paths (for ce_fwd_bwd_path and ce_query_plan). */
 typedef enum {
     CE_PATH_AUTO = 0,      /* let the library choose                                */
-    CE_PATH_ROWS_WARP = 1, /* small rows: one warp per row, rows staged by TMA       */
+    CE_PATH_ROWS_WARP = 1, /* one warp per row, rows staged by TMA: rows of up to
+                              8 KB held in registers, rows of up to 48 KB swept in
+                              shared memory (CE_PATH_AUTO takes the swept form
+                              where 8 warps per SM fit, up to ~27 KB)             */
     CE_PATH_ROW_SPLIT = 2, /* rows (or row slices across a cluster of `split` CTAs)
                               staged once in shared memory by TMA                    */
     CE_PATH_STREAM = 3,    /* any row: chunk partials, then a recompute-and-write

@@ -106,6 +106,7 @@ struct Plan {
     long long slice = 0;  // classes per slice (split path)
     int rows_per_tile = 0;
     int per_sm = 1;       // warp path: the build for 1, 2 or 3 resident CTAs per SM
+    int swept_nw = 0;     // warp path, rows swept in shared memory: warps per CTA (else 0)
     int vecs = 8;         // split path: 16-byte vectors per thread (8, 12 or 16)
     bool pipe = false;    // split path: the pipelined kernel (slices of at most 8 vectors)
     long long chunks = 0; // stream path
@@ -210,6 +211,84 @@ int plan_warp(long long B, long long C, int es, const DeviceInfo &d, int dtype, 
     pl->slot_bytes = slot_bytes;
     pl->rows_per_tile = (int)R;
     pl->per_sm = want;
+    return CE_OK;
+}
+
+// Tuning knobs: CE_SWEPT_WARPS=16, 8 or 4 and CE_SWEPT_SLOTS=1..4 force the
+// swept warp path's warps per CTA and slots per warp (0 or unset: chosen
+// from the row's bytes).  Read once.
+int env_int_once(const char *name, int *cache) {
+    if (*cache < 0) {
+        const char *e = getenv(name);
+        *cache = e ? atoi(e) : 0;
+    }
+    return *cache;
+}
+int swept_warps_override() {
+    static int v = -1;
+    return env_int_once("CE_SWEPT_WARPS", &v);
+}
+int swept_slots_override() {
+    static int v = -1;
+    return env_int_once("CE_SWEPT_SLOTS", &v);
+}
+
+// Warp path for rows longer than a warp's registers hold (8 KB .. 48 KB):
+// one row per tile, swept in its slot.  What the time depends on is the
+// warps resident per SM (each sweeps its row with little parallelism of its
+// own): measured on GB300 (16384 rows), one slot per warp and the most
+// resident warps won -- 12 KB rows 0.77-0.78 of peak with 16 warps per SM,
+// 16 KB bf16 rows 0.81 with three 4-warp CTAs per SM against 0.49 with one
+// CTA of four warps and three slots each, 24 KB rows 0.76-0.88 with 8 warps
+// -- and with 4 warps per SM (31 KB rows) the two-pass kernel is faster.  So
+// the build (16, 8 or 4 warps per CTA) with the most resident warps per SM
+// is taken, one slot per warp (ties: the larger CTA); the planner's own
+// choice requires 8 resident warps per SM, a forced warp path takes
+// whatever fits.
+int plan_warp_swept(long long B, long long C, int es, const DeviceInfo &d, int dtype, bool forced,
+                    Plan *pl) {
+    const long long row_bytes = C * es;
+    if (row_bytes > ce::kWarpChunkRowMax) return CE_ERR_PATH;
+    const int budget = d.smem_optin - kStaticSmemReserve;
+    const int slot_bytes = round_up(row_bytes + 32, 128);
+    auto resident = [&](int nw, int slots, int *per_sm) {
+        const int smem = slots * slot_bytes * nw;
+        return cached_occupancy(
+            dtype, CE_PATH_ROWS_WARP, -nw - 100 * slots, smem,
+            [&](int *v) { return ce::rows_warp_swept_max_ctas_per_sm(dtype, nw, smem, v); },
+            per_sm);
+    };
+    int nw = 0, slots = 1, per_sm = 0;
+    const int fw = swept_warps_override(), fs = swept_slots_override();
+    for (int w : {16, 8, 4}) {
+        if (fw && w != fw) continue;
+        const int sl = fs >= 1 && fs <= ce::kMaxWarpSlots ? fs : 1;
+        if ((long long)sl * w * slot_bytes > budget) continue;
+        int n = 0;
+        const int rc = resident(w, sl, &n);
+        if (rc != CE_OK) return rc;
+        if (n >= 1 && w * n > nw * per_sm) {
+            nw = w;
+            slots = sl;
+            per_sm = n;
+        }
+    }
+    if (nw == 0) return CE_ERR_PATH;
+    if (!forced && nw * per_sm < 8) return CE_ERR_PATH;
+    long long ctas = (B + nw - 1) / nw;
+    const long long cap = (long long)d.sms * per_sm;
+    if (ctas > cap) ctas = cap;
+    pl->path = CE_PATH_ROWS_WARP;
+    pl->split = 1;
+    pl->ctas = (int)ctas;
+    pl->threads = nw * 32;
+    pl->smem = slots * slot_bytes * nw;
+    pl->launches = 1;
+    pl->nslots = slots;
+    pl->slot_bytes = slot_bytes;
+    pl->rows_per_tile = 1;
+    pl->per_sm = 1;
+    pl->swept_nw = nw;
     return CE_OK;
 }
 
@@ -355,6 +434,9 @@ cudaError_t launch_split_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, 
 cudaError_t launch_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, cudaStream_t s) {
     switch (pl.path) {
         case CE_PATH_ROWS_WARP:
+            if (pl.swept_nw)
+                return ce::launch_rows_warp_swept(p, dtype, pl.swept_nw, pl.ctas, pl.nslots,
+                                                  pl.slot_bytes, pl.smem, s);
             return ce::launch_rows_warp(p, dtype, pl.per_sm, pl.ctas, pl.nslots, pl.rows_per_tile,
                                         pl.slot_bytes, pl.smem, s);
         case CE_PATH_ROW_SPLIT:
@@ -377,16 +459,22 @@ int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl
     const long long row_bytes = C * es;
     switch (path) {
         case CE_PATH_AUTO:
-            // rows of at most 8 KB: a warp each; rows one CTA holds in
-            // registers: the split kernel at K = 1; longer rows: two passes
-            // through one CTA (measured faster on GB300 than splitting a row
-            // across a cluster or the streaming path)
+            // rows of at most 8 KB: a warp each, held in registers; rows for
+            // which 8 warps per SM fit: a warp each, swept in shared memory;
+            // rows one CTA holds in registers: the split kernel at K = 1;
+            // longer rows: two passes through one CTA (measured faster on
+            // GB300 than splitting a row across a cluster or the streaming
+            // path)
             if (row_bytes <= kWarpRowMax) return plan_warp(B, C, es, d, dtype, pl);
+            rc = plan_warp_swept(B, C, es, d, dtype, false, pl);
+            if (rc != CE_ERR_PATH) return rc;
             rc = plan_split(B, C, es, d, dtype, 0, pl);
             if (rc == CE_OK && pl->split == 1) return rc;
             if (rc != CE_OK && rc != CE_ERR_PATH) return rc;
             return plan_twopass(B, d, dtype, pl);
-        case CE_PATH_ROWS_WARP: return plan_warp(B, C, es, d, dtype, pl);
+        case CE_PATH_ROWS_WARP:
+            if (row_bytes <= kWarpRowMax) return plan_warp(B, C, es, d, dtype, pl);
+            return plan_warp_swept(B, C, es, d, dtype, true, pl);
         case CE_PATH_ROW_SPLIT: return plan_split(B, C, es, d, dtype, split, pl);
         case CE_PATH_STREAM:
             if (split != 0 && split != ce::kStreamChunk) return CE_ERR_PATH;

@@ -56,6 +56,15 @@ cudaError_t split_pipe_max_clusters(int dtype, int K, int smem, int *clusters);
 cudaError_t launch_rows_warp(const ParamsEx &p, int dtype, int per_sm, int ctas, int slots,
                              int rows_per_tile, int slot_bytes, int smem, cudaStream_t s);
 cudaError_t rows_warp_max_ctas_per_sm(int dtype, int per_sm, long long C, int smem, int *ctas);
+// The same kernel for rows longer than a warp's registers hold: each row is
+// swept in its shared-memory slot (max, sum, gradient) kWarpChunkVecs vectors
+// per lane at a time; nw (16, 8 or 4) warps per CTA, one CTA per SM, one row
+// per tile.
+constexpr int kWarpChunkVecs = 8;
+constexpr long long kWarpChunkRowMax = 49152;  // bytes
+cudaError_t launch_rows_warp_swept(const ParamsEx &p, int dtype, int nw, int ctas, int slots,
+                                   int slot_bytes, int smem, cudaStream_t s);
+cudaError_t rows_warp_swept_max_ctas_per_sm(int dtype, int nw, int smem, int *ctas);
 
 // Two-pass row path (ce_row_twopass.cu): one CTA per SM, a row at a time,
 // rows of any length streamed twice through a ring of `nslots` chunks of

@@ -1,4 +1,5 @@
-// Warp-per-row kernel for rows of at most 8 KB (classifier heads).
+// Warp-per-row kernel for rows of at most 8 KB (classifier heads), and, swept
+// in shared memory instead of held in registers, rows of up to 48 KB.
 //
 // Each warp owns a private ring of `slots` shared-memory tiles; a tile is
 // `rows_per_tile` consecutive rows of the logits, staged by one TMA bulk copy.
@@ -18,11 +19,14 @@
 namespace ce {
 namespace {
 
-template <typename T, int MAXV, int MINB, typename P>
-__global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
+// MAXV > 0: the row in registers (at most MAXV vectors per lane).  MAXV = 0:
+// the row swept in its slot, kWarpChunkVecs vectors per lane at a time (rows
+// longer than a warp's registers hold; NWK warps, one CTA per SM).
+template <typename T, int MAXV, int MINB, typename P, int NWK = warp_kernel_warps(MINB)>
+__global__ void __launch_bounds__(NWK * 32, MINB)
     rows_warp_kernel(P p, int slots, int rows_per_tile, int slot_bytes) {
     using E = Elem<T>;
-    constexpr int NW = warp_kernel_warps(MINB);
+    constexpr int NW = NWK;
     constexpr int ES = E::kBytes;
     constexpr int W = E::kVec;
     constexpr int W2 = W / 2;
@@ -37,7 +41,7 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const long long B = p.B;
-    const int C = (int)p.C;  // at most 4096 on this path
+    const int C = (int)p.C;  // rows of at most kWarpChunkRowMax bytes on this path
     // tiles and warps in 32 bits (B < 2^31, rows_per_tile <= 2048)
     const unsigned R = (unsigned)rows_per_tile;
     const unsigned ntiles = ((unsigned)B + R - 1u) / R;
@@ -185,183 +189,346 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
             const int tv = has_t ? t - nh : -0x40000000;  // target relative to vector 0
             const int v_t = has_t && tv >= 0 && tv < nvec * W ? tv / W : -1;  // its vector
 
-            const uint4 kNeg = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord,
-                                          E::kNegInfWord);
-            uint4 x[MAXV];
+            if constexpr (MAXV > 0) {
+                const uint4 kNeg = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord,
+                                              E::kNegInfWord);
+                uint4 x[MAXV];
 #pragma unroll
-            for (int k = 0; k < MAXV; ++k) {
-                const int v = lane + 32 * k;
-                x[k] = kNeg;
-                if (v < nvec) x[k] = lds128(vrow + 16 * v);
-            }
-            // head and tail elements exist only for rows that do not start and
-            // end on a 16-byte boundary (the same in every lane)
-            const bool ragged = (nh | nt) != 0;
-            float hz = -INFINITY, tz = -INFINITY;
-            if (ragged) {
-                if (lane < nh) hz = E::load(row + lane * ES);
-                if (lane < nt) tz = E::load(vrow + (nvec * W + lane) * ES);
-            }
-            const float zt = has_t ? E::load(row + t * ES) : 0.f;
-            // lane 0 also takes the target's vector
-            const uint4 xt = lane == 0 && v_t >= 0 ? lds128(vrow + 16 * v_t) : kNeg;
-
-            // Step 1: max
-            float m = fmaxf(hz, tz);
-            typename E::MaxAcc macc = E::max_init();
-#pragma unroll
-            for (int k = 0; k < MAXV; ++k) E::max_step(macc, x[k]);
-            m = fmaxf(m, E::max_value(macc));
-            m = warp_max(m);
-            const float M = m * kLog2e;
-            const unsigned long long nM2 = f2_pack(-M, -M);
-
-            // Step 2: sum of exponentials without the target's term.  The
-            // target's vector is left out whole; lane 0 adds its other elements.
-            unsigned long long acc = 0ull;
-#pragma unroll
-            for (int k = 0; k < MAXV; ++k) {
-                const int v = lane + 32 * k;
-                unsigned long long e2[W2];
-                E::unpack2(x[k], e2);
-#pragma unroll
-                for (int j = 0; j < W2; ++j) {
-                    float a, b;
-                    f2_unpack(f2_fma(e2[j], kL2E2, nM2), a, b);
-                    e2[j] = f2_pack(ex2(a), ex2(b));
+                for (int k = 0; k < MAXV; ++k) {
+                    const int v = lane + 32 * k;
+                    x[k] = kNeg;
+                    if (v < nvec) x[k] = lds128(vrow + 16 * v);
                 }
-                if (kKeepExp) x[k] = E::pack2(e2);
-                unsigned long long vs = W2 == 4 ? f2_add(f2_add(e2[0], e2[1]),
-                                                         f2_add(e2[W2 - 2], e2[W2 - 1]))
-                                                : f2_add(e2[0], e2[W2 - 1]);
-                if (v != v_t) acc = f2_add(acc, vs);
-            }
-            float sa, sb;
-            f2_unpack(acc, sa, sb);
-            if (lane == 0 && v_t >= 0) {
-                float z[W];
-                E::unpack(xt, z);
-                const int d = tv - v_t * W;
-#pragma unroll
-                for (int j = 0; j < W; ++j)
-                    if (j != d) sa += ex2(fmaf(z[j], kLog2e, -M));
-            }
-            float eh = 0.f, et = 0.f;
-            if (ragged) {
-                if (lane < nh) eh = ex2(fmaf(hz, kLog2e, -M));
-                if (lane < nt) et = ex2(fmaf(tz, kLog2e, -M));
-                if (lane != t) sa += eh;
-                if (nh + nvec * W + lane != t) sb += et;
-            }
-            const float s_rest = warp_sum(sa + sb);
-            const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
-            const float S = s_rest + e_t;
-
-            // Step 4: gradient; (p_t - 1) / B = -S_rest / (S B), times the
-            // upstream gradient (1/B becomes 1 for the sum and per-row losses)
-            const float scale = fast_rcp(S) * row_grad_factor(p, gsc, r);
-            const unsigned long long sc2 = f2_pack(scale, scale);
-            const float g_t = -s_rest * scale;
-
-            // Step 3: loss of the row, log(S / e_t) -- before the gradient, so
-            // that the warp's last row can count it done first
-            if (lane == 0 && !is_softmax(p)) {
-                float l;
-                if (has_t) {
-                    l = row_loss(s_rest, e_t, S, zt, M);
-                } else {
-                    l = NAN;
-                    atomicAdd(&p.err[kErrBadTarget], 1);
+                // head and tail elements exist only for rows that do not start and
+                // end on a 16-byte boundary (the same in every lane)
+                const bool ragged = (nh | nt) != 0;
+                float hz = -INFINITY, tz = -INFINITY;
+                if (ragged) {
+                    if (lane < nh) hz = E::load(row + lane * ES);
+                    if (lane < nt) tz = E::load(vrow + (nvec * W + lane) * ES);
                 }
-                p.loss_rows[r] = l;
-            }
-            if (i + 1 == ntl && r + 1 == r1) warp_done();
+                const float zt = has_t ? E::load(row + t * ES) : 0.f;
+                // lane 0 also takes the target's vector
+                const uint4 xt = lane == 0 && v_t >= 0 ? lds128(vrow + 16 * v_t) : kNeg;
 
-            if (write_grad) {
-                unsigned char *grow = p.grad + (size_t)r * C * ES;
-                unsigned char *gvec = grow + nh * ES;
-                auto grad2 = [&](const uint4 &xv, unsigned long long (&g2)[W2]) {
-                    E::unpack2(xv, g2);
+                // Step 1: max
+                float m = fmaxf(hz, tz);
+                typename E::MaxAcc macc = E::max_init();
+#pragma unroll
+                for (int k = 0; k < MAXV; ++k) E::max_step(macc, x[k]);
+                m = fmaxf(m, E::max_value(macc));
+                m = warp_max(m);
+                const float M = m * kLog2e;
+                const unsigned long long nM2 = f2_pack(-M, -M);
+
+                // Step 2: sum of exponentials without the target's term.  The
+                // target's vector is left out whole; lane 0 adds its other elements.
+                unsigned long long acc = 0ull;
+#pragma unroll
+                for (int k = 0; k < MAXV; ++k) {
+                    const int v = lane + 32 * k;
+                    unsigned long long e2[W2];
+                    E::unpack2(x[k], e2);
 #pragma unroll
                     for (int j = 0; j < W2; ++j) {
-                        if (!kKeepExp) {
-                            float a, b;
-                            f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
-                            g2[j] = f2_pack(ex2(a), ex2(b));
+                        float a, b;
+                        f2_unpack(f2_fma(e2[j], kL2E2, nM2), a, b);
+                        e2[j] = f2_pack(ex2(a), ex2(b));
+                    }
+                    if (kKeepExp) x[k] = E::pack2(e2);
+                    unsigned long long vs = W2 == 4 ? f2_add(f2_add(e2[0], e2[1]),
+                                                             f2_add(e2[W2 - 2], e2[W2 - 1]))
+                                                    : f2_add(e2[0], e2[W2 - 1]);
+                    if (v != v_t) acc = f2_add(acc, vs);
+                }
+                float sa, sb;
+                f2_unpack(acc, sa, sb);
+                if (lane == 0 && v_t >= 0) {
+                    float z[W];
+                    E::unpack(xt, z);
+                    const int d = tv - v_t * W;
+#pragma unroll
+                    for (int j = 0; j < W; ++j)
+                        if (j != d) sa += ex2(fmaf(z[j], kLog2e, -M));
+                }
+                float eh = 0.f, et = 0.f;
+                if (ragged) {
+                    if (lane < nh) eh = ex2(fmaf(hz, kLog2e, -M));
+                    if (lane < nt) et = ex2(fmaf(tz, kLog2e, -M));
+                    if (lane != t) sa += eh;
+                    if (nh + nvec * W + lane != t) sb += et;
+                }
+                const float s_rest = warp_sum(sa + sb);
+                const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
+                const float S = s_rest + e_t;
+
+                // Step 4: gradient; (p_t - 1) / B = -S_rest / (S B), times the
+                // upstream gradient (1/B becomes 1 for the sum and per-row losses)
+                const float scale = fast_rcp(S) * row_grad_factor(p, gsc, r);
+                const unsigned long long sc2 = f2_pack(scale, scale);
+                const float g_t = -s_rest * scale;
+
+                // Step 3: loss of the row, log(S / e_t) -- before the gradient, so
+                // that the warp's last row can count it done first
+                if (lane == 0 && !is_softmax(p)) {
+                    float l;
+                    if (has_t) {
+                        l = row_loss(s_rest, e_t, S, zt, M);
+                    } else {
+                        l = NAN;
+                        atomicAdd(&p.err[kErrBadTarget], 1);
+                    }
+                    p.loss_rows[r] = l;
+                }
+                if (i + 1 == ntl && r + 1 == r1) warp_done();
+
+                if (write_grad) {
+                    unsigned char *grow = p.grad + (size_t)r * C * ES;
+                    unsigned char *gvec = grow + nh * ES;
+                    auto grad2 = [&](const uint4 &xv, unsigned long long (&g2)[W2]) {
+                        E::unpack2(xv, g2);
+#pragma unroll
+                        for (int j = 0; j < W2; ++j) {
+                            if (!kKeepExp) {
+                                float a, b;
+                                f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
+                                g2[j] = f2_pack(ex2(a), ex2(b));
+                            }
+                            g2[j] = f2_mul(g2[j], sc2);
                         }
-                        g2[j] = f2_mul(g2[j], sc2);
+                    };
+                    if (vec_store) {
+#pragma unroll
+                        for (int k = 0; k < MAXV; ++k) {
+                            const int v = lane + 32 * k;
+                            if (v < nvec) {
+                                unsigned long long g2[W2];
+                                grad2(x[k], g2);
+                                *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack2(g2);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < MAXV; ++k) {
+                            const int v = lane + 32 * k;
+                            if (v < nvec) {
+                                unsigned long long g2[W2];
+                                grad2(x[k], g2);
+#pragma unroll
+                                for (int j = 0; j < W2; ++j) {
+                                    float a, b;
+                                    f2_unpack(g2[j], a, b);
+                                    E::store(gvec + (v * W + 2 * j) * ES, a);
+                                    E::store(gvec + (v * W + 2 * j + 1) * ES, b);
+                                }
+                            }
+                        }
+                    }
+                    // the owner of the target's vector overwrites the target,
+                    // after its vector's store
+                    if (v_t >= 0 && lane == (v_t & 31)) E::store(grow + (size_t)t * ES, g_t);
+                    // test hook: the whole vectors' fp32 values, before their
+                    // rounding (recomputed so that the loop above carries none of it)
+                    if (grad_f32_of(p)) {
+#pragma unroll
+                        for (int k = 0; k < MAXV; ++k) {
+                            const int v = lane + 32 * k;
+                            if (v < nvec) {
+                                unsigned long long g2[W2];
+                                E::unpack2(x[k], g2);
+#pragma unroll
+                                for (int j = 0; j < W2; ++j) {
+                                    if (!kKeepExp) {
+                                        float a, b;
+                                        f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
+                                        g2[j] = f2_pack(ex2(a), ex2(b));
+                                    }
+                                    float a, b;
+                                    f2_unpack(f2_mul(g2[j], sc2), a, b);
+                                    grad_f32_store<ES>(p, gvec + (v * W + 2 * j) * ES, a);
+                                    grad_f32_store<ES>(p, gvec + (v * W + 2 * j + 1) * ES, b);
+                                }
+                                if (v == v_t) grad_f32_store<ES>(p, grow + (size_t)t * ES, g_t);
+                            }
+                        }
+                    }
+                    if (ragged) {
+                        if (lane < nh) {
+                            const float gh = lane == t ? g_t : eh * scale;
+                            E::store(grow + lane * ES, gh);
+                            grad_f32_store<ES>(p, grow + lane * ES, gh);
+                        }
+                        if (lane < nt) {
+                            const int c = nh + nvec * W + lane;
+                            const float gc = c == t ? g_t : et * scale;
+                            E::store(grow + c * ES, gc);
+                            grad_f32_store<ES>(p, grow + c * ES, gc);
+                        }
+                    }
+                }
+            } else {
+                // The row stays in its slot and is swept there three times, CH
+                // vectors per lane at a time: the max, the sum of exponentials
+                // without the target's term, the gradient -- the register
+                // build's per-element arithmetic.
+                constexpr int CH = kWarpChunkVecs;
+                const uint4 kNeg = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord,
+                                              E::kNegInfWord);
+                auto load_chunk = [&](int base, uint4 (&x)[CH]) {
+#pragma unroll
+                    for (int k = 0; k < CH; ++k) {
+                        const int v = base + lane + 32 * k;
+                        x[k] = v < nvec ? lds128(vrow + 16 * v) : kNeg;
                     }
                 };
-                if (vec_store) {
+                const bool ragged = (nh | nt) != 0;
+                float hz = -INFINITY, tz = -INFINITY;
+                if (ragged) {
+                    if (lane < nh) hz = E::load(row + lane * ES);
+                    if (lane < nt) tz = E::load(vrow + (nvec * W + lane) * ES);
+                }
+                const float zt = has_t ? E::load(row + t * ES) : 0.f;
+
+                // Step 1: max
+                float m = fmaxf(hz, tz);
+                {
+                    typename E::MaxAcc macc = E::max_init();
+                    for (int base = 0; base < nvec; base += 32 * CH) {
+                        uint4 x[CH];
+                        load_chunk(base, x);
 #pragma unroll
-                    for (int k = 0; k < MAXV; ++k) {
-                        const int v = lane + 32 * k;
-                        if (v < nvec) {
-                            unsigned long long g2[W2];
-                            grad2(x[k], g2);
-                            *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack2(g2);
-                        }
+                        for (int k = 0; k < CH; ++k) E::max_step(macc, x[k]);
                     }
-                } else {
+                    m = fmaxf(m, E::max_value(macc));
+                }
+                m = warp_max(m);
+                const float M = m * kLog2e;
+                const unsigned long long nM2 = f2_pack(-M, -M);
+
+                // Step 2: sum of exponentials without the target's term (the
+                // lane holding the target's vector adds its other elements)
+                unsigned long long acc = 0ull;
+                float sa = 0.f;
+                for (int base = 0; base < nvec; base += 32 * CH) {
+                    uint4 x[CH];
+                    load_chunk(base, x);
 #pragma unroll
-                    for (int k = 0; k < MAXV; ++k) {
-                        const int v = lane + 32 * k;
-                        if (v < nvec) {
-                            unsigned long long g2[W2];
-                            grad2(x[k], g2);
+                    for (int k = 0; k < CH; ++k) {
+                        const int v = base + lane + 32 * k;
+                        if (v == v_t) {
+                            float z[W];
+                            E::unpack(x[k], z);
+                            const int d = tv - v_t * W;
 #pragma unroll
-                            for (int j = 0; j < W2; ++j) {
-                                float a, b;
-                                f2_unpack(g2[j], a, b);
-                                E::store(gvec + (v * W + 2 * j) * ES, a);
-                                E::store(gvec + (v * W + 2 * j + 1) * ES, b);
-                            }
+                            for (int j = 0; j < W; ++j)
+                                if (j != d) sa += ex2(fmaf(z[j], kLog2e, -M));
+                            continue;
                         }
+                        unsigned long long e2[W2];
+                        E::unpack2(x[k], e2);
+#pragma unroll
+                        for (int j = 0; j < W2; ++j) {
+                            float a, b;
+                            f2_unpack(f2_fma(e2[j], kL2E2, nM2), a, b);
+                            e2[j] = f2_pack(ex2(a), ex2(b));
+                        }
+                        const unsigned long long vs =
+                            W2 == 4 ? f2_add(f2_add(e2[0], e2[1]), f2_add(e2[W2 - 2], e2[W2 - 1]))
+                                    : f2_add(e2[0], e2[W2 - 1]);
+                        acc = f2_add(acc, vs);
                     }
                 }
-                // the owner of the target's vector overwrites the target,
-                // after its vector's store
-                if (v_t >= 0 && lane == (v_t & 31)) E::store(grow + (size_t)t * ES, g_t);
-                // test hook: the whole vectors' fp32 values, before their
-                // rounding (recomputed so that the loop above carries none of it)
-                if (grad_f32_of(p)) {
+                float pa, pb;
+                f2_unpack(acc, pa, pb);
+                float eh = 0.f, et = 0.f;
+                if (ragged) {
+                    if (lane < nh) eh = ex2(fmaf(hz, kLog2e, -M));
+                    if (lane < nt) et = ex2(fmaf(tz, kLog2e, -M));
+                    if (lane != t) sa += eh;
+                    if (nh + nvec * W + lane != t) pb += et;
+                }
+                const float s_rest = warp_sum(sa + pa + pb);
+                const float e_t = has_t ? ex2(fmaf(zt, kLog2e, -M)) : 0.f;
+                const float S = s_rest + e_t;
+                const float scale = fast_rcp(S) * row_grad_factor(p, gsc, r);
+                const unsigned long long sc2 = f2_pack(scale, scale);
+                const float g_t = -s_rest * scale;
+
+                // Step 3: loss of the row, before the gradient
+                if (lane == 0 && !is_softmax(p)) {
+                    float l;
+                    if (has_t) {
+                        l = row_loss(s_rest, e_t, S, zt, M);
+                    } else {
+                        l = NAN;
+                        atomicAdd(&p.err[kErrBadTarget], 1);
+                    }
+                    p.loss_rows[r] = l;
+                }
+                if (i + 1 == ntl && r + 1 == r1) warp_done();
+
+                // Step 4: gradient, a third sweep of the slot; the owner of the
+                // target's vector overwrites the target after its vector
+                if (write_grad) {
+                    unsigned char *grow = p.grad + (size_t)r * C * ES;
+                    unsigned char *gvec = grow + nh * ES;
+                    for (int base = 0; base < nvec; base += 32 * CH) {
+                        uint4 x[CH];
+                        load_chunk(base, x);
 #pragma unroll
-                    for (int k = 0; k < MAXV; ++k) {
-                        const int v = lane + 32 * k;
-                        if (v < nvec) {
-                            unsigned long long g2[W2];
-                            E::unpack2(x[k], g2);
+                        for (int k = 0; k < CH; ++k) {
+                            const int v = base + lane + 32 * k;
+                            if (v < nvec) {
+                                unsigned long long g2[W2];
+                                E::unpack2(x[k], g2);
 #pragma unroll
-                            for (int j = 0; j < W2; ++j) {
-                                if (!kKeepExp) {
+                                for (int j = 0; j < W2; ++j) {
                                     float a, b;
                                     f2_unpack(f2_fma(g2[j], kL2E2, nM2), a, b);
-                                    g2[j] = f2_pack(ex2(a), ex2(b));
+                                    g2[j] = f2_mul(f2_pack(ex2(a), ex2(b)), sc2);
                                 }
-                                float a, b;
-                                f2_unpack(f2_mul(g2[j], sc2), a, b);
-                                grad_f32_store<ES>(p, gvec + (v * W + 2 * j) * ES, a);
-                                grad_f32_store<ES>(p, gvec + (v * W + 2 * j + 1) * ES, b);
+                                if (vec_store) {
+                                    *reinterpret_cast<uint4 *>(gvec + 16 * v) = E::pack2(g2);
+                                } else {
+#pragma unroll
+                                    for (int j = 0; j < W2; ++j) {
+                                        float a, b;
+                                        f2_unpack(g2[j], a, b);
+                                        E::store(gvec + (v * W + 2 * j) * ES, a);
+                                        E::store(gvec + (v * W + 2 * j + 1) * ES, b);
+                                    }
+                                }
+                                if (grad_f32_of(p)) {  // test hook: the values before rounding
+#pragma unroll
+                                    for (int j = 0; j < W2; ++j) {
+                                        float a, b;
+                                        f2_unpack(g2[j], a, b);
+                                        grad_f32_store<ES>(p, gvec + (v * W + 2 * j) * ES, a);
+                                        grad_f32_store<ES>(p, gvec + (v * W + 2 * j + 1) * ES, b);
+                                    }
+                                }
+                                if (v == v_t) {
+                                    E::store(grow + (size_t)t * ES, g_t);
+                                    grad_f32_store<ES>(p, grow + (size_t)t * ES, g_t);
+                                }
                             }
-                            if (v == v_t) grad_f32_store<ES>(p, grow + (size_t)t * ES, g_t);
                         }
                     }
-                }
-                if (ragged) {
-                    if (lane < nh) {
-                        const float gh = lane == t ? g_t : eh * scale;
-                        E::store(grow + lane * ES, gh);
-                        grad_f32_store<ES>(p, grow + lane * ES, gh);
-                    }
-                    if (lane < nt) {
-                        const int c = nh + nvec * W + lane;
-                        const float gc = c == t ? g_t : et * scale;
-                        E::store(grow + c * ES, gc);
-                        grad_f32_store<ES>(p, grow + c * ES, gc);
+                    if (ragged) {
+                        if (lane < nh) {
+                            const float gh = lane == t ? g_t : eh * scale;
+                            E::store(grow + lane * ES, gh);
+                            grad_f32_store<ES>(p, grow + lane * ES, gh);
+                        }
+                        if (lane < nt) {
+                            const int c = nh + nvec * W + lane;
+                            const float gc = c == t ? g_t : et * scale;
+                            E::store(grow + c * ES, gc);
+                            grad_f32_store<ES>(p, grow + c * ES, gc);
+                        }
                     }
                 }
             }
-
         }
         __syncwarp();
         if (lane == 0 && issued < ntl) {
@@ -405,15 +572,15 @@ __global__ void __launch_bounds__(warp_kernel_warps(MINB) * 32, MINB)
     }
 }
 
-template <typename T, int MAXV, int MINB, typename P>
+template <typename T, int MAXV, int MINB, typename P, int NWK = warp_kernel_warps(MINB)>
 cudaError_t launch_p(const P &p, int ctas, int slots, int rows_per_tile, int slot_bytes,
                      int smem, cudaStream_t s) {
-    auto kern = rows_warp_kernel<T, MAXV, MINB, P>;
+    auto kern = rows_warp_kernel<T, MAXV, MINB, P, NWK>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas, 1, 1);
-    cfg.blockDim = dim3(warp_kernel_warps(MINB) * 32, 1, 1);
+    cfg.blockDim = dim3(NWK * 32, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -479,6 +646,39 @@ cudaError_t launch_t(const ParamsEx &p, int per_sm, int ctas, int slots, int row
     return launch_m<T, 1>(p, ctas, slots, rows_per_tile, slot_bytes, smem, s);
 }
 
+// The swept build (rows longer than the registers hold): NWK warps, one tile
+// of one row per slot.
+template <typename T, int NWK>
+cudaError_t launch_c(const ParamsEx &p, int ctas, int slots, int slot_bytes, int smem,
+                     cudaStream_t s) {
+    if (is_plain(p))
+        return launch_p<T, 0, 1, Params, NWK>(static_cast<const Params &>(p), ctas, slots, 1,
+                                              slot_bytes, smem, s);
+    return launch_p<T, 0, 1, ParamsEx, NWK>(p, ctas, slots, 1, slot_bytes, smem, s);
+}
+template <typename T, int NWK>
+cudaError_t occ_c(int smem, int *ctas) {
+    auto kern = rows_warp_kernel<T, 0, 1, Params, NWK>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, NWK * 32, smem);
+}
+template <typename T>
+cudaError_t launch_ct(const ParamsEx &p, int nw, int ctas, int slots, int slot_bytes, int smem,
+                      cudaStream_t s) {
+    if (nw == 16) return launch_c<T, 16>(p, ctas, slots, slot_bytes, smem, s);
+    if (nw == 8) return launch_c<T, 8>(p, ctas, slots, slot_bytes, smem, s);
+    if (nw == 4) return launch_c<T, 4>(p, ctas, slots, slot_bytes, smem, s);
+    return cudaErrorInvalidValue;
+}
+template <typename T>
+cudaError_t occ_ct(int nw, int smem, int *ctas) {
+    if (nw == 16) return occ_c<T, 16>(smem, ctas);
+    if (nw == 8) return occ_c<T, 8>(smem, ctas);
+    if (nw == 4) return occ_c<T, 4>(smem, ctas);
+    return cudaErrorInvalidValue;
+}
+
 template <typename T>
 cudaError_t occ_t(int per_sm, long long C, int smem, int *ctas) {
     if (per_sm >= 3) return occ_m<T, 3>(C, smem, ctas);
@@ -501,6 +701,19 @@ cudaError_t rows_warp_max_ctas_per_sm(int dtype, int per_sm, long long C, int sm
     if (dtype == 0) return occ_t<float>(per_sm, C, smem, ctas);
     if (dtype == 2) return occ_t<__half>(per_sm, C, smem, ctas);
     return occ_t<__nv_bfloat16>(per_sm, C, smem, ctas);
+}
+
+cudaError_t launch_rows_warp_swept(const ParamsEx &p, int dtype, int nw, int ctas, int slots,
+                                   int slot_bytes, int smem, cudaStream_t s) {
+    if (dtype == 0) return launch_ct<float>(p, nw, ctas, slots, slot_bytes, smem, s);
+    if (dtype == 2) return launch_ct<__half>(p, nw, ctas, slots, slot_bytes, smem, s);
+    return launch_ct<__nv_bfloat16>(p, nw, ctas, slots, slot_bytes, smem, s);
+}
+
+cudaError_t rows_warp_swept_max_ctas_per_sm(int dtype, int nw, int smem, int *ctas) {
+    if (dtype == 0) return occ_ct<float>(nw, smem, ctas);
+    if (dtype == 2) return occ_ct<__half>(nw, smem, ctas);
+    return occ_ct<__nv_bfloat16>(nw, smem, ctas);
 }
 
 }  // namespace ce

@@ -61,6 +61,15 @@ WARP_SHAPES = [(1, 1), (3, 2), (8, 3), (5, 5), (7, 7), (64, 10), (33, 31), (9, 3
 SPLIT_SHAPES = [(1, 1), (2, 3), (3, 17), (5, 1000), (4, 4099), (3, 8191), (6, 16385), (2, 40000),
                 (3, 50257)]
 STREAM_SHAPES = [(1, 1), (3, 5), (2, 4095), (2, 4096), (3, 4097), (2, 10000), (2, 50257)]
+# rows longer than a warp's registers hold (8 KB .. 48 KB), swept in shared
+# memory by the warp kernel: just past 8 KB, ragged, one and several sweeps
+# of 8 vectors per lane, the longest row, and many rows per warp (the ring
+# wraps)
+SWEPT_SHAPES = {"f32": [(1, 2049), (5, 2051), (37, 3001), (6, 4095), (7, 4096), (3, 8191),
+                        (4, 12000), (3000, 4500)],
+                "bf16": [(1, 4097), (5, 4101), (37, 6001), (6, 8191), (7, 8192), (3, 16383),
+                         (4, 24000), (3000, 9001)],
+                "f16": [(5, 4101), (9, 16384), (3, 24000)]}
 # the two-pass kernel's chunks hold 4096 fp32 / 8192 16-bit elements: rows
 # inside one chunk, across a chunk boundary, many chunks, and long rows
 TWOPASS_SHAPES = [(1, 1), (3, 2), (5, 5), (7, 31), (4, 1000), (3, 4095), (3, 4096), (2, 4097),
@@ -76,6 +85,32 @@ def test_warp_path_shapes(B, C, dtype):
     loss, grad = run(z, t, WARP)
     torch.cuda.synchronize()
     check_full(inp, loss, grad, f"warp {B}x{C} {dtype}")
+
+
+@pytest.mark.parametrize("dtype,B,C", [(d, b, c) for d, v in SWEPT_SHAPES.items() for b, c in v])
+def test_swept_warp_path_shapes(B, C, dtype):
+    inp = _case(B, C, dtype, seed=B * 7919 + C)
+    z, t = device_inputs(inp)
+    loss, grad = run(z, t, WARP)
+    torch.cuda.synchronize()
+    check_full(inp, loss, grad, f"swept warp {B}x{C} {dtype}")
+
+
+def test_swept_warp_path_is_planned_for_medium_rows():
+    """Rows past 8 KB for which 8 warps per SM fit (up to ~27 KB) go to the
+    warp kernel's swept build; 31 KB rows do not; past 48 KB the forced warp
+    path refuses."""
+    for C, dt in [(8000, ce.CE_BF16), (4500, ce.CE_F32), (6000, ce.CE_F32), (12000, ce.CE_BF16)]:
+        plan = ce.ce_query_plan(16384, C, dt)
+        assert plan["path_name"] == "rows_warp", (C, plan)
+        assert plan["threads"] in (128, 256, 512), plan
+    assert ce.ce_query_plan(8192, 16000, ce.CE_BF16)["path_name"] != "rows_warp"
+    assert ce.ce_query_plan(8192, 32000, ce.CE_BF16)["path_name"] == "row_split"
+    z = torch.zeros(2, 12289, device="cuda")  # 49156 bytes: past the swept build
+    t = torch.zeros(2, dtype=torch.int32, device="cuda")
+    with pytest.raises(ce.CEError) as ei:
+        ce.ce_fwd_bwd_path(z, t, torch.empty(1, device="cuda"), torch.empty_like(z), None, WARP, 0)
+    assert ei.value.status == 9
 
 
 @pytest.mark.parametrize("K", [1, 2, 3, 4, 6, 8])
@@ -177,7 +212,8 @@ def test_f16_refuses_slices_beyond_64kb():
 # ------------------------------------------------------ pointer alignment
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("path,split,C", [(WARP, 0, 37), (WARP, 0, 1001), (SPLIT, 1, 5003),
+@pytest.mark.parametrize("path,split,C", [(WARP, 0, 37), (WARP, 0, 1001), (WARP, 0, 5003),
+                                          (SPLIT, 1, 5003),
                                           (SPLIT, 4, 7001), (STREAM, 0, 5003),
                                           (TWOPASS, 0, 3), (TWOPASS, 0, 5003)])
 @pytest.mark.parametrize("zoff,goff", [(1, 0), (0, 1), (3, 2), (1, 1)])
@@ -204,7 +240,8 @@ def test_unaligned_tensors(dtype, path, split, C, zoff, goff):
 
 # ------------------------------------------------------------- data errors
 
-@pytest.mark.parametrize("path,split,C,dtype", [(WARP, 0, 100, "f32"), (SPLIT, 1, 9000, "bf16"),
+@pytest.mark.parametrize("path,split,C,dtype", [(WARP, 0, 100, "f32"), (WARP, 0, 9000, "bf16"),
+                                                (SPLIT, 1, 9000, "bf16"),
                                                 (SPLIT, 4, 9000, "f32"), (STREAM, 0, 9000, "f32"),
                                                 (TWOPASS, 0, 9000, "f32")])
 def test_out_of_range_targets(path, split, C, dtype):
@@ -227,7 +264,8 @@ def test_out_of_range_targets(path, split, C, dtype):
 
 # ------------------------------------------------------ stated properties
 
-@pytest.mark.parametrize("path,split,C,dtype", [(WARP, 0, 1000, "f32"), (SPLIT, 1, 32000, "bf16"),
+@pytest.mark.parametrize("path,split,C,dtype", [(WARP, 0, 1000, "f32"), (WARP, 0, 9001, "bf16"),
+                                                (SPLIT, 1, 32000, "bf16"),
                                                 (SPLIT, 4, 50257, "f32"), (STREAM, 0, 9000, "bf16"),
                                                 (TWOPASS, 0, 50257, "f32"),
                                                 (TWOPASS, 0, 128256, "bf16")])

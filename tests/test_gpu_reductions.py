@@ -32,7 +32,7 @@ MEAN, SUM, NONE = ce.CE_REDUCE_MEAN, ce.CE_REDUCE_SUM, ce.CE_REDUCE_NONE
 # (path, split, B, C): the warp kernel, the barrier-per-row split kernel at
 # K = 1 and with 100 KB fp32 slices, the pipelined split kernel, the streaming
 # path, the two-pass path
-PATHS = [(WARP, 0, 300, 1000), (SPLIT, 1, 5, 20000), (SPLIT, 4, 6, 40000),
+PATHS = [(WARP, 0, 300, 1000), (WARP, 0, 7, 9001), (SPLIT, 1, 5, 20000), (SPLIT, 4, 6, 40000),
          (SPLIT, 2, 3, 50257), (STREAM, 0, 3, 10000), (TWOPASS, 0, 5, 50257)]
 
 

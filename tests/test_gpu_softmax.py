@@ -42,6 +42,7 @@ TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 # K = 2, the streaming path, the two-pass path (short, chunk-sized and long
 # rows)
 PATHS = [(WARP, 0, 1, 1), (WARP, 0, 7, 7), (WARP, 0, 300, 1000), (WARP, 0, 5, 2047),
+         (WARP, 0, 9, 9001),
          (SPLIT, 1, 3, 17), (SPLIT, 1, 5, 20000), (SPLIT, 4, 6, 40000), (SPLIT, 2, 3, 50257),
          (SPLIT, 8, 2, 128256), (STREAM, 0, 1, 1), (STREAM, 0, 3, 10000), (STREAM, 0, 2, 4097),
          (TWOPASS, 0, 1, 1), (TWOPASS, 0, 7, 7), (TWOPASS, 0, 5, 4099), (TWOPASS, 0, 3, 50257),
