@@ -13,10 +13,13 @@
 //                            barrier; many rows in flight per SM;
 //   softmax_bwd_vec_kernel   rows of at most kVecThreads x kVecPerThread 16-byte
 //                            vectors whose every row starts 16-byte aligned in
-//                            all three tensors: each thread loads its vectors
-//                            of p and dy into registers (all loads in flight
-//                            before the first use), one block reduction, the
-//                            row written from the registers;
+//                            all three tensors: 128 threads per row up to 16 KB
+//                            (the CTA's 512 threads take 4 rows at a time),
+//                            512 beyond, each thread's
+//                            vectors of p and dy in registers (all loads in
+//                            flight before the first use), one reduction over
+//                            the row's threads, the row written from the
+//                            registers;
 //   softmax_bwd_any_kernel   any row: pass 1 accumulates the dot product over
 //                            the row, pass 2 reads p and dy again and writes dx
 //                            (p and dy cross HBM twice).
@@ -56,29 +59,52 @@ __device__ __forceinline__ float block_sum_fixed(float v, float *red) {
     return t;
 }
 
-template <typename T>
+// Sum over the TPR threads of row group g (warps [g * TPR / 32, ...)): warp
+// sums, then the group's warps through `red` and named barrier 1 + g (barrier
+// 0 is __syncthreads).  Every thread of the group gets the same bits.
+template <int TPR>
+__device__ __forceinline__ float group_sum_fixed(float v, float *red, int g) {
+    constexpr int GW = TPR / 32;
+    v = warp_sum(v);
+    const int lane = threadIdx.x & 31, wg = (threadIdx.x >> 5) % GW;
+    if (lane == 0) red[g * GW + wg] = v;
+    if (TPR == 32) return v;
+    named_sync(1 + g, TPR);
+    float t = lane < GW ? red[g * GW + lane] : 0.f;
+    t = warp_sum(t);
+    named_sync(1 + g, TPR);  // red is reused by the group's next row
+    return t;
+}
+
+// TPR threads per row (128 or 512), kVecThreads / TPR rows of the CTA at a
+// time: rows of at most TPR x kVecPerThread 16-byte vectors.
+template <typename T, int TPR>
 __global__ void __launch_bounds__(kVecThreads, 1)
     softmax_bwd_vec_kernel(const unsigned char *P, const unsigned char *DY, unsigned char *DX,
                            long long B, long long C) {
     using E = Elem<T>;
     constexpr int W = E::kVec;
     constexpr int W2 = W / 2;
+    constexpr int RPC = kVecThreads / TPR;  // rows per CTA at a time
     __shared__ float red[kVecThreads / 32];
     pdl_trigger();
     pdl_wait();
-    const int tid = threadIdx.x;
+    const int g = threadIdx.x / TPR;    // the thread's row group
+    const int tid = threadIdx.x % TPR;  // its place in the group
     const long long nvec = C / W;  // whole vectors per row (C * es is a multiple of 16)
     const size_t row_bytes = (size_t)C * E::kBytes;
-    // The CTA's rows are b, b + grid, ...; the next row's reads overlap the
-    // current row.  fp32: a thread's vectors of the next row are loaded into
-    // its registers as soon as it has written the same vectors of the current
-    // row.  16-bit (whose unpacked pairs leave no registers for that): the
-    // next row of p and dy is prefetched into L2 by one bulk request each when
-    // the current row starts, so its loads are served by L2.
+    const long long first = (long long)blockIdx.x * RPC + g;
+    const long long step = (long long)gridDim.x * RPC;
+    // A group's rows are first, first + step, ...; the next row's reads
+    // overlap the current row.  fp32: a thread's vectors of the next row are
+    // loaded into its registers as soon as it has written the same vectors of
+    // the current row.  16-bit (whose unpacked pairs leave no registers for
+    // that): the next row of p and dy is prefetched into L2 in 16 KB bulk
+    // requests when the current row starts, so its loads are served by L2.
     constexpr bool kRegPipe = sizeof(T) == 4;
     uint4 pv[kVecPerThread], dv[kVecPerThread];
     auto load_vec = [&](long long b, int k) {
-        const long long v = tid + (long long)k * kVecThreads;
+        const long long v = tid + (long long)k * TPR;
         pv[k] = make_uint4(0u, 0u, 0u, 0u);
         dv[k] = make_uint4(0u, 0u, 0u, 0u);
         if (b < B && v < nvec) {
@@ -88,13 +114,14 @@ __global__ void __launch_bounds__(kVecThreads, 1)
     };
     if (kRegPipe) {
 #pragma unroll
-        for (int k = 0; k < kVecPerThread; ++k) load_vec(blockIdx.x, k);
+        for (int k = 0; k < kVecPerThread; ++k) load_vec(first, k);
     }
-    for (long long b = blockIdx.x; b < B; b += gridDim.x) {
+    // each group loops over its own rows and meets only its own barrier
+    for (long long b = first; b < B; b += step) {
         uint4 *xrow = reinterpret_cast<uint4 *>(DX + (size_t)b * row_bytes);
         if (!kRegPipe) {
             // 16 KB pieces of the next row of p (threads 0-3) and dy (4-7)
-            const long long bn = b + gridDim.x;
+            const long long bn = b + step;
             const size_t off = (size_t)(tid & 3) * kPrefetchPiece;
             if (tid < 8 && bn < B && off < row_bytes) {
                 const unsigned char *src = (tid < 4 ? P : DY) + (size_t)bn * row_bytes + off;
@@ -115,11 +142,11 @@ __global__ void __launch_bounds__(kVecThreads, 1)
         }
         float sa, sb;
         f2_unpack(acc, sa, sb);
-        const float dot = block_sum_fixed<kVecThreads>(sa + sb, red);
+        const float dot = group_sum_fixed<TPR>(sa + sb, red, g);
         const unsigned long long nd2 = f2_pack(-dot, -dot);
 #pragma unroll
         for (int k = 0; k < kVecPerThread; ++k) {
-            const long long v = tid + (long long)k * kVecThreads;
+            const long long v = tid + (long long)k * TPR;
             if (v < nvec) {
                 unsigned long long p2[W2], d2[W2];
                 E::unpack2(pv[k], p2);
@@ -128,7 +155,7 @@ __global__ void __launch_bounds__(kVecThreads, 1)
                 for (int i = 0; i < W2; ++i) p2[i] = f2_mul(p2[i], f2_add(d2[i], nd2));
                 __stcs(xrow + v, E::pack2(p2));
             }
-            if (kRegPipe) load_vec(b + gridDim.x, k);
+            if (kRegPipe) load_vec(b + step, k);
         }
     }
 }
@@ -270,7 +297,14 @@ cudaError_t launch_t(const void *p, const void *dy, void *dx, long long B, long 
     if (nvec <= 32 * kWarpMaxVpl)
         return launch_rows(softmax_bwd_warp_kernel<T, kWarpMaxVpl>, kWarpCtaThreads,
                            kRowsPerWarpCta, p, dy, dx, B, C, sms, s);
-    return launch_rows(softmax_bwd_vec_kernel<T>, kVecThreads, 1, p, dy, dx, B, C, sms, s);
+    // rows of up to 16 KB: 128 threads each, four rows of the CTA at once
+    // (measured on GB300: 16 KB rows 183 -> 132 us bf16, 186 -> 118 us fp32,
+    // 16384 rows); longer rows: 512 threads (two 256-thread groups were
+    // slower on 32 KB bf16 rows, 134 against 124 us)
+    if (nvec <= 128 * kVecPerThread)
+        return launch_rows(softmax_bwd_vec_kernel<T, 128>, kVecThreads, kVecThreads / 128, p, dy,
+                           dx, B, C, sms, s);
+    return launch_rows(softmax_bwd_vec_kernel<T, 512>, kVecThreads, 1, p, dy, dx, B, C, sms, s);
 }
 
 }  // namespace

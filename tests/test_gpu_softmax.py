@@ -193,9 +193,12 @@ def _check_bwd(p, dy, dx, dtype, what):
              dtype, what)
 
 
-# rows the register kernel takes (16-byte multiples, at most 64 KB) and rows
-# it refuses: odd widths and rows beyond 64 KB
+# rows the register kernels take (16-byte multiples, at most 64 KB: a warp
+# per row up to 4 KB, 128 threads per row up to 16 KB -- four rows of a CTA
+# at once, groups with unequal row counts -- and 512 beyond) and rows they
+# refuse: odd widths and rows beyond 64 KB
 BWD_SHAPES = [(1, 4), (3, 8), (64, 1000), (300, 1024), (7, 8192), (2, 16384), (5, 16000),
+              (9, 3000), (1030, 2048), (3, 4096),
               (1, 1), (3, 5), (9, 1001), (4, 20000), (2, 50257)]
 
 
