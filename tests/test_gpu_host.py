@@ -60,9 +60,11 @@ def _both(inp, pinned=True, stream=None, grad_to_host=False):
     return lh, grad_h, loss_d, grad_d
 
 
-# (B, C, dtype): the warp, split and two-pass kernels, f16, ragged rows, and
+# (B, C, dtype): the warp kernel (rows in registers and swept in shared
+# memory), the split and two-pass kernels, f16, ragged rows, and
 # batches of several 64 MiB chunks (a last chunk of fewer rows included)
-CASES = [(8, 10, "f32"), (3, 200000, "f32"), (4096, 1000, "f32"), (1024, 32000, "bf16"),
+CASES = [(8, 10, "f32"), (3, 200000, "f32"), (4096, 1000, "f32"), (600, 9001, "bf16"),
+         (1024, 32000, "bf16"),
          (512, 32000, "f16"), (7, 3001, "f32"), (40000, 1000, "f32"), (4096, 32000, "bf16"),
          (110, 600000, "bf16"), (1500, 50257, "f32"), (1100, 128256, "bf16")]
 

@@ -52,10 +52,12 @@ def _same_bits(a, b):
     return torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
-# (B, C, dtype): the warp-per-row kernel, the split kernel (one CTA per row),
+# (B, C, dtype): the warp-per-row kernel (rows in registers, and 18 KB rows
+# swept in shared memory), the split kernel (one CTA per row),
 # the two-pass kernel (fp32 C = 200000), and B at the scratch's limit (the last
 # row losses sit at the end of the static array)
-CASES = [(300, 1000, "f32"), (97, 32000, "bf16"), (40, 200000, "f32"), (MAX_ROWS, 8, "f32")]
+CASES = [(300, 1000, "f32"), (300, 9001, "bf16"), (97, 32000, "bf16"), (40, 200000, "f32"),
+         (MAX_ROWS, 8, "f32")]
 
 
 def test_noalloc_matches_ce_fwd_bwd_on_two_calls_in_a_row():
