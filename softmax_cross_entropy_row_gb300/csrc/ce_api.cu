@@ -109,6 +109,7 @@ struct Plan {
     int swept_nw = 0;     // warp path, rows swept in shared memory: warps per CTA (else 0)
     int vecs = 8;         // split path: 16-byte vectors per thread (8, 12 or 16)
     bool pipe = false;    // split path: the pipelined kernel (slices of at most 8 vectors)
+    int split_threads = ce::kSplitThreads;  // split path at K = 1: threads per CTA
     long long chunks = 0; // stream path
 };
 
@@ -232,6 +233,13 @@ int swept_slots_override() {
     static int v = -1;
     return env_int_once("CE_SWEPT_SLOTS", &v);
 }
+// Tuning knob: CE_SPLIT_THREADS=512 keeps the split kernel at K = 1 in CTAs
+// of kSplitThreads threads for rows a 128-thread CTA holds (0 or unset: 128
+// threads there).  Read once.
+int split_threads_override() {
+    static int v = -1;
+    return env_int_once("CE_SPLIT_THREADS", &v);
+}
 
 // Warp path for rows longer than a warp's registers hold (8 KB .. 48 KB):
 // one row per tile, swept in its slot.  What the time depends on is the
@@ -336,8 +344,24 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     }
     if (K != 1 && K != 2 && K != 3 && K != 4 && K != 6 && K != 8) return CE_ERR_PATH;
     const long long se = slice_of(K);
-    const int vecs = vecs_of(se);
-    const int nslots = nslots_of(se);
+    int vecs = vecs_of(se);
+    int nslots = nslots_of(se);
+    // K = 1 rows of at most 32 KB (16 vectors per thread): 128-thread CTAs,
+    // two slots each, several CTAs per SM.  Measured on GB300 (8192 rows):
+    // 31 KB rows 0.80 of peak bf16 / 0.92 fp32, against 0.54 / 0.68 in one
+    // 512-thread CTA per SM, which pays ~2.3 us per row; 192- and 256-thread
+    // CTAs ran slower than 512 on 32-48 KB rows (one CTA per SM by registers).
+    // f16 is built for 8 vectors per thread only.
+    int nt = ce::kSplitThreads;
+    if (K == 1 && split_threads_override() != ce::kSplitThreads) {
+        const long long need = se * es + 32, cap = 128LL * 16;
+        const int v128 = need <= 8 * cap ? 8 : need <= 12 * cap ? 12 : need <= 16 * cap ? 16 : 0;
+        if (v128 && !(dtype == CE_F16 && v128 > 8)) {
+            nt = 128;
+            vecs = v128;
+            if (nslots > 2) nslots = 2;
+        }
+    }
     if (vecs == 0 || nslots < 1) return CE_ERR_PATH;
     if (dtype == CE_F16 && vecs > 8) return CE_ERR_PATH;  // f16 is built for 8 vectors only
     const long long slot_bytes = slot_of(se);
@@ -347,10 +371,10 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     const bool pipe = K > 1 && vecs <= ce::kPipeVecs && split_pipe_enabled();
     int clusters = 0;
     int rc = cached_occupancy(
-        dtype, CE_PATH_ROW_SPLIT, K * 64 + vecs + (pipe ? 32 : 0), smem,
+        dtype, CE_PATH_ROW_SPLIT, K * 64 + vecs + (pipe ? 32 : 0) + nt * 1000, smem,
         [&](int *v) {
             return pipe ? ce::split_pipe_max_clusters(dtype, K, smem, v)
-                        : ce::split_max_clusters(dtype, K, vecs, smem, v);
+                        : ce::split_max_clusters(dtype, K, nt, vecs, smem, v);
         },
         &clusters);
     if (rc != CE_OK) return rc;
@@ -359,7 +383,8 @@ int plan_split(long long B, long long C, int es, const DeviceInfo &d, int dtype,
     pl->path = CE_PATH_ROW_SPLIT;
     pl->split = K;
     pl->ctas = clusters * K;
-    pl->threads = ce::kSplitThreads;
+    pl->threads = nt;
+    pl->split_threads = nt;
     pl->vecs = vecs;
     pl->pipe = pipe;
     pl->smem = smem;
@@ -427,8 +452,8 @@ cudaError_t launch_split_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, 
     if (pl.pipe)
         return ce::launch_split_pipe(p, dtype, pl.split, pl.ctas, pl.nslots, pl.slot_bytes,
                                      pl.slice, pl.smem, s);
-    return ce::launch_split(p, dtype, pl.split, pl.vecs, pl.ctas, pl.nslots, pl.slot_bytes,
-                            pl.slice, pl.smem, split_stage_enabled() ? 1 : 0, s);
+    return ce::launch_split(p, dtype, pl.split, pl.split_threads, pl.vecs, pl.ctas, pl.nslots,
+                            pl.slot_bytes, pl.slice, pl.smem, split_stage_enabled() ? 1 : 0, s);
 }
 
 cudaError_t launch_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, cudaStream_t s) {

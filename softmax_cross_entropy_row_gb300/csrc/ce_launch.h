@@ -33,14 +33,15 @@ constexpr int kMaxWarpSlots = 4;  // per warp
 // Split-row path: one row (K = 1) or one slice of a row per CTA of a cluster
 // of K CTAs; `nslots` staged slices of `slot_bytes` each per CTA.
 // K CTAs per row (1, 2, 3, 4, 6 or 8), each holding a slice of at most
-// kSplitThreads * vecs 16-byte vectors (vecs = 8, 12 or 16) in registers.
-// `staged` = 1: gradients of whole vectors go out through the row's own slot
-// by one TMA bulk store (needs grad and logits equally aligned mod 16).
-cudaError_t launch_split(const ParamsEx &p, int dtype, int K, int vecs, int ctas, int nslots,
-                         int slot_bytes, long long slice_elems, int smem, int staged,
+// nt * vecs 16-byte vectors (vecs = 8, 12 or 16) in registers; nt threads per
+// CTA: kSplitThreads, or at K = 1 also 128 (narrower CTAs, several per SM).  `staged` = 1: gradients of whole vectors go out through the row's own
+// slot by one TMA bulk store (needs grad and logits equally aligned mod 16).
+cudaError_t launch_split(const ParamsEx &p, int dtype, int K, int nt, int vecs, int ctas,
+                         int nslots, int slot_bytes, long long slice_elems, int smem, int staged,
                          cudaStream_t s);
-// Largest number of co-resident clusters of K CTAs with `smem` dynamic bytes.
-cudaError_t split_max_clusters(int dtype, int K, int vecs, int smem, int *clusters);
+// Largest number of co-resident clusters of K CTAs of nt threads with `smem`
+// dynamic bytes.
+cudaError_t split_max_clusters(int dtype, int K, int nt, int vecs, int smem, int *clusters);
 
 // The pipelined split-row kernel (ce_row_pipe.cu): K = 2..8 CTAs per row,
 // slices of at most kSplitThreads * kPipeVecs vectors, no CTA-wide barrier per

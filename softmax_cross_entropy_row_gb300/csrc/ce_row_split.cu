@@ -571,10 +571,15 @@ cudaError_t max_clusters_k(int smem, int *clusters) {
     return cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
 }
 
+// At K = 1 the CTA may be narrower than kSplitThreads (nt = 128: rows of
+// 128 x V vectors, several CTAs per SM); clusters keep kSplitThreads.
 template <typename T, int V>
-cudaError_t launch_v(const ParamsEx &p, int K, int ctas, int nslots, int slot_bytes, long long se,
-                     int smem, int staged, cudaStream_t s) {
+cudaError_t launch_v(const ParamsEx &p, int K, int nt, int ctas, int nslots, int slot_bytes,
+                     long long se, int smem, int staged, cudaStream_t s) {
     constexpr int NT = kSplitThreads;
+    if (K == 1 && nt == 128)
+        return launch_k<T, 1, 128, V>(p, ctas, nslots, slot_bytes, se, smem, staged, s);
+    if (nt != NT) return cudaErrorInvalidValue;
     switch (K) {
         case 1: return launch_k<T, 1, NT, V>(p, ctas, nslots, slot_bytes, se, smem, staged, s);
         case 2: return launch_k<T, 2, NT, V>(p, ctas, nslots, slot_bytes, se, smem, staged, s);
@@ -587,8 +592,10 @@ cudaError_t launch_v(const ParamsEx &p, int K, int ctas, int nslots, int slot_by
 }
 
 template <typename T, int V>
-cudaError_t max_clusters_v(int K, int smem, int *clusters) {
+cudaError_t max_clusters_v(int K, int nt, int smem, int *clusters) {
     constexpr int NT = kSplitThreads;
+    if (K == 1 && nt == 128) return max_clusters_k<T, 1, 128, V>(smem, clusters);
+    if (nt != NT) return cudaErrorInvalidValue;
     switch (K) {
         case 1: return max_clusters_k<T, 1, NT, V>(smem, clusters);
         case 2: return max_clusters_k<T, 2, NT, V>(smem, clusters);
@@ -603,49 +610,54 @@ cudaError_t max_clusters_v(int K, int smem, int *clusters) {
 // f16 rows are built for slices of 8 vectors per thread only (the planner
 // keeps 16-bit rows there, as for bf16).
 template <typename T>
-cudaError_t launch_t(const ParamsEx &p, int K, int vecs, int ctas, int nslots, int slot_bytes,
-                     long long se, int smem, int staged, cudaStream_t s) {
+cudaError_t launch_t(const ParamsEx &p, int K, int nt, int vecs, int ctas, int nslots,
+                     int slot_bytes, long long se, int smem, int staged, cudaStream_t s) {
     if constexpr (std::is_same<T, __half>::value) {
         if (vecs != 8) return cudaErrorInvalidValue;
-        return launch_v<T, 8>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
+        return launch_v<T, 8>(p, K, nt, ctas, nslots, slot_bytes, se, smem, staged, s);
     } else {
-        if (vecs == 16) return launch_v<T, 16>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
-        if (vecs == 12) return launch_v<T, 12>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
-        if (vecs == 8) return launch_v<T, 8>(p, K, ctas, nslots, slot_bytes, se, smem, staged, s);
+        if (vecs == 16)
+            return launch_v<T, 16>(p, K, nt, ctas, nslots, slot_bytes, se, smem, staged, s);
+        if (vecs == 12)
+            return launch_v<T, 12>(p, K, nt, ctas, nslots, slot_bytes, se, smem, staged, s);
+        if (vecs == 8)
+            return launch_v<T, 8>(p, K, nt, ctas, nslots, slot_bytes, se, smem, staged, s);
         return cudaErrorInvalidValue;
     }
 }
 
 template <typename T>
-cudaError_t max_clusters_t(int K, int vecs, int smem, int *clusters) {
+cudaError_t max_clusters_t(int K, int nt, int vecs, int smem, int *clusters) {
     if constexpr (std::is_same<T, __half>::value) {
         if (vecs != 8) return cudaErrorInvalidValue;
-        return max_clusters_v<T, 8>(K, smem, clusters);
+        return max_clusters_v<T, 8>(K, nt, smem, clusters);
     } else {
-        if (vecs == 16) return max_clusters_v<T, 16>(K, smem, clusters);
-        if (vecs == 12) return max_clusters_v<T, 12>(K, smem, clusters);
-        if (vecs == 8) return max_clusters_v<T, 8>(K, smem, clusters);
+        if (vecs == 16) return max_clusters_v<T, 16>(K, nt, smem, clusters);
+        if (vecs == 12) return max_clusters_v<T, 12>(K, nt, smem, clusters);
+        if (vecs == 8) return max_clusters_v<T, 8>(K, nt, smem, clusters);
         return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_split(const ParamsEx &p, int dtype, int K, int vecs, int ctas, int nslots,
-                         int slot_bytes, long long slice_elems, int smem, int staged,
+cudaError_t launch_split(const ParamsEx &p, int dtype, int K, int nt, int vecs, int ctas,
+                         int nslots, int slot_bytes, long long slice_elems, int smem, int staged,
                          cudaStream_t s) {
     if (dtype == 0)
-        return launch_t<float>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem, staged, s);
+        return launch_t<float>(p, K, nt, vecs, ctas, nslots, slot_bytes, slice_elems, smem,
+                               staged, s);
     if (dtype == 2)
-        return launch_t<__half>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem, staged, s);
-    return launch_t<__nv_bfloat16>(p, K, vecs, ctas, nslots, slot_bytes, slice_elems, smem,
+        return launch_t<__half>(p, K, nt, vecs, ctas, nslots, slot_bytes, slice_elems, smem,
+                                staged, s);
+    return launch_t<__nv_bfloat16>(p, K, nt, vecs, ctas, nslots, slot_bytes, slice_elems, smem,
                                    staged, s);
 }
 
-cudaError_t split_max_clusters(int dtype, int K, int vecs, int smem, int *clusters) {
-    if (dtype == 0) return max_clusters_t<float>(K, vecs, smem, clusters);
-    if (dtype == 2) return max_clusters_t<__half>(K, vecs, smem, clusters);
-    return max_clusters_t<__nv_bfloat16>(K, vecs, smem, clusters);
+cudaError_t split_max_clusters(int dtype, int K, int nt, int vecs, int smem, int *clusters) {
+    if (dtype == 0) return max_clusters_t<float>(K, nt, vecs, smem, clusters);
+    if (dtype == 2) return max_clusters_t<__half>(K, nt, vecs, smem, clusters);
+    return max_clusters_t<__nv_bfloat16>(K, nt, vecs, smem, clusters);
 }
 
 }  // namespace ce

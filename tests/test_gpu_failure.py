@@ -34,7 +34,7 @@ SHORT_WAIT_CYCLES = 1_000_000  # about half a millisecond
 # kernel alone (K = 1) and in a cluster of two (100 KB slices, so not the
 # pipelined kernel); the pipelined split kernel (K = 2, 9 KB slices); the
 # two-pass kernel
-CASES = [(WARP, 0, 40, 1000, "f32"), (WARP, 0, 40, 9001, "bf16"), (SPLIT, 1, 6, 20000, "f32"), (SPLIT, 2, 6, 50257, "f32"),
+CASES = [(WARP, 0, 40, 1000, "f32"), (WARP, 0, 40, 9001, "bf16"), (SPLIT, 1, 6, 7000, "f32"), (SPLIT, 1, 6, 20000, "f32"), (SPLIT, 2, 6, 50257, "f32"),
          (SPLIT, 2, 6, 9000, "bf16"), (TWOPASS, 0, 6, 50257, "f32"), (TWOPASS, 0, 5, 9000, "bf16")]
 
 

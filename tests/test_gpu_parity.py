@@ -104,8 +104,11 @@ def test_swept_warp_path_is_planned_for_medium_rows():
         plan = ce.ce_query_plan(16384, C, dt)
         assert plan["path_name"] == "rows_warp", (C, plan)
         assert plan["threads"] in (128, 256, 512), plan
-    assert ce.ce_query_plan(8192, 16000, ce.CE_BF16)["path_name"] != "rows_warp"
-    assert ce.ce_query_plan(8192, 32000, ce.CE_BF16)["path_name"] == "row_split"
+    # 31 KB rows: the split kernel in 128-thread CTAs; 64 KB rows: 512 threads
+    plan = ce.ce_query_plan(8192, 16000, ce.CE_BF16)
+    assert (plan["path_name"], plan["threads"]) == ("row_split", 128), plan
+    plan = ce.ce_query_plan(8192, 32000, ce.CE_BF16)
+    assert (plan["path_name"], plan["threads"]) == ("row_split", 512), plan
     z = torch.zeros(2, 12289, device="cuda")  # 49156 bytes: past the swept build
     t = torch.zeros(2, dtype=torch.int32, device="cuda")
     with pytest.raises(ce.CEError) as ei:
