@@ -452,8 +452,11 @@ cudaError_t launch_split_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, 
     if (pl.pipe)
         return ce::launch_split_pipe(p, dtype, pl.split, pl.ctas, pl.nslots, pl.slot_bytes,
                                      pl.slice, pl.smem, s);
+    // staging hands a slot back one row late, so it needs a second slot (with
+    // one, the next row's copy would wait for a slot that never comes back)
+    const int staged = split_stage_enabled() && pl.nslots >= 2 ? 1 : 0;
     return ce::launch_split(p, dtype, pl.split, pl.split_threads, pl.vecs, pl.ctas, pl.nslots,
-                            pl.slot_bytes, pl.slice, pl.smem, split_stage_enabled() ? 1 : 0, s);
+                            pl.slot_bytes, pl.slice, pl.smem, staged, s);
 }
 
 cudaError_t launch_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, cudaStream_t s) {

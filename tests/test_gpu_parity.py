@@ -134,6 +134,21 @@ def test_split_path_shapes(B, C, dtype, K):
     check_full(inp, loss, grad, f"split K={K} {B}x{C} {dtype}")
 
 
+@pytest.mark.parametrize("K,C", [(1, 30000), (1, 30001), (2, 60000)])
+def test_split_path_with_one_slot(K, C):
+    """fp32 slices of ~117 KB leave room for one ring slot per CTA: the
+    gradient is then stored directly (staging hands a slot back one row late
+    and needs a second), every row is computed and no wait gives up."""
+    inp = _case(9, C, "f32", seed=C + K)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ce.ce_get_device_errors(s)  # clear
+        z, t = device_inputs(inp)
+        loss, grad = run(z, t, SPLIT, K, s)
+        assert ce.ce_get_device_errors(s) == (0, 0)
+    check_full(inp, loss, grad, f"split K={K} one slot {C}")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("B,C", STREAM_SHAPES)
 def test_stream_path_shapes(B, C, dtype):
