@@ -79,19 +79,23 @@ HOST_ONLY_SOURCES = ("ce_api.cu",)
 SHARED_DEVICE_SOURCES = ("ce_device.cuh", "ce_launch.h")
 KERNEL_SOURCES = {"rows_warp": "ce_rows_warp.cu", "row_split": "ce_row_split.cu",
                   "row_pipe": "ce_row_pipe.cu", "row_twopass": "ce_row_twopass.cu",
-                  "stream": "ce_stream.cu"}
+                  "stream": "ce_stream.cu", "rows_online": "ce_rows_online.cu"}
 PLAN_KEYS = ("path", "split", "ctas", "threads", "smem_bytes")
 
 
 def source_hash(kernel: str | None = None) -> str:
-    """Hash of a kernel's device sources (its file and the shared headers), or
-    of every csrc file but the host-only ones when no kernel is named."""
+    """Hash of a kernel's device sources (its file, a header of the same name
+    if it has one, and the shared headers), or of every csrc file but the
+    host-only ones when no kernel is named."""
     csrc = os.path.join(ROOT, "softmax_cross_entropy_row_gb300", "csrc")
     if kernel is None:
         names = sorted(os.path.basename(p) for p in glob.glob(os.path.join(csrc, "*"))
                        if os.path.basename(p) not in HOST_ONLY_SOURCES)
     else:
-        names = sorted((KERNEL_SOURCES[kernel],) + SHARED_DEVICE_SOURCES)
+        own = KERNEL_SOURCES[kernel]
+        header = os.path.splitext(own)[0] + ".h"
+        names = sorted((own,) + SHARED_DEVICE_SOURCES
+                       + ((header,) if os.path.exists(os.path.join(csrc, header)) else ()))
     h = hashlib.sha256()
     for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
@@ -437,6 +441,8 @@ wl.WORKLOADS_BY_NAME.setdefault(F16_HEAD.name, F16_HEAD)
 NEXT_ROWS = [("f16_logits", "lm_head_8192x32000_f16", "plain"),
              ("loss_only_mean", "classifier_4096x1000_f32", "forward"),
              ("loss_only_mean", "lm_head_8192x32000_bf16", "forward"),
+             ("loss_only_mean", "lm_head_4096x128256_bf16_peaked", "forward"),
+             ("loss_only_mean", "stress_16384x50257_f32", "forward"),
              ("sum_scalar_upstream", "classifier_4096x1000_f32", "sum"),
              ("none_per_row_upstream", "classifier_4096x1000_f32", "none"),
              ("softmax_forward", "lm_head_8192x32000_bf16", "softmax_fwd"),

@@ -68,10 +68,16 @@ typedef enum {
                               staged once in shared memory by TMA                    */
     CE_PATH_STREAM = 3,    /* any row: chunk partials, then a recompute-and-write
                               pass (a second launch; logits read twice from HBM)    */
-    CE_PATH_ROW_TWOPASS = 4 /* any row, one CTA per row: a running max and sum over
+    CE_PATH_ROW_TWOPASS = 4, /* any row, one CTA per row: a running max and sum over
                               chunks staged by TMA, then the gradient from a second
                               read of the row (served by L2).  CE_PATH_AUTO takes it
                               for rows one CTA cannot hold in registers             */
+    CE_PATH_ROWS_ONLINE = 5 /* the loss alone (grad_out NULL), any row: one warp per
+                              row, read once from global memory with a running max
+                              and a rescaled sum per lane.  CE_PATH_AUTO takes it
+                              for the loss alone on rows past 8 KB in batches of
+                              at least 8 rows per SM.  With a gradient, or for the
+                              softmax forward: CE_ERR_PATH                          */
 } ce_path;
 
 /*
@@ -115,6 +121,7 @@ int ce_fwd_bwd(const void *logits, const int32_t *targets, int64_t B, int64_t C,
  *   split  CE_PATH_ROW_SPLIT: CTAs per row (1, 2, 3, 4, 6 or 8; 0 = choose;
  *          f16 rows need slices of at most 64 KB per CTA);
  *          CE_PATH_STREAM: classes per chunk (multiple of 8; 0 = choose);
+ *          CE_PATH_ROWS_ONLINE: 1 + the kernel build (0 .. 4; 0 = choose);
  *          ignored otherwise.
  * Returns CE_ERR_PATH when the forced path cannot hold the row in shared
  * memory; otherwise as ce_fwd_bwd.  All paths give results within the same

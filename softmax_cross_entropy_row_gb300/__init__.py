@@ -33,13 +33,15 @@ CE_PATH_ROWS_WARP = 1
 CE_PATH_ROW_SPLIT = 2
 CE_PATH_STREAM = 3
 CE_PATH_ROW_TWOPASS = 4
+CE_PATH_ROWS_ONLINE = 5
 
 CE_REDUCE_MEAN = 0
 CE_REDUCE_SUM = 1
 CE_REDUCE_NONE = 2
 
 PATH_NAMES = {CE_PATH_ROWS_WARP: "rows_warp", CE_PATH_ROW_SPLIT: "row_split",
-              CE_PATH_STREAM: "stream", CE_PATH_ROW_TWOPASS: "row_twopass"}
+              CE_PATH_STREAM: "stream", CE_PATH_ROW_TWOPASS: "row_twopass",
+              CE_PATH_ROWS_ONLINE: "rows_online"}
 
 STATUS = {0: "CE_OK", 1: "CE_ERR_NULL", 2: "CE_ERR_SHAPE", 3: "CE_ERR_DTYPE",
           4: "CE_ERR_ALIGN", 5: "CE_ERR_CUDA", 6: "CE_ERR_OVERLAP", 7: "CE_ERR_POINTER",

@@ -17,6 +17,7 @@
 #include "../../include/ce.h"
 #include "../../include/ce_testing.h"
 #include "ce_launch.h"
+#include "ce_rows_online.h"
 
 namespace {
 
@@ -111,11 +112,13 @@ struct Plan {
     bool pipe = false;    // split path: the pipelined kernel (slices of at most 8 vectors)
     int split_threads = ce::kSplitThreads;  // split path at K = 1: threads per CTA
     long long chunks = 0; // stream path
+    int online_build = 0; // loss-only warp-per-row path: the kernel build
 };
 
 constexpr int kStaticSmemReserve = 2048;       // static __shared__ of the kernels
 constexpr long long kWarpRowMax = 8192;        // bytes: warp-per-row path up to here
 constexpr long long kWarpTileTarget = 2048;    // bytes of rows per warp tile
+constexpr long long kOnlineMinRowsPerSm = 8;   // loss-only warp-per-row path from here
 
 int round_up(long long v, long long a) { return (int)((v + a - 1) / a * a); }
 
@@ -435,6 +438,50 @@ int plan_twopass(long long B, const DeviceInfo &d, int dtype, Plan *pl) {
     return CE_OK;
 }
 
+// Loss-only warp-per-row path: a warp streams each row once from global
+// memory (no staging), so its time is set by how many loads the resident
+// warps keep in flight.  Measured on GB300 (loss alone, mean): the build of
+// 16 vectors per lane per step (8 KB per warp) and two 8-warp CTAs per SM is
+// the fastest or within 1% of it on rows of 16 KB to 256 KB (8192 x 32000
+// bf16 107 -> 81 us against the split kernel, 4096 x 128256 bf16 169 -> 151
+// against the two-pass kernel, 16384 x 16000 bf16 123 -> 80 against the
+// swept warp kernel), but a row that leaves its last step mostly empty wastes
+// that step's issue slots: 12 KB fp32 and 18 KB bf16 rows ran 8% faster on
+// the build of 4 vectors per lane (2 KB per step, five CTAs per SM).  So the
+// 8 KB build is taken when the row fills at least 90% of its steps, else the
+// 2 KB one.  Rows are dealt to warps round-robin; the grid has just enough
+// warps that each takes the same number of rows, ceil(B / w) with w the
+// resident warps, so no warp has a row more than the others.
+// `build_forced`: 0 = choose, else build_forced - 1.
+int online_build_for(long long row_bytes) {
+    constexpr long long kStepBytes = 32LL * 16 * 16;  // build 3: 16 vectors per lane
+    const long long steps = (row_bytes + kStepBytes - 1) / kStepBytes;
+    return row_bytes * 10 >= steps * kStepBytes * 9 ? 3 : 4;
+}
+
+int plan_online(long long B, long long row_bytes, const DeviceInfo &d, int dtype, int build_forced,
+                Plan *pl) {
+    const int build = build_forced > 0 ? build_forced - 1 : online_build_for(row_bytes);
+    if (build >= ce::kOnlineBuilds) return CE_ERR_PATH;
+    int per_sm = 0;
+    int rc = cached_occupancy(
+        dtype, CE_PATH_ROWS_ONLINE, build, 0,
+        [&](int *v) { return ce::rows_online_max_ctas_per_sm(dtype, build, v); }, &per_sm);
+    if (rc != CE_OK) return rc;
+    if (per_sm < 1) return CE_ERR_PATH;
+    const long long resident = (long long)per_sm * d.sms * ce::kOnlineWarps;
+    const long long rows_per_warp = (B + resident - 1) / resident;
+    const long long warps = (B + rows_per_warp - 1) / rows_per_warp;
+    pl->path = CE_PATH_ROWS_ONLINE;
+    pl->split = build + 1;
+    pl->ctas = (int)((warps + ce::kOnlineWarps - 1) / ce::kOnlineWarps);
+    pl->threads = ce::kOnlineWarps * 32;
+    pl->smem = 0;
+    pl->launches = 1;
+    pl->online_build = build;
+    return CE_OK;
+}
+
 int plan_stream(long long B, long long C, Plan *pl) {
     const long long chunks = (C + ce::kStreamChunk - 1) / ce::kStreamChunk;
     if (B * chunks > 0x7fffffffLL) return CE_ERR_SHAPE;
@@ -471,12 +518,17 @@ cudaError_t launch_plan(const ce::ParamsEx &p, int dtype, const Plan &pl, cudaSt
             return launch_split_plan(p, dtype, pl, s);
         case CE_PATH_ROW_TWOPASS:
             return ce::launch_twopass(p, dtype, pl.ctas, pl.nslots, pl.smem, twopass_hint(), s);
+        case CE_PATH_ROWS_ONLINE:
+            return ce::launch_rows_online(p, dtype, pl.online_build, pl.ctas, s);
         default:
             return ce::launch_stream(p, dtype, pl.chunks, s);
     }
 }
 
-int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl) {
+// loss_only: no gradient and no softmax output is written (the call's
+// grad_out is NULL).
+int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl,
+              bool loss_only = false) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -492,8 +544,12 @@ int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl
             // rows one CTA holds in registers: the split kernel at K = 1;
             // longer rows: two passes through one CTA (measured faster on
             // GB300 than splitting a row across a cluster or the streaming
-            // path)
+            // path); the loss alone, on rows past 8 KB in batches of at least
+            // 8 rows per SM: a warp per row, read once (at 4 rows per SM the
+            // other kernels were faster: 11.0 against 13.5 us on 32000 bf16)
             if (row_bytes <= kWarpRowMax) return plan_warp(B, C, es, d, dtype, pl);
+            if (loss_only && B >= kOnlineMinRowsPerSm * (long long)d.sms)
+                return plan_online(B, row_bytes, d, dtype, 0, pl);
             rc = plan_warp_swept(B, C, es, d, dtype, false, pl);
             if (rc != CE_ERR_PATH) return rc;
             rc = plan_split(B, C, es, d, dtype, 0, pl);
@@ -508,6 +564,9 @@ int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl
             if (split != 0 && split != ce::kStreamChunk) return CE_ERR_PATH;
             return plan_stream(B, C, pl);
         case CE_PATH_ROW_TWOPASS: return plan_twopass(B, d, dtype, pl);
+        case CE_PATH_ROWS_ONLINE:
+            if (!loss_only) return CE_ERR_PATH;
+            return plan_online(B, row_bytes, d, dtype, split, pl);
         default: return CE_ERR_PATH;
     }
 }
@@ -670,10 +729,11 @@ int run(const void *logits, const int32_t *targets, int64_t B, int64_t C, int dt
     }
 
     Plan pl;
-    if ((rc = make_plan(B, C, dtype, path, split, &pl)) != CE_OK) return rc;
+    if ((rc = make_plan(B, C, dtype, path, split, &pl, !softmax && !grad_out)) != CE_OK) return rc;
     const bool hooked = hooks && (hooks->skip_copy_row >= 0 || hooks->wait_limit_cycles > 0 ||
                                   hooks->grad_f32_out);
-    if (hooked && pl.path == CE_PATH_STREAM) return CE_ERR_PATH;  // stages nothing
+    if (hooked && (pl.path == CE_PATH_STREAM || pl.path == CE_PATH_ROWS_ONLINE))
+        return CE_ERR_PATH;  // stage nothing
 
     const size_t rows_bytes = align_up((size_t)B, 1024) * sizeof(float);
     size_t need = kHeaderBytes + rows_bytes;

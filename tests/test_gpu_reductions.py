@@ -96,8 +96,12 @@ def test_reductions_on_every_path(path, split, B, C, dtype, reduction, with_grad
 
 
 def test_loss_only_matches_the_full_call_bitwise():
-    """ce_forward, ce_fwd_bwd_ex without a gradient and the full call give the
-    same loss bits (same row arithmetic, same fixed-order sum)."""
+    """Where the loss alone runs the full call's kernel (rows of at most 8 KB,
+    or batches of fewer than 8 rows per SM), ce_forward, ce_fwd_bwd_ex
+    without a gradient and the full call give the same loss bits (same row
+    arithmetic, same fixed-order sum).  Larger loss-only batches take the
+    online kernel, whose sums are formed in another order
+    (test_gpu_online.py)."""
     for B, C, dtype in [(512, 3000, "f32"), (64, 32000, "bf16"), (24, 128256, "bf16")]:
         inp = wl.random_case(B, C, dtype, seed=4)
         z, t = device_inputs(inp)
@@ -111,9 +115,10 @@ def test_loss_only_matches_the_full_call_bitwise():
         assert l_fwd.item() == l_full.item() == l_none.item(), (B, C, dtype)
 
 
-@pytest.mark.parametrize("name", ["classifier_4096x1000_f32", "lm_head_8192x32000_bf16"])
+@pytest.mark.parametrize("name", ["classifier_4096x1000_f32", "lm_head_8192x32000_bf16",
+                                  "lm_head_4096x128256_bf16_peaked", "stress_16384x50257_f32"])
 def test_full_size_loss_only_and_per_row(name):
-    """The headline workloads: the loss alone (mean) and the per-row losses."""
+    """The benchmark workloads: the loss alone (mean) and every row's loss."""
     w = wl.WORKLOADS_BY_NAME[name]
     inp = wl.make_inputs(w)
     z, t = device_inputs(inp)
