@@ -241,6 +241,8 @@ int ce_fwd_bwd_host_grad(const void *logits_host, const int32_t *targets_host, i
  * ce_query_plan -- the launch that ce_fwd_bwd would make for this shape on
  * the current device (path, split, total CTAs, threads per CTA, dynamic shared
  * memory per CTA, kernel launches per call).  Any output pointer may be NULL.
+ * The loss alone (grad_out NULL) runs the same launch except on rows past
+ * 8 KB in batches of at least 8 rows per SM, which take CE_PATH_ROWS_ONLINE.
  */
 int ce_query_plan(int64_t B, int64_t C, int dtype, int *path, int *split, int *ctas,
                   int *threads, int *smem_bytes, int *launches);
