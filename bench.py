@@ -83,22 +83,27 @@ KERNEL_SOURCES = {"rows_warp": "ce_rows_warp.cu", "row_split": "ce_row_split.cu"
 PLAN_KEYS = ("path", "split", "ctas", "threads", "smem_bytes")
 
 
-def source_hash(kernel: str | None = None) -> str:
-    """Hash of a kernel's device sources (its file, a header of the same name
-    if it has one, and the shared headers), or of every csrc file but the
-    host-only ones when no kernel is named."""
-    csrc = os.path.join(ROOT, "softmax_cross_entropy_row_gb300", "csrc")
+CSRC = os.path.join(ROOT, "softmax_cross_entropy_row_gb300", "csrc")
+
+
+def kernel_source_names(kernel: str | None = None) -> list[str]:
+    """The csrc files a kernel's device code comes from: its file, a header of
+    the same name if it has one, and the shared headers; every csrc file but
+    the host-only ones when no kernel is named."""
     if kernel is None:
-        names = sorted(os.path.basename(p) for p in glob.glob(os.path.join(csrc, "*"))
-                       if os.path.basename(p) not in HOST_ONLY_SOURCES)
-    else:
-        own = KERNEL_SOURCES[kernel]
-        header = os.path.splitext(own)[0] + ".h"
-        names = sorted((own,) + SHARED_DEVICE_SOURCES
-                       + ((header,) if os.path.exists(os.path.join(csrc, header)) else ()))
+        return sorted(os.path.basename(p) for p in glob.glob(os.path.join(CSRC, "*"))
+                      if os.path.basename(p) not in HOST_ONLY_SOURCES)
+    own = KERNEL_SOURCES[kernel]
+    header = os.path.splitext(own)[0] + ".h"
+    return sorted((own,) + SHARED_DEVICE_SOURCES
+                  + ((header,) if os.path.exists(os.path.join(CSRC, header)) else ()))
+
+
+def source_hash(kernel: str | None = None) -> str:
+    """Hash of the files kernel_source_names lists (names and contents)."""
     h = hashlib.sha256()
-    for name in names:
-        with open(os.path.join(csrc, name), "rb") as f:
+    for name in kernel_source_names(kernel):
+        with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -52,6 +52,14 @@ def test_device_code_hashes_ignore_the_host_layer():
     assert len(bench.source_hash()) == 16
     hashes = {k: bench.source_hash(k) for k in bench.KERNEL_SOURCES}
     assert len(set(hashes.values())) == len(hashes)
+    # a kernel with an interface header of its own hashes it too (its
+    # constants shape the kernel); the others hash their file and the shared
+    # headers alone
+    assert bench.kernel_source_names("rows_online") == sorted(
+        ["ce_rows_online.cu", "ce_rows_online.h"] + list(bench.SHARED_DEVICE_SOURCES))
+    assert bench.kernel_source_names("rows_warp") == sorted(
+        ["ce_rows_warp.cu"] + list(bench.SHARED_DEVICE_SOURCES))
+    assert "ce_api.cu" not in bench.kernel_source_names()
 
 
 @pytest.mark.parametrize("name", ["classifier_4096x1000_f32", "lm_head_8192x32000_bf16",
