@@ -36,6 +36,27 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"libce.so does not export {name}"
 
 
+def _declared_constants(header=HEADER):
+    text = re.sub(r"/\*.*?\*/", "", open(header).read(), flags=re.S)
+    return {n: int(v) for n, v in re.findall(r"\b(CE_[A-Z0-9_]+)\s*=\s*(-?\d+)", text)}
+
+
+def test_binding_constants_match_the_header():
+    """The binding passes the header's numbers: every dtype, reduction and
+    kernel path constant of ce.h has the same value in the Python module, and
+    every status has a message of its own."""
+    consts = _declared_constants()
+    mirrored = [n for n in consts if n.startswith(("CE_PATH_", "CE_REDUCE_"))
+                or n in ("CE_F32", "CE_BF16", "CE_F16")]
+    assert "CE_PATH_ROWS_ONLINE" in mirrored and len(mirrored) >= 12
+    for name in mirrored:
+        assert getattr(ce, name) == consts[name], name
+    lib = ce.load_library()
+    statuses = [v for n, v in consts.items() if n == "CE_OK" or n.startswith("CE_ERR_")]
+    messages = {lib.ce_status_string(v).decode() for v in statuses}
+    assert len(messages) == len(statuses)
+
+
 def test_test_header_declares_the_hooks():
     assert set(_declared_functions(TEST_HEADER)) == set(ce.TEST_EXPORTS)
 
