@@ -548,8 +548,10 @@ int make_plan(long long B, long long C, int dtype, int path, int split, Plan *pl
             // 8 rows per SM: a warp per row, read once (at 4 rows per SM the
             // other kernels were faster: 11.0 against 13.5 us on 32000 bf16)
             if (row_bytes <= kWarpRowMax) return plan_warp(B, C, es, d, dtype, pl);
-            if (loss_only && B >= kOnlineMinRowsPerSm * (long long)d.sms)
-                return plan_online(B, row_bytes, d, dtype, 0, pl);
+            if (loss_only && B >= kOnlineMinRowsPerSm * (long long)d.sms) {
+                rc = plan_online(B, row_bytes, d, dtype, 0, pl);
+                if (rc != CE_ERR_PATH) return rc;
+            }
             rc = plan_warp_swept(B, C, es, d, dtype, false, pl);
             if (rc != CE_ERR_PATH) return rc;
             rc = plan_split(B, C, es, d, dtype, 0, pl);
